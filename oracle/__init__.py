@@ -1,0 +1,195 @@
+"""CPU oracle for the fused residual-add + RMSNorm + quantisation op (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by the
+benchmark's CPU-baseline / reference leg, never by the library.  The C source
+(``rmsq_oracle.c``) holds the definition and the passages it follows; it shares
+no code with the CUDA path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rmsq_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle_rmsq.so")
+
+# The oracle's own names for the quantisation modes and activation types.
+MODES = {
+    "fp8_static": 0,
+    "fp8_per_token": 1,
+    "fp8_group128_row": 2,
+    "fp8_group128_col": 3,
+    "fp8_group64_row": 4,
+    "fp8_group64_col": 5,
+    "nvfp4": 6,
+}
+DTYPES = {"bf16": 0, "fp16": 1}
+GROUP = {"fp8_group128_row": 128, "fp8_group128_col": 128,
+         "fp8_group64_row": 64, "fp8_group64_col": 64}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def compile_oracle(force: bool = False) -> str:
+    """gcc -O2 -ffp-contract=off, no fast-math: binary32 RNE, no contraction."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(compile_oracle())
+            f32, u8, u16, i64, vp = (ctypes.c_float, ctypes.c_uint8, ctypes.c_uint16,
+                                     ctypes.c_int64, ctypes.c_void_p)
+            L.oracle_bf16_to_float.argtypes, L.oracle_bf16_to_float.restype = [u16], f32
+            L.oracle_fp16_to_float.argtypes, L.oracle_fp16_to_float.restype = [u16], f32
+            L.oracle_float_to_bf16.argtypes, L.oracle_float_to_bf16.restype = [f32], u16
+            L.oracle_float_to_fp16.argtypes, L.oracle_float_to_fp16.restype = [f32], u16
+            L.oracle_e4m3_encode.argtypes, L.oracle_e4m3_encode.restype = [f32], u8
+            L.oracle_e4m3_decode.argtypes, L.oracle_e4m3_decode.restype = [u8], f32
+            L.oracle_e2m1_encode.argtypes, L.oracle_e2m1_encode.restype = [f32], u8
+            L.oracle_e2m1_decode.argtypes, L.oracle_e2m1_decode.restype = [u8], f32
+            L.oracle_tree_sum.argtypes, L.oracle_tree_sum.restype = [vp, i64], f32
+            for name in ("oracle_e4m3_encode_array", "oracle_e2m1_encode_array",
+                         "oracle_float_to_bf16_array", "oracle_float_to_fp16_array"):
+                getattr(L, name).argtypes = [vp, vp, i64]
+                getattr(L, name).restype = None
+            L.oracle_fused_add_rmsnorm_quant.argtypes = [
+                vp, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int,
+                ctypes.c_int]
+            L.oracle_fused_add_rmsnorm_quant.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    v = _f32(v)
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_e4m3_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e2m1_encode(v) -> np.ndarray:
+    v = _f32(v)
+    out = np.empty(v.shape, np.uint8)
+    lib().oracle_e2m1_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    L = lib()
+    return np.array([L.oracle_e4m3_decode(int(c)) for c in np.ravel(codes)],
+                    np.float32).reshape(np.shape(codes))
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    L = lib()
+    return np.array([L.oracle_e2m1_decode(int(c)) for c in np.ravel(codes)],
+                    np.float32).reshape(np.shape(codes))
+
+
+def float_to_act(v, dtype: str) -> np.ndarray:
+    v = _f32(v)
+    out = np.empty(v.shape, np.uint16)
+    fn = lib().oracle_float_to_bf16_array if dtype == "bf16" else lib().oracle_float_to_fp16_array
+    fn(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def act_to_float(bits, dtype: str) -> np.ndarray:
+    L = lib()
+    fn = L.oracle_bf16_to_float if dtype == "bf16" else L.oracle_fp16_to_float
+    return np.array([fn(int(b)) for b in np.ravel(bits)], np.float32).reshape(np.shape(bits))
+
+
+def tree_sum(v) -> float:
+    v = _f32(v)
+    return float(lib().oracle_tree_sum(_ptr(v), v.size))
+
+
+def scale_shape(mode: str, n: int, H: int):
+    """Shape and dtype of the scale output of ``mode`` for an [n, H] input."""
+    if mode == "fp8_static":
+        return None
+    if mode == "fp8_per_token":
+        return (n,), np.float32
+    if mode == "nvfp4":
+        return (n, H // 16), np.uint8
+    G = GROUP[mode]
+    if mode.endswith("_col"):
+        return (H // G, n), np.float32
+    return (n, H // G), np.float32
+
+
+def run(x, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
+        dtype: str = "bf16", want_y: bool = False, nthreads: int = 1) -> dict:
+    """Run the oracle on host bit patterns (uint16 [n, H], [n, H] or None, [H]).
+
+    Returns a dict with ``q`` (uint8 [n, H] for FP8, [n, H/2] for NVFP4),
+    ``scales`` (None for FP8 static), ``residual_out`` (None without a
+    residual) and, when ``want_y``, the fp32 ``y`` [n, H].
+    """
+    x = np.ascontiguousarray(x, np.uint16)
+    n, H = x.shape
+    weight = np.ascontiguousarray(weight, np.uint16)
+    assert weight.shape == (H,)
+    res = None if residual is None else np.ascontiguousarray(residual, np.uint16)
+    q = np.zeros((n, H // 2) if mode == "nvfp4" else (n, H), np.uint8)
+    ss = scale_shape(mode, n, H)
+    scales = None if ss is None else np.zeros(ss[0], ss[1])
+    res_out = None if res is None else np.zeros((n, H), np.uint16)
+    y = np.zeros((n, H), np.float32) if want_y else None
+    rc = lib().oracle_fused_add_rmsnorm_quant(
+        _ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), MODES[mode],
+        ctypes.c_float(scale_in), _ptr(q), _ptr(scales), _ptr(res_out), _ptr(y),
+        n, H, DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": scales, "residual_out": res_out, "y": y}
+
+
+def nvfp4_global_scale(y_amax: float) -> float:
+    """gs = 448 * 6 / amax(all y), as the NVFP4 workload defines it (fp32 division)."""
+    return float(np.float32(2688.0) / np.float32(y_amax))
+
+
+def run_workload(wl, mode: str, *, scale_in: float | None = None, want_y: bool = False,
+                 nthreads: int = 1) -> dict:
+    """Run a ``rmsq_inputs.Workload``.  For NVFP4 without an explicit scale_in,
+    a first pass computes y and sets gs = 2688 / amax(all y)."""
+    if mode == "fp8_static" and scale_in is None:
+        scale_in = wl.static_scale
+    out = None
+    if mode == "nvfp4" and scale_in is None:
+        pre = run(wl.x, wl.residual, wl.weight, eps=wl.eps, mode="fp8_per_token",
+                  dtype=wl.dtype, want_y=True, nthreads=nthreads)
+        scale_in = nvfp4_global_scale(float(np.max(np.abs(pre["y"]))))
+        if want_y:
+            out = pre["y"]
+    r = run(wl.x, wl.residual, wl.weight, eps=wl.eps, mode=mode, scale_in=scale_in or 0.0,
+            dtype=wl.dtype, want_y=want_y and out is None, nthreads=nthreads)
+    if out is not None:
+        r["y"] = out
+    r["scale_in"] = scale_in
+    return r

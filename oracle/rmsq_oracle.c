@@ -1,0 +1,401 @@
+/*
+ * CPU oracle for the fused residual-add + RMSNorm + activation quantisation op.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain, obviously-correct
+ * statement of what the op computes.  Only the tests, the smoke check and the
+ * benchmark's CPU-baseline / reference leg load it.  It shares no code, header,
+ * table or constant with the CUDA library, and the CUDA library never calls it.
+ *
+ * What it follows:
+ *  - vLLM docs, "Fusion torch.compile passes", section "RMSNorm + Quantization
+ *    (fuse_norm_quant)": rms_norm(x) -> quant_fp8(y) and
+ *    fused_add_rms_norm(x, residual) -> quant_fp8(y), the residual updated in
+ *    place; schemes FP8 static per-tensor, FP8 dynamic per-token, FP8 dynamic
+ *    per-token-group (128/64).
+ *  - blog "[vLLM] Compilation Fusion Passes", sections "RMSNormQuantFusionPass"
+ *    (eps 1e-5 / 1e-6), "Pattern matching structure" (result/input/weight/scale/
+ *    epsilon), "Fused Add + RMSNorm + Group Quantization" (the FUSED_OPS keys:
+ *    static tensor, dynamic token, dynamic 128-group, symmetric), "Why this
+ *    design" (column-major scales).
+ *  - vLLM PR #51925 summary (prhub), "Motivation" and "Key source snippets":
+ *    residual update + RMSNorm, then block scales and conversion to FP4 with an
+ *    fp32 activation (global) scale passed in.
+ * The pages print no formula; the scale rules (amax/448 floored at 1e-12,
+ * block scale e4m3(amax/6 * gs), gs = 448*6/amax) and the saturation rules are
+ * the workload definitions that go with the pages' workloads.
+ *
+ * Arithmetic: IEEE-754 binary32, round-to-nearest-even, no FMA contraction
+ * (built with -ffp-contract=off), subnormals kept.  Every step runs in the
+ * order written below.  Readings of points the pages leave open:
+ *  R1 RMSNorm normalises the T-rounded h (= residual_out), not the fp32 sum.
+ *  R2 y stays fp32 (not rounded to T) before quantisation.
+ *  R3 sum of squares: canonical pairwise tree (zero-pad to a power of two,
+ *     add adjacent pairs level by level).
+ *  R4 q = e4m3(y / s) with a correctly rounded fp32 division.
+ *  R5 group scales are floored at 1e-12 like per-token scales.
+ *  R6 NVFP4 global scale gs is an input; r = gs / decode(block scale) per
+ *     block (0 when the block scale is 0); q = e2m1(y * r).
+ *  R7 E2M1 nibble order: element 2j in the low nibble of byte j.
+ *  R8 column-major group scales use stride n_tokens.
+ *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_BF16 = 0, OR_FP16 = 1 };
+enum {
+    OR_FP8_STATIC = 0,
+    OR_FP8_PER_TOKEN = 1,
+    OR_FP8_G128_ROW = 2,
+    OR_FP8_G128_COL = 3,
+    OR_FP8_G64_ROW = 4,
+    OR_FP8_G64_COL = 5,
+    OR_NVFP4 = 6
+};
+
+/* ------------------------------------------------------------------------ */
+/* Number formats, from their definitions.                                  */
+/* ------------------------------------------------------------------------ */
+
+static float bits_to_float(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t float_to_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+
+/* bf16 is the upper half of a binary32: widening is exact. */
+float oracle_bf16_to_float(uint16_t b) { return bits_to_float((uint32_t)b << 16); }
+
+/* binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+float oracle_fp16_to_float(uint16_t b)
+{
+    int sign = b >> 15, e = (b >> 10) & 0x1f, m = b & 0x3ff;
+    float v;
+    if (e == 0)
+        v = ldexpf((float)m, -24);                  /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(1024 + m), e - 25);      /* (1 + m/1024) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* binary32 -> bf16, round to nearest, ties to even on the 16 dropped bits. */
+uint16_t oracle_float_to_bf16(float f)
+{
+    uint32_t u = float_to_bits(f);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+    uint32_t upper = u >> 16, lower = u & 0xffffu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1; /* carry may reach inf */
+    return (uint16_t)upper;
+}
+
+/* binary32 -> binary16, round to nearest even; overflow to +-inf. */
+uint16_t oracle_float_to_fp16(float f)
+{
+    uint16_t sign = (uint16_t)(signbit(f) ? 0x8000 : 0);
+    float a = fabsf(f);
+    if (isnan(f)) return (uint16_t)(sign | 0x7e00);
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7c00);   /* halfway 65504..65536 ties up to inf */
+    if (a < ldexpf(1.0f, -14)) {                           /* subnormal range, step 2^-24 */
+        float k = rintf(ldexpf(a, 24));                    /* exact scaling, RNE */
+        return (uint16_t)(sign | (uint16_t)k);            /* k == 1024 is the smallest normal */
+    }
+    int ex;
+    frexpf(a, &ex);                                        /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                                        /* a in [2^e, 2^(e+1)) */
+    float k = rintf(ldexpf(a, 10 - e));                    /* significand * 1024 in [1024, 2048] */
+    if (k == 2048.0f) { k = 1024.0f; e += 1; }
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)((int)k - 1024));
+}
+
+/* OCP FP8 E4M3 (E4M3FN): bias 7, 3 fraction bits, no infinities, 0x7f/0xff
+ * NaN, max 448, subnormals k * 2^-9.  Round to nearest even, saturate finite
+ * and infinite magnitudes above 448 to 448, NaN -> 0x7f, sign always kept. */
+uint8_t oracle_e4m3_encode(float v)
+{
+    if (isnan(v)) return 0x7f;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    float a = fabsf(v);
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7e);
+    if (a < ldexpf(1.0f, -6)) {                            /* subnormal range, step 2^-9 */
+        float k = rintf(ldexpf(a, 9));                     /* 0..8; 8 is the smallest normal */
+        return (uint8_t)(sign | (uint8_t)k);
+    }
+    int ex;
+    frexpf(a, &ex);
+    int e = ex - 1;
+    float k = rintf(ldexpf(a, 3 - e));                     /* in [8, 16] */
+    if (k == 16.0f) { k = 8.0f; e += 1; }
+    int code = ((e + 7) << 3) | ((int)k - 8);
+    if (code > 0x7e) code = 0x7e;
+    return (uint8_t)(sign | code);
+}
+
+float oracle_e4m3_decode(uint8_t c)
+{
+    int sign = c >> 7, e = (c >> 3) & 0xf, m = c & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexpf((float)m, -9);
+    else v = ldexpf((float)(8 + m), e - 10);               /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* FP4 E2M1: bias 1, 1 fraction bit: {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  Round to
+ * nearest even, saturate to 6, sign always kept (-0 -> 0x8). */
+uint8_t oracle_e2m1_encode(float v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    float a = fabsf(v);
+    if (isnan(v)) return 0x7;      /* not reached by the tests (NaN is out of scope) */
+    if (a >= 6.0f) return (uint8_t)(sign | 0x7);
+    if (a < 1.0f) {                                        /* subnormal range, step 0.5 */
+        float k = rintf(a * 2.0f);                         /* 0, 1, 2; 2 is 1.0 */
+        return (uint8_t)(sign | (uint8_t)k);
+    }
+    int ex;
+    frexpf(a, &ex);
+    int e = ex - 1;                                        /* 0, 1 or 2 */
+    float k = rintf(ldexpf(a, 1 - e));                     /* in [2, 4] */
+    if (k == 4.0f) { k = 2.0f; e += 1; }
+    int code = ((e + 1) << 1) | ((int)k - 2);
+    if (code > 7) code = 7;
+    return (uint8_t)(sign | code);
+}
+
+float oracle_e2m1_decode(uint8_t c)
+{
+    int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    float v = (e == 0) ? 0.5f * (float)m : ldexpf((float)(2 + m), e - 2);
+    return sign ? -v : v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Canonical pairwise sum (reading R3).                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Zero-pad v[0..n) to P = next power of two >= n, then replace the sequence by
+ * the sums of adjacent pairs (v[2k] + v[2k+1]) until one value is left.
+ * buf must hold P floats. */
+float oracle_tree_sum_buf(const float *v, int64_t n, float *buf)
+{
+    if (n <= 0) return 0.0f;
+    int64_t P = 1;
+    while (P < n) P <<= 1;
+    for (int64_t i = 0; i < P; ++i) buf[i] = (i < n) ? v[i] : 0.0f;
+    for (int64_t len = P; len > 1; len >>= 1)
+        for (int64_t k = 0; k < len / 2; ++k) buf[k] = buf[2 * k] + buf[2 * k + 1];
+    return buf[0];
+}
+
+float oracle_tree_sum(const float *v, int64_t n)
+{
+    int64_t P = 1;
+    while (P < n) P <<= 1;
+    float *buf = (float *)malloc((size_t)P * sizeof(float));
+    float s = oracle_tree_sum_buf(v, n, buf);
+    free(buf);
+    return s;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The op, one row at a time.                                               */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t *x, *residual, *weight;
+    float eps;
+    int mode;
+    float scale_in;          /* FP8 static: s;  NVFP4: global scale gs */
+    uint8_t *out_q;
+    void *out_scales;
+    uint16_t *residual_out;
+    float *y_out;            /* optional fp32 copy of y [n, H] for diagnostics */
+    int64_t n, H;
+    int dtype;
+} OracleArgs;
+
+typedef struct {
+    float *h, *sq, *y, *buf;
+} RowScratch;
+
+static float widen(int dtype, uint16_t b)
+{
+    return dtype == OR_BF16 ? oracle_bf16_to_float(b) : oracle_fp16_to_float(b);
+}
+
+static uint16_t narrow(int dtype, float f)
+{
+    return dtype == OR_BF16 ? oracle_float_to_bf16(f) : oracle_float_to_fp16(f);
+}
+
+static int group_size(int mode)
+{
+    switch (mode) {
+    case OR_FP8_G128_ROW: case OR_FP8_G128_COL: return 128;
+    case OR_FP8_G64_ROW: case OR_FP8_G64_COL: return 64;
+    default: return 0;
+    }
+}
+
+static void oracle_row(const OracleArgs *a, int64_t t, RowScratch *s)
+{
+    const int64_t H = a->H;
+    const uint16_t *xr = a->x + t * H;
+
+    /* Step 1: residual add, h rounded to the activation type and written back
+     * as the updated residual (R1); without a residual, h = x. */
+    for (int64_t i = 0; i < H; ++i) {
+        if (a->residual) {
+            float sum = widen(a->dtype, xr[i]) + widen(a->dtype, a->residual[t * H + i]);
+            uint16_t hb = narrow(a->dtype, sum);
+            a->residual_out[t * H + i] = hb;
+            s->h[i] = widen(a->dtype, hb);
+        } else {
+            s->h[i] = widen(a->dtype, xr[i]);
+        }
+    }
+
+    /* Step 2: sum of squares by the canonical tree (R3). */
+    for (int64_t i = 0; i < H; ++i) s->sq[i] = s->h[i] * s->h[i];
+    float S = oracle_tree_sum_buf(s->sq, H, s->buf);
+
+    /* Step 3: mean square and reciprocal RMS, each correctly rounded. */
+    float ms = S / (float)H;
+    float inv = 1.0f / sqrtf(ms + a->eps);
+
+    /* Step 4: y = (h * inv) * w, kept in fp32 (R2). */
+    for (int64_t i = 0; i < H; ++i)
+        s->y[i] = (s->h[i] * inv) * widen(a->dtype, a->weight[i]);
+    if (a->y_out) memcpy(a->y_out + t * H, s->y, (size_t)H * sizeof(float));
+
+    /* Step 5: quantisation. */
+    uint8_t *q = a->out_q;
+    if (a->mode == OR_FP8_STATIC) {
+        float sc = a->scale_in;
+        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(s->y[i] / sc);
+    } else if (a->mode == OR_FP8_PER_TOKEN) {
+        float amax = 0.0f;
+        for (int64_t i = 0; i < H; ++i) amax = fmaxf(amax, fabsf(s->y[i]));
+        float sc = fmaxf(amax / 448.0f, 1e-12f);
+        ((float *)a->out_scales)[t] = sc;
+        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(s->y[i] / sc);
+    } else if (a->mode == OR_NVFP4) {
+        float gs = a->scale_in;
+        uint8_t *bs = (uint8_t *)a->out_scales;
+        for (int64_t b = 0; b < H / 16; ++b) {
+            const float *yb = s->y + 16 * b;
+            float amax = 0.0f;
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(yb[k]));
+            uint8_t sb = oracle_e4m3_encode((amax / 6.0f) * gs);
+            bs[t * (H / 16) + b] = sb;
+            float d = oracle_e4m3_decode(sb);
+            float r = (d == 0.0f) ? 0.0f : gs / d;
+            for (int k = 0; k < 16; k += 2) {
+                uint8_t lo = oracle_e2m1_encode(yb[k] * r);
+                uint8_t hi = oracle_e2m1_encode(yb[k + 1] * r);
+                q[t * (H / 2) + 8 * b + k / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    } else {
+        int G = group_size(a->mode);
+        int col = (a->mode == OR_FP8_G128_COL || a->mode == OR_FP8_G64_COL);
+        float *sc_out = (float *)a->out_scales;
+        for (int64_t g = 0; g < H / G; ++g) {
+            const float *yg = s->y + G * g;
+            float amax = 0.0f;
+            for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));
+            float sc = fmaxf(amax / 448.0f, 1e-12f);
+            if (col) sc_out[g * a->n + t] = sc;
+            else sc_out[t * (H / G) + g] = sc;
+            for (int k = 0; k < G; ++k) q[t * H + G * g + k] = oracle_e4m3_encode(yg[k] / sc);
+        }
+    }
+}
+
+typedef struct {
+    const OracleArgs *a;
+    int64_t r0, r1;
+    int ok;
+} Span;
+
+static void *run_span(void *p)
+{
+    Span *sp = (Span *)p;
+    int64_t H = sp->a->H, P = 1;
+    while (P < H) P <<= 1;
+    RowScratch s;
+    s.h = (float *)malloc((size_t)H * sizeof(float));
+    s.sq = (float *)malloc((size_t)H * sizeof(float));
+    s.y = (float *)malloc((size_t)H * sizeof(float));
+    s.buf = (float *)malloc((size_t)P * sizeof(float));
+    sp->ok = s.h && s.sq && s.y && s.buf;
+    if (sp->ok)
+        for (int64_t t = sp->r0; t < sp->r1; ++t) oracle_row(sp->a, t, &s);
+    free(s.h); free(s.sq); free(s.y); free(s.buf);
+    return NULL;
+}
+
+/* Whole tensor.  Rows are independent, so splitting them over threads gives
+ * bit-identical results for any thread count.  Returns 0 on success,
+ * -1 on a bad argument, -2 on an allocation or thread failure. */
+int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
+                                   const uint16_t *weight, float eps, int mode, float scale_in,
+                                   uint8_t *out_q, void *out_scales, uint16_t *residual_out,
+                                   float *y_out, int64_t n, int64_t H, int dtype, int nthreads)
+{
+    if (n < 0 || H <= 0 || mode < 0 || mode > 6 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    if (!x || !weight || !out_q || (residual && !residual_out)) return -1;
+    if (mode != OR_FP8_STATIC && !out_scales) return -1;
+    if (mode == OR_NVFP4 && H % 16) return -1;
+    if (group_size(mode) && H % group_size(mode)) return -1;
+    OracleArgs a = {x, residual, weight, eps, mode, scale_in, out_q, out_scales,
+                    residual_out, y_out, n, H, dtype};
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+    Span *spans = (Span *)calloc((size_t)nthreads, sizeof(Span));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!spans || !th) { free(spans); free(th); return -2; }
+    int rc = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        spans[i].a = &a;
+        spans[i].r0 = n * i / nthreads;
+        spans[i].r1 = n * (i + 1) / nthreads;
+    }
+    if (nthreads == 1) {
+        run_span(&spans[0]);
+    } else {
+        int started = 0;
+        for (; started < nthreads; ++started)
+            if (pthread_create(&th[started], NULL, run_span, &spans[started])) break;
+        for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+        if (started < nthreads) rc = -2;
+    }
+    for (int i = 0; i < nthreads && !rc; ++i)
+        if (!spans[i].ok) rc = -2;
+    free(spans);
+    free(th);
+    return rc;
+}
+
+/* Array forms of the codecs, for exhaustive checks. */
+void oracle_e4m3_encode_array(const float *v, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(v[i]);
+}
+
+void oracle_e2m1_encode_array(const float *v, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(v[i]);
+}
+
+void oracle_float_to_bf16_array(const float *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_float_to_bf16(v[i]);
+}
+
+void oracle_float_to_fp16_array(const float *v, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_float_to_fp16(v[i]);
+}
