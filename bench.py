@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused residual-add + RMSNorm + quantisation path on GB300.
+
+One step = one launch of the fused kernel over the whole batch (all steps of
+the path: residual add, residual write-back, RMSNorm, scale, quantise, pack).
+Default workload: the Llama-8B-shaped layer, 4096 tokens x 4096 hidden bf16,
+residual add on, FP8 E4M3 dynamic per-token scales.
+
+Prints ONE JSON line (rank 0).  ``value`` is algorithmic HBM GB/s (bytes the
+op must move / device time), whole job over all ranks.  Inputs are resident in
+HBM before the timed region; consecutive steps rotate over buffer sets whose
+total size is more than 4x the L2 cache, so no step reads the previous step's
+data from L2.  ``e2e`` is the same metric with the inputs copied from pinned
+host memory and the outputs read back inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused add-RMSNorm+quant HBM GB/s and tokens/s on 1 GB300 vs ~8 TB/s peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- bytes
+def algorithmic_bytes(mode: str, n: int, H: int, es: int, residual: bool) -> int:
+    """Bytes the op must move for one launch over n rows of width H."""
+    per_tok = H * es                              # x
+    if residual:
+        per_tok += 2 * H * es                     # residual in, residual_out
+    per_tok += H // 2 if mode == "nvfp4" else H   # codes
+    if mode == "fp8_per_token":
+        per_tok += 4
+    elif mode.startswith("fp8_group"):
+        per_tok += 4 * H // (128 if "128" in mode else 64)
+    elif mode == "nvfp4":
+        per_tok += H // 16
+    fixed = H * es + (4 if mode in ("fp8_static", "nvfp4") else 0)   # weight, scale_in
+    return n * per_tok + fixed
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (host timestamped) of SM clock and throttle reasons."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int = 0, period_ms: int = 20):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside and self.samples:
+            mid = (t0 + t1) / 2
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+            note = "timed region shorter than the sampling period: nearest sample"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        reasons = set()
+        for p in inside:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), p[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][1]), "reasons": sorted(reasons),
+                "samples": len(inside), "note": note}
+
+
+# --------------------------------------------------------------------------- helpers
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_digest() -> str:
+    from residual_add_rmsnorm_rmsq_gb300 import _build
+    return _build.source_digest()
+
+
+def profiled_traffic(kernel_name: str, digest: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel_name)
+    if not e or e.get("source_digest") != digest:
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def workload_spec(name: str):
+    import rmsq_inputs as ri
+    specs = {
+        "llama_fp8_per_token": (lambda: ri.llama(4096, True), "fp8_per_token"),
+        "llama_fp8_per_token_nores": (lambda: ri.llama(4096, False), "fp8_per_token"),
+        "llama_fp8_static": (lambda: ri.llama(4096, True), "fp8_static"),
+        "dsv3_fp8_group128_row": (lambda: ri.dsv3(8192), "fp8_group128_row"),
+        "dsv3_fp8_group128_col": (lambda: ri.dsv3(8192), "fp8_group128_col"),
+        "dsv3_fp8_group64_row": (lambda: ri.dsv3(8192), "fp8_group64_row"),
+        "dsv3_fp8_group64_col": (lambda: ri.dsv3(8192), "fp8_group64_col"),
+        "qwen_nvfp4_4096": (lambda: ri.qwen_nvfp4(4096), "nvfp4"),
+        "qwen_nvfp4_16384": (lambda: ri.qwen_nvfp4(16384), "nvfp4"),
+    }
+    return specs[name]
+
+
+def gpu_scale_in(torch, rq, wl, mode, x, r, w):
+    """scale_in for the timed launches: the workload's static scale, or for
+    NVFP4 gs = 2688 / amax(y) with amax(y) taken from a per-token FP8 launch of
+    the library itself (amax(y) = 448 * max over rows of the row scale)."""
+    if mode == "fp8_static":
+        return torch.tensor([wl.static_scale or 0.1], dtype=torch.float32, device="cuda")
+    if mode != "nvfp4":
+        return None
+    _, sc, _ = rq.fused_add_rmsnorm_quant(x, r, w, wl.eps, "fp8_per_token")
+    amax = float(sc.max().item()) * 448.0
+    return torch.tensor([np.float32(2688.0) / np.float32(amax)], dtype=torch.float32, device="cuda")
+
+
+class Buffers:
+    """Rotating device buffer sets for one workload and mode."""
+
+    def __init__(self, torch, rq, wl, mode, min_total_bytes):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        n, H = wl.n_tokens, wl.hidden
+        self.es = 2
+        self.res = wl.residual is not None
+        self.bytes = algorithmic_bytes(mode, n, H, 2, self.res)
+        self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        x0 = torch.from_numpy(wl.x.view(np.int16)).view(tdt).cuda()
+        r0 = None if not self.res else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).cuda()
+        self.w = torch.from_numpy(wl.weight.view(np.int16)).view(tdt).cuda()
+        self.scale_in = gpu_scale_in(torch, rq, wl, mode, x0, r0, self.w)
+        self.x, self.r, self.ro, self.q, self.sc = [], [], [], [], []
+        for i in range(self.sets):
+            self.x.append(x0 if i == 0 else x0.clone())
+            if self.res:
+                self.r.append(r0 if i == 0 else r0.clone())
+                self.ro.append(torch.empty_like(r0))
+            else:
+                self.r.append(None)
+                self.ro.append(None)
+            self.q.append(torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device="cuda"))
+            self.sc.append(rq.scales_like(mode, n, H, "cuda"))
+
+
+def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
+    """Mean device time per launch (ms) over `steps` launches, CUDA events on `stream`."""
+    def launch(i):
+        k = i % bufs.sets
+        rq.fused_add_rmsnorm_quant(bufs.x[k], bufs.r[k], bufs.w, wl.eps, mode, bufs.scale_in,
+                                   out_q=bufs.q[k], out_scales=bufs.sc[k], residual_out=bufs.ro[k],
+                                   stream=stream)
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            launch(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            launch(warmup + i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
+    """Same op through the public API with host buffers: pinned host -> device
+    copies of x and residual, the launch, device -> pinned host copies of
+    codes, scales and residual_out, all inside the timed region."""
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    hx = torch.from_numpy(wl.x.view(np.int16)).view(tdt).pin_memory()
+    hr = None if wl.residual is None else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).pin_memory()
+    hq = torch.empty(bufs.q[0].shape, dtype=torch.uint8).pin_memory()
+    hs = None if bufs.sc[0] is None else torch.empty(bufs.sc[0].shape, dtype=bufs.sc[0].dtype).pin_memory()
+    hro = None if hr is None else torch.empty_like(hr).pin_memory()
+    h2d = hx.numel() * 2 + (0 if hr is None else hr.numel() * 2)
+    d2h = hq.numel() + (0 if hs is None else hs.numel() * hs.element_size()) + \
+        (0 if hro is None else hro.numel() * 2)
+
+    def step():
+        bufs.x[0].copy_(hx, non_blocking=True)
+        if hr is not None:
+            bufs.r[0].copy_(hr, non_blocking=True)
+        rq.fused_add_rmsnorm_quant(bufs.x[0], bufs.r[0], bufs.w, wl.eps, mode, bufs.scale_in,
+                                   out_q=bufs.q[0], out_scales=bufs.sc[0], residual_out=bufs.ro[0],
+                                   stream=stream)
+        hq.copy_(bufs.q[0], non_blocking=True)
+        if hs is not None:
+            hs.copy_(bufs.sc[0], non_blocking=True)
+        if hro is not None:
+            hro.copy_(bufs.ro[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline(wl, mode, budget_s: float = 20.0) -> dict:
+    """The oracle as it stands, row-parallel over the process's cores, on a
+    bounded prefix of the workload's rows; median of 3 runs."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    scale = wl.static_scale if mode == "fp8_static" else (1000.0 if mode == "nvfp4" else 0.0)
+    rows = min(wl.n_tokens, 256)
+    while True:
+        t = time.perf_counter()
+        oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
+                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+        dt = time.perf_counter() - t
+        if rows >= wl.n_tokens or dt * 3 * 4 > budget_s / 2:
+            break
+        rows = min(wl.n_tokens, rows * 4)
+    times = []
+    for _ in range(3):
+        t = time.perf_counter()
+        oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
+                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+        times.append(time.perf_counter() - t)
+    med = statistics.median(times)
+    nbytes = algorithmic_bytes(mode, rows, wl.hidden, 2, wl.residual is not None)
+    return {"value": round(nbytes / med / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "tokens_per_s": round(rows / med, 1),
+            "sample": f"first {rows} of {wl.n_tokens} rows, median of 3 runs, {cores} threads"}
+
+
+# --------------------------------------------------------------------------- arms
+def run_reference(args, rank, world):
+    """The oracle, timed on the host cores as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    mk, mode = workload_spec(args.workload)
+    wl = mk()
+    cores = len(os.sched_getaffinity(0))
+    scale = wl.static_scale if mode == "fp8_static" else (1000.0 if mode == "nvfp4" else 0.0)
+    # size the per-step sample so that warmup + steps fit in about a minute
+    probe = 64
+    t = time.perf_counter()
+    oracle.run(wl.x[:probe], None if wl.residual is None else wl.residual[:probe], wl.weight,
+               eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+    per_row = (time.perf_counter() - t) / probe
+    rows = int(max(8, min(wl.n_tokens, 60.0 / max(1, args.steps + args.warmup) / per_row)))
+
+    def step():
+        oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
+                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = algorithmic_bytes(mode, rows, wl.hidden, 2, wl.residual is not None)
+    value = nbytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "tokens_per_s": round(rows / dt, 1),
+        "config": {"workload": args.workload, "n_tokens": wl.n_tokens, "hidden": wl.hidden,
+                   "quant_mode": mode, "residual": wl.residual is not None,
+                   "step_sample_rows": rows, "l2": "host (CPU oracle)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {rows} of {wl.n_tokens} rows per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+    import residual_add_rmsnorm_rmsq_gb300 as rq
+    from residual_add_rmsnorm_rmsq_gb300 import _build
+    _build.build()
+    rq.load()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    stream = torch.cuda.Stream()
+
+    mk, mode = workload_spec(args.workload)
+    wl = mk()
+    bufs = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up, then the timed region (clocks sampled during it)
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) if rank == 0 else None
+    time_launches(torch, rq, wl, mode, bufs, 1, args.warmup, stream)
+    barrier()
+    t_wall0 = time.time()
+    ms = time_launches(torch, rq, wl, mode, bufs, args.steps, 0, stream)
+    t_wall1 = time.time()
+    barrier()
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    per_launch = bufs.bytes
+    value = per_launch * world / (ms / 1e3) / 1e9
+    tokens_s = wl.n_tokens * world / (ms / 1e3)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    achieved = per_launch / (ms / 1e3) / 1e9
+    digest = kernel_digest()
+    kname = f"rows_kernel<{wl.dtype},{mode},{'res' if bufs.res else 'nores'}>"
+    traffic = profiled_traffic(kname, digest)
+
+    e2e_ms, h2d, d2h = e2e_measure(torch, rq, wl, mode, bufs, min(args.steps, 50), stream)
+    e2e_val = per_launch * world / (e2e_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, shapes of the pages' workloads)",
+        "tokens_per_s": round(tokens_s, 1),
+        "config": {"workload": args.workload, "n_tokens": wl.n_tokens, "hidden": wl.hidden,
+                   "quant_mode": mode, "residual": bufs.res, "eps": wl.eps,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"rotating {bufs.sets} buffer sets ({bufs.sets * per_launch / 1e6:.0f} MB > 4x L2)",
+                   "bytes_per_step": per_launch},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "kernel": kname},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 6)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_sweep:
+        line["modes"] = sweep(torch, rq, stream, peak, args)
+    if not args.no_cpu and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, mode)
+    print(json.dumps(line), flush=True)
+
+
+def sweep(torch, rq, stream, peak, args):
+    """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of peak)."""
+    import rmsq_inputs as ri
+    out = {}
+    groups = [
+        (lambda: ri.llama(4096, True), ["llama_fp8_per_token", "llama_fp8_static"]),
+        (lambda: ri.llama(4096, False), ["llama_fp8_per_token_nores"]),
+        (lambda: ri.dsv3(8192), ["dsv3_fp8_group128_row", "dsv3_fp8_group128_col",
+                                 "dsv3_fp8_group64_row", "dsv3_fp8_group64_col"]),
+        (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096"]),
+        (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384"]),
+    ]
+    for make, names in groups:
+        wl = make()
+        for name in names:
+            mode = workload_spec(name)[1]
+            bufs = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
+            ms = time_launches(torch, rq, wl, mode, bufs, args.sweep_steps, 5, stream)
+            gbs = bufs.bytes / (ms / 1e3) / 1e9
+            out[name] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "tokens_per_s": round(wl.n_tokens / (ms / 1e3), 1), "bytes": bufs.bytes}
+            del bufs
+            torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama_fp8_per_token")
+    ap.add_argument("--sweep-steps", type=int, default=300)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

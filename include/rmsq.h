@@ -1,0 +1,164 @@
+/*
+ * librmsq — fused residual-add + RMSNorm + activation quantisation on GB300 (sm_103a).
+ *
+ * The operation is the one vLLM's RMSNorm + quantisation fusion puts in place
+ * of a separate (fused-add) RMSNorm kernel and a quantisation kernel:
+ *   vLLM docs, "Fusion torch.compile passes", section
+ *   "RMSNorm + Quantization (fuse_norm_quant)": rms_norm(x) -> quant_fp8(y) and
+ *   fused_add_rms_norm(x, residual) -> quant_fp8(y), the residual updated in
+ *   place; schemes FP8 static per-tensor, FP8 dynamic per-token and FP8
+ *   dynamic per-token-group (128/64);
+ *   blog "[vLLM] Compilation Fusion Passes", sections "Pattern matching
+ *   structure" (result, input, weight, scale, epsilon), "Fused Add + RMSNorm +
+ *   Group Quantization" (the fused-op table keyed by quant scheme and fused
+ *   add), "Type validation" (input and weight share one dtype) and "Why this
+ *   design" (column-major scales);
+ *   vLLM PR #51925 summary (prhub), "Motivation" and "Key source snippets":
+ *   residual update + RMSNorm followed by NVFP4 block scales and FP4 values,
+ *   with an fp32 activation (global) scale given as an input.
+ *
+ * Per row t of an [n_tokens, hidden] activation (T = bf16 or fp16):
+ *   h    = T(fp32(x) + fp32(residual))       (h = x when residual is NULL)
+ *   residual_out = h
+ *   S    = pairwise-tree sum of fp32(h)^2     (zero-pad to a power of two,
+ *                                              add adjacent pairs level by level)
+ *   inv  = 1 / sqrt(S / hidden + eps)         (IEEE division and square root)
+ *   y    = (fp32(h) * inv) * fp32(weight)     (fp32, not rounded to T)
+ *   then one of the quantisation modes below.  All fp32 arithmetic rounds to
+ *   nearest even; results are bit-identical to that definition.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" must be addressable by the current CUDA device
+ *     (cudaMalloc / torch CUDA tensors, or managed memory).  The caller owns
+ *     every buffer; the library allocates no device memory and keeps no
+ *     per-call state.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous with respect to the host and do not synchronise.
+ *   - Argument errors are reported synchronously, before any launch, and leave
+ *     every output untouched.  A failed launch returns RMSQ_ERR_CUDA; the CUDA
+ *     error code is then available from rmsq_last_cuda_error().
+ *   - Device code is built for sm_103a only; any other device gives
+ *     RMSQ_ERR_UNSUPPORTED_DEVICE and there is no CPU fallback.
+ */
+#ifndef RMSQ_H
+#define RMSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RMSQ_VERSION 10000        /* 1.0.0 */
+#define RMSQ_MAX_HIDDEN 16384
+
+typedef enum {
+    RMSQ_OK = 0,
+    RMSQ_ERR_INVALID_ARG = 1,        /* NULL where a pointer is required, bad enum, bad eps */
+    RMSQ_ERR_ALIGNMENT = 2,          /* a pointer misses the alignment stated below */
+    RMSQ_ERR_ALIAS = 3,              /* outputs overlap inputs other than as allowed */
+    RMSQ_ERR_UNSUPPORTED_SHAPE = 4,  /* hidden not a multiple of 8 / the group / 16, or too large */
+    RMSQ_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
+    RMSQ_ERR_NO_DEVICE = 6,          /* no CUDA device / driver */
+    RMSQ_ERR_CUDA = 7                /* a CUDA runtime call or launch failed */
+} rmsq_status;
+
+typedef enum { RMSQ_BF16 = 0, RMSQ_FP16 = 1 } rmsq_dtype;
+
+/*
+ * Quantisation modes (blog "[vLLM] Compilation Fusion Passes", section
+ * "Fused Add + RMSNorm + Group Quantization": static per-tensor, dynamic
+ * per-token and dynamic 128-group symmetric FP8; vLLM docs "Fusion
+ * torch.compile passes", fuse_norm_quant: group 128 or 64; PR #51925: NVFP4).
+ * E4M3 is OCP FP8 E4M3FN: round to nearest even, magnitudes above 448
+ * (including infinities) saturate to 448, sign kept (-0 -> 0x80).
+ *
+ *  RMSQ_FP8_STATIC        s = scale_in[0];                q = e4m3(y / s)
+ *  RMSQ_FP8_PER_TOKEN     s_t = max(amax_t(|y|) / 448, 1e-12), fp32 [n_tokens]
+ *  RMSQ_FP8_GROUP{128,64}_ROW  s_{t,g} over G contiguous elements, fp32 [n_tokens, hidden/G]
+ *  RMSQ_FP8_GROUP{128,64}_COL  same values stored [hidden/G, n_tokens] (column-major)
+ *                         q = e4m3(y / s), one byte per element, [n_tokens, hidden]
+ *  RMSQ_NVFP4             per 16-element block b: sb = e4m3((amax_b / 6) * gs),
+ *                         gs = scale_in[0]; d = decode(sb); r = d ? gs / d : 0;
+ *                         q = e2m1(y * r) (values {0,.5,1,1.5,2,3,4,6}, round to
+ *                         nearest even, saturate at 6, sign kept); element 2j in
+ *                         the low nibble of byte j: q is u8 [n_tokens, hidden/2],
+ *                         block scales u8 (E4M3) [n_tokens, hidden/16], row-major.
+ * The divisions y / s are correctly rounded fp32 divisions.
+ */
+typedef enum {
+    RMSQ_FP8_STATIC = 0,
+    RMSQ_FP8_PER_TOKEN = 1,
+    RMSQ_FP8_GROUP128_ROW = 2,
+    RMSQ_FP8_GROUP128_COL = 3,
+    RMSQ_FP8_GROUP64_ROW = 4,
+    RMSQ_FP8_GROUP64_COL = 5,
+    RMSQ_NVFP4 = 6
+} rmsq_quant_mode;
+
+/*
+ * rmsq_fused_add_rmsnorm_quant — one launch of the fused op over n_tokens rows.
+ *
+ *  x            device, T[n_tokens, hidden], row-major, 16-byte aligned.
+ *  residual     device, T[n_tokens, hidden], 16-byte aligned, or NULL (plain
+ *               RMSNorm + quant: h = x, nothing is written to residual_out).
+ *  weight       device, T[hidden], 16-byte aligned (same dtype as x).
+ *  eps          finite, >= 0 (1e-5 and 1e-6 are the values the pages use).
+ *  quant_mode   an rmsq_quant_mode.
+ *  scale_in     device, one fp32: the static scale s (FP8_STATIC) or the global
+ *               scale gs (NVFP4); ignored (may be NULL) for the dynamic FP8
+ *               modes.  Its value must be finite and > 0; it is not checked.
+ *  out_q        device, u8[n_tokens, hidden] (FP8) or u8[n_tokens, hidden/2]
+ *               (NVFP4), 16-byte aligned.
+ *  out_scales   device; fp32 per-token / per-group scales (4-byte aligned) or
+ *               u8 NVFP4 block scales; ignored (may be NULL) for FP8_STATIC.
+ *               rmsq_query_sizes gives the byte sizes.
+ *  residual_out device, T[n_tokens, hidden], 16-byte aligned; NULL exactly when
+ *               residual is NULL.  It may be the same pointer as residual (the
+ *               in-place update of fused_add_rms_norm) or as x.
+ *  n_tokens     >= 0 and < 2^31; 0 returns RMSQ_OK without a launch.
+ *  hidden       > 0, a multiple of 8 (16 for NVFP4, G for the group modes),
+ *               <= RMSQ_MAX_HIDDEN.
+ *  dtype        an rmsq_dtype: the type of x, residual, weight, residual_out.
+ *  stream       cudaStream_t to launch on.
+ * Aliasing: besides residual_out == residual or residual_out == x, no output
+ * may overlap any input or another output, and x / residual / residual_out
+ * must be identical or disjoint.
+ * Returns an rmsq_status.
+ */
+int rmsq_fused_add_rmsnorm_quant(const void *x, const void *residual, const void *weight,
+                                 float eps, int quant_mode, const float *scale_in,
+                                 void *out_q, void *out_scales, void *residual_out,
+                                 int64_t n_tokens, int64_t hidden, int dtype, void *stream);
+
+/*
+ * rmsq_query_sizes — bytes of out_q and out_scales for a mode and shape (host
+ * only, no device needed).  scale_bytes is 0 for FP8_STATIC.
+ */
+int rmsq_query_sizes(int quant_mode, int64_t n_tokens, int64_t hidden, size_t *q_bytes,
+                     size_t *scale_bytes);
+
+/*
+ * rmsq_debug_convert — the library's own fp32 -> 8-bit / 4-bit conversions on
+ * a device array, so that tests can pin them against a reference encoder.
+ * kind 0: out[i] = e4m3(in[i]) (E4M3FN, nearest even, saturating);
+ * kind 1: out[i] = e2m1(in[i]) in the low nibble (high nibble 0).
+ * in: device fp32[n]; out: device u8[n]; no alignment requirement.
+ */
+int rmsq_debug_convert(int kind, const float *in, uint8_t *out, int64_t n, void *stream);
+
+/* Text for an rmsq_status (static storage, never NULL). */
+const char *rmsq_status_string(int status);
+
+/* CUDA error code (cudaError_t) of the last RMSQ_ERR_CUDA on this thread. */
+int rmsq_last_cuda_error(void);
+
+/* RMSQ_VERSION of the built library. */
+int rmsq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSQ_H */

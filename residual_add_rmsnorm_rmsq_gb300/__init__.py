@@ -1,0 +1,164 @@
+"""Python binding of librmsq (fused residual-add + RMSNorm + FP8 / NVFP4 quantisation).
+
+Argument marshalling only: every step of the op runs in the library's CUDA
+kernels.  torch is used for device memory and streams.  The names follow the C
+ABI in ``include/rmsq.h``; if the built library is missing this module raises
+instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "librmsq.so")
+
+# rmsq_status
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_ALIAS, ERR_UNSUPPORTED_SHAPE, \
+    ERR_UNSUPPORTED_DEVICE, ERR_NO_DEVICE, ERR_CUDA = range(8)
+
+# rmsq_quant_mode
+MODES = {
+    "fp8_static": 0,
+    "fp8_per_token": 1,
+    "fp8_group128_row": 2,
+    "fp8_group128_col": 3,
+    "fp8_group64_row": 4,
+    "fp8_group64_col": 5,
+    "nvfp4": 6,
+}
+# rmsq_dtype
+DTYPES = {torch.bfloat16: 0, torch.float16: 1}
+MAX_HIDDEN = 16384
+
+EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_query_sizes", "rmsq_debug_convert",
+           "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
+
+
+class RmsqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = status_string(status) if _lib is not None else str(status)
+        if status == ERR_CUDA and _lib is not None:
+            msg += f" (cudaError {_lib.rmsq_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [status {status}]")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load librmsq.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"librmsq.so not built ({p}); run __graft_entry__.build()")
+        L = ctypes.CDLL(p)
+        vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+        L.rmsq_fused_add_rmsnorm_quant.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci, vp]
+        L.rmsq_fused_add_rmsnorm_quant.restype = ci
+        L.rmsq_query_sizes.argtypes = [ci, i64, i64, ctypes.POINTER(ctypes.c_size_t),
+                                       ctypes.POINTER(ctypes.c_size_t)]
+        L.rmsq_query_sizes.restype = ci
+        L.rmsq_debug_convert.argtypes = [ci, vp, vp, i64, vp]
+        L.rmsq_debug_convert.restype = ci
+        L.rmsq_status_string.argtypes = [ci]
+        L.rmsq_status_string.restype = ctypes.c_char_p
+        L.rmsq_last_cuda_error.argtypes = []
+        L.rmsq_last_cuda_error.restype = ci
+        L.rmsq_version.argtypes = []
+        L.rmsq_version.restype = ci
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return load().rmsq_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return load().rmsq_version()
+
+
+def query_sizes(mode: str, n_tokens: int, hidden: int) -> tuple[int, int]:
+    q, s = ctypes.c_size_t(), ctypes.c_size_t()
+    st = load().rmsq_query_sizes(MODES[mode], n_tokens, hidden, ctypes.byref(q), ctypes.byref(s))
+    if st:
+        raise RmsqError(st, "rmsq_query_sizes")
+    return q.value, s.value
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def scales_like(mode: str, n_tokens: int, hidden: int, device) -> torch.Tensor | None:
+    """An output tensor of the right shape and dtype for the scales of ``mode``."""
+    if mode == "fp8_static":
+        return None
+    if mode == "fp8_per_token":
+        return torch.empty(n_tokens, dtype=torch.float32, device=device)
+    if mode == "nvfp4":
+        return torch.empty(n_tokens, hidden // 16, dtype=torch.uint8, device=device)
+    G = 128 if "128" in mode else 64
+    shape = (hidden // G, n_tokens) if mode.endswith("_col") else (n_tokens, hidden // G)
+    return torch.empty(shape, dtype=torch.float32, device=device)
+
+
+def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weight: torch.Tensor,
+                            eps: float, mode: str, scale_in: torch.Tensor | None = None, *,
+                            out_q: torch.Tensor | None = None,
+                            out_scales: torch.Tensor | None = None,
+                            residual_out: torch.Tensor | None = None, stream=None):
+    """rmsq_fused_add_rmsnorm_quant on torch CUDA tensors.
+
+    x, residual, residual_out: [n, H] bf16/fp16, contiguous; weight: [H];
+    scale_in: fp32 device tensor with one element (FP8 static scale / NVFP4
+    global scale).  Missing outputs are allocated.  Pass
+    ``residual_out=residual`` for the in-place update.
+    Returns (q, scales, residual_out).
+    """
+    L = load()
+    n, H = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {x.dtype}")
+    for t in (x, residual, weight, residual_out, out_q, out_scales, scale_in):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    if out_q is None:
+        out_q = torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device=x.device)
+    if out_scales is None:
+        out_scales = scales_like(mode, n, H, x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(residual)
+    st = L.rmsq_fused_add_rmsnorm_quant(_p(x), _p(residual), _p(weight), ctypes.c_float(eps),
+                                        MODES[mode], _p(scale_in), _p(out_q), _p(out_scales),
+                                        _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
+    return out_q, out_scales, residual_out
+
+
+def debug_convert(kind: str, values: torch.Tensor, stream=None) -> torch.Tensor:
+    """The library's E4M3 ("e4m3") or E2M1 ("e2m1", low nibble) conversion of a
+    fp32 CUDA tensor."""
+    L = load()
+    v = values.contiguous().float()
+    out = torch.empty(v.shape, dtype=torch.uint8, device=v.device)
+    st = L.rmsq_debug_convert({"e4m3": 0, "e2m1": 1}[kind], _p(v), _p(out), v.numel(), _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_debug_convert")
+    return out

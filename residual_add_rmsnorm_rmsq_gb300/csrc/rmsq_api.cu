@@ -1,0 +1,204 @@
+// C ABI of librmsq: argument checks, device check, dispatch.  Declarations and
+// the meaning of every argument are in include/rmsq.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "rmsq.h"
+#include "rmsq_launch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 128;
+// Per-device compute capability (major * 10 + minor), 0 = not yet queried.
+std::atomic<int> g_cc[kMaxDevices];
+// Device count: -1 = not yet queried.
+std::atomic<int> g_device_count{-1};
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return RMSQ_ERR_CUDA;
+}
+
+// RMSQ_OK when the current device is a compute capability 10.3 part.
+int check_device() {
+    int count = g_device_count.load(std::memory_order_acquire);
+    if (count < 0) {
+        cudaError_t e = cudaGetDeviceCount(&count);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            count = 0;
+        }
+        g_device_count.store(count, std::memory_order_release);
+    }
+    if (count == 0) return RMSQ_ERR_NO_DEVICE;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return RMSQ_ERR_UNSUPPORTED_DEVICE;
+    int cc = g_cc[dev].load(std::memory_order_acquire);
+    if (cc == 0) {
+        int major = 0, minor = 0;
+        e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e != cudaSuccess) return fail_cuda(e);
+        cc = major * 10 + minor;
+        g_cc[dev].store(cc, std::memory_order_release);
+    }
+    return cc == 103 ? RMSQ_OK : RMSQ_ERR_UNSUPPORTED_DEVICE;
+}
+
+int group_of(int mode) {
+    switch (mode) {
+    case RMSQ_FP8_GROUP128_ROW:
+    case RMSQ_FP8_GROUP128_COL: return 128;
+    case RMSQ_FP8_GROUP64_ROW:
+    case RMSQ_FP8_GROUP64_COL: return 64;
+    default: return 0;
+    }
+}
+
+int check_shape(int mode, int64_t n, int64_t hidden) {
+    if (mode < RMSQ_FP8_STATIC || mode > RMSQ_NVFP4) return RMSQ_ERR_INVALID_ARG;
+    if (n < 0 || hidden <= 0) return RMSQ_ERR_INVALID_ARG;
+    if (n > INT32_MAX || hidden > RMSQ_MAX_HIDDEN || hidden % 8 != 0) return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    if (mode == RMSQ_NVFP4 && hidden % 16 != 0) return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    const int g = group_of(mode);
+    if (g && hidden % g != 0) return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    return RMSQ_OK;
+}
+
+void sizes_of(int mode, int64_t n, int64_t hidden, size_t* q, size_t* sc) {
+    *q = static_cast<size_t>(mode == RMSQ_NVFP4 ? n * (hidden / 2) : n * hidden);
+    switch (mode) {
+    case RMSQ_FP8_STATIC: *sc = 0; break;
+    case RMSQ_FP8_PER_TOKEN: *sc = static_cast<size_t>(n) * 4; break;
+    case RMSQ_NVFP4: *sc = static_cast<size_t>(n * (hidden / 16)); break;
+    default: *sc = static_cast<size_t>(n * (hidden / group_of(mode))) * 4; break;
+    }
+}
+
+struct Span {
+    uintptr_t lo, hi;   // [lo, hi); empty when lo == hi
+};
+
+Span span(const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, p ? a + bytes : a};
+}
+
+bool overlaps(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int rmsq_fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps,
+                                 int quant_mode, const float* scale_in, void* out_q, void* out_scales,
+                                 void* residual_out, int64_t n_tokens, int64_t hidden, int dtype,
+                                 void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(quant_mode, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return RMSQ_OK;
+
+    const bool needs_scale_in = quant_mode == RMSQ_FP8_STATIC || quant_mode == RMSQ_NVFP4;
+    const bool has_scales = quant_mode != RMSQ_FP8_STATIC;
+    if (!x || !weight || !out_q) return RMSQ_ERR_INVALID_ARG;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSQ_ERR_INVALID_ARG;
+    if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
+    if (has_scales && !out_scales) return RMSQ_ERR_INVALID_ARG;
+    if (!needs_scale_in) scale_in = nullptr;
+    if (!has_scales) out_scales = nullptr;
+
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16) ||
+        !aligned(residual_out, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4))
+        return RMSQ_ERR_ALIGNMENT;
+    if (quant_mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+
+    size_t q_bytes = 0, sc_bytes = 0;
+    sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
+    const size_t act = static_cast<size_t>(n_tokens * hidden) * 2;
+    const Span X = span(x, act), R = span(residual, act), W = span(weight, hidden * 2),
+               RO = span(residual_out, act), Q = span(out_q, q_bytes), SC = span(out_scales, sc_bytes),
+               SI = span(scale_in, 4);
+    if (residual && X.lo != R.lo && overlaps(X, R)) return RMSQ_ERR_ALIAS;
+    if (residual_out) {
+        if (RO.lo != X.lo && overlaps(RO, X)) return RMSQ_ERR_ALIAS;
+        if (RO.lo != R.lo && overlaps(RO, R)) return RMSQ_ERR_ALIAS;
+        if (overlaps(RO, W) || overlaps(RO, SI)) return RMSQ_ERR_ALIAS;
+    }
+    const Span outs[2] = {Q, SC};
+    for (const Span& o : outs)
+        if (overlaps(o, X) || overlaps(o, R) || overlaps(o, W) || overlaps(o, RO) || overlaps(o, SI))
+            return RMSQ_ERR_ALIAS;
+    if (overlaps(Q, SC)) return RMSQ_ERR_ALIAS;
+
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+
+    rmsq::LaunchArgs la;
+    la.x = x;
+    la.res = residual;
+    la.w = weight;
+    la.res_out = residual_out;
+    la.q = out_q;
+    la.scales = out_scales;
+    la.scale_in = scale_in;
+    la.eps = eps;
+    la.mode = quant_mode;
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::launch_rows_bf16(la, s) : rmsq::launch_rows_fp16(la, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return RMSQ_OK;
+}
+
+int rmsq_query_sizes(int quant_mode, int64_t n_tokens, int64_t hidden, size_t* q_bytes,
+                     size_t* scale_bytes) {
+    if (!q_bytes || !scale_bytes) return RMSQ_ERR_INVALID_ARG;
+    const int st = check_shape(quant_mode, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    sizes_of(quant_mode, n_tokens, hidden, q_bytes, scale_bytes);
+    return RMSQ_OK;
+}
+
+int rmsq_debug_convert(int kind, const float* in, uint8_t* out, int64_t n, void* stream) {
+    if ((kind != 0 && kind != 1) || n < 0) return RMSQ_ERR_INVALID_ARG;
+    if (n == 0) return RMSQ_OK;
+    if (!in || !out) return RMSQ_ERR_INVALID_ARG;
+    if (!aligned(in, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (overlaps(span(in, static_cast<size_t>(n) * 4), span(out, static_cast<size_t>(n))))
+        return RMSQ_ERR_ALIAS;
+    const int st = check_device();
+    if (st != RMSQ_OK) return st;
+    const cudaError_t e = rmsq::launch_convert(kind, in, out, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
+const char* rmsq_status_string(int status) {
+    switch (status) {
+    case RMSQ_OK: return "ok";
+    case RMSQ_ERR_INVALID_ARG: return "invalid argument";
+    case RMSQ_ERR_ALIGNMENT: return "misaligned pointer";
+    case RMSQ_ERR_ALIAS: return "overlapping buffers";
+    case RMSQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case RMSQ_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case RMSQ_ERR_NO_DEVICE: return "no CUDA device";
+    case RMSQ_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int rmsq_last_cuda_error(void) { return t_last_cuda_error; }
+
+int rmsq_version(void) { return RMSQ_VERSION; }
+
+}  // extern "C"

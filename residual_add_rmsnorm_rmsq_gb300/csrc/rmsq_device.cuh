@@ -1,0 +1,164 @@
+// Device helpers for the fused residual-add + RMSNorm + quantisation kernels (sm_103a).
+//
+// Number formats: OCP FP8 E4M3FN and FP4 E2M1, converted with the hardware
+// cvt instructions (round to nearest even, .satfinite).  Every fp32 step uses
+// the explicitly rounded intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
+// __fsqrt_rn) so that no multiply-add contraction changes a rounding.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace rmsq {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// Activation types: unpack one 32-bit word (two elements, the lower-addressed
+// element in bits 0..15) to fp32, and pack two fp32 with round-to-nearest-even.
+// ---------------------------------------------------------------------------
+struct Bf16T {
+    static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+    static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+};
+
+struct Fp16T {
+    static __device__ __forceinline__ float lo(uint32_t w) {
+        float f;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
+        return f;
+    }
+    static __device__ __forceinline__ float hi(uint32_t w) {
+        float f;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(w));
+        return f;
+    }
+    static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+        uint32_t r;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Global memory access.  Activations are touched once: no L1 allocation on
+// loads, streaming (evict-first) stores.  The weight row is shared by every
+// row of the launch and goes through the read-only path.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_act(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_weight(const uint4* p) {
+    uint4 v;
+    asm("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
+    asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) {
+    asm volatile("st.global.cs.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Conversions.
+// ---------------------------------------------------------------------------
+
+// Two fp32 -> two E4M3 codes: code(lo) in bits 0..7, code(hi) in bits 8..15.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight fp32 -> eight E2M1 codes packed in one word: element k in nibble k.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// Exact value of a non-negative, finite E4M3 code (the NVFP4 block scale):
+// exponent field e, fraction m: e == 0 -> m * 2^-9, else (1 + m/8) * 2^(e-7).
+__device__ __forceinline__ float e4m3_value_nonneg(uint32_t c) {
+    const uint32_t e = (c >> 3) & 0xfu, m = c & 7u;
+    return e == 0 ? __fmul_rn(__uint2float_rn(m), 0.001953125f)
+                  : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// E4M3 codes of y0/s and y1/s where each quotient is the correctly rounded
+// fp32 division.  Fast path: multiply by two bracketing reciprocals
+// rdn = RN(RN(1/s) * (1 - 2^-20)) and rup = RN(RN(1/s) * (1 + 2^-20)).  The
+// products lie strictly below / above the rounded quotient in magnitude (the
+// three roundings involved move a value by less than 3 * 2^-24 relative),
+// and the saturating nearest-even E4M3 cast is monotone, so equal codes at
+// both ends are the code of the quotient.  Otherwise (about one pair in
+// 2^15) the quotients are computed with __fdiv_rn.
+__device__ __forceinline__ uint32_t fp8_pair(float y0, float y1, float rdn, float rup, float s) {
+    const uint32_t cd = e4m3x2(__fmul_rn(y0, rdn), __fmul_rn(y1, rdn));
+    const uint32_t cu = e4m3x2(__fmul_rn(y0, rup), __fmul_rn(y1, rup));
+    if (cd == cu) return cd;
+    return e4m3x2(__fdiv_rn(y0, s), __fdiv_rn(y1, s));
+}
+
+// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.
+__device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s) {
+    const float r = __fdiv_rn(1.0f, s);
+    const float rdn = __fmul_rn(r, 0.99999904632568359375f);   // 1 - 2^-20
+    const float rup = __fmul_rn(r, 1.00000095367431640625f);   // 1 + 2^-20
+    uint2 out;
+    out.x = fp8_pair(v[0], v[1], rdn, rup, s) | (fp8_pair(v[2], v[3], rdn, rup, s) << 16);
+    out.y = fp8_pair(v[4], v[5], rdn, rup, s) | (fp8_pair(v[6], v[7], rdn, rup, s) << 16);
+    return out;
+}
+
+// Pairwise tree over the squares of eight consecutive elements.
+__device__ __forceinline__ float leaf8_sumsq(const float (&h)[8]) {
+    const float a = __fadd_rn(__fmul_rn(h[0], h[0]), __fmul_rn(h[1], h[1]));
+    const float b = __fadd_rn(__fmul_rn(h[2], h[2]), __fmul_rn(h[3], h[3]));
+    const float c = __fadd_rn(__fmul_rn(h[4], h[4]), __fmul_rn(h[5], h[5]));
+    const float d = __fadd_rn(__fmul_rn(h[6], h[6]), __fmul_rn(h[7], h[7]));
+    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+}
+
+// Butterfly sum over the 32 lanes: at step k lanes differing in bit k add
+// their values, which is the pairwise tree over lane index (fp32 addition is
+// commutative, so both partners hold the same node value).
+__device__ __forceinline__ float warp_tree_sum(float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+template <int LANES>
+__device__ __forceinline__ float lanes_max(float v) {
+#pragma unroll
+    for (int o = 1; o < LANES; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+    return v;
+}
+
+}  // namespace rmsq

@@ -1,0 +1,8 @@
+// bf16 instantiations of the row kernel.
+#include "rmsq_dispatch.cuh"
+
+namespace rmsq {
+cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream) {
+    return launch_rows<Bf16T>(a, stream);
+}
+}  // namespace rmsq

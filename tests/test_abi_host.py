@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel runs).
+
+The library must load, export every entry point include/rmsq.h declares, and
+reject bad arguments with the documented status before touching a device.
+Pointers here are fake addresses: validation never dereferences them.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import residual_add_rmsnorm_rmsq_gb300 as rq
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "rmsq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from residual_add_rmsnorm_rmsq_gb300 import _build
+    _build.build()
+    return rq.load()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*(rmsq_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared()
+    assert set(names) == set(rq.EXPORTS), names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert rq.version() == 10000
+    for s in range(8):
+        assert rq.status_string(s)
+    assert rq.status_string(99) == "unknown status"
+
+
+def test_query_sizes(L):
+    assert rq.query_sizes("fp8_static", 4, 64) == (256, 0)
+    assert rq.query_sizes("fp8_per_token", 4, 64) == (256, 16)
+    assert rq.query_sizes("fp8_group128_row", 3, 256) == (768, 24)
+    assert rq.query_sizes("fp8_group64_col", 3, 256) == (768, 48)
+    assert rq.query_sizes("nvfp4", 5, 2048) == (5 * 1024, 5 * 128)
+    with pytest.raises(rq.RmsqError):
+        rq.query_sizes("nvfp4", 5, 40)
+
+
+A, B, C, D, E, F = (0x10000000 * k for k in range(1, 7))   # far-apart fake addresses
+
+
+def call(L, x=A, res=B, w=C, eps=1e-6, mode=1, s_in=None, q=D, sc=E, ro=F, n=4, H=64, dt=0):
+    vp = ctypes.c_void_p
+    return L.rmsq_fused_add_rmsnorm_quant(vp(x) if x else None, vp(res) if res else None,
+                                          vp(w) if w else None, ctypes.c_float(eps), mode,
+                                          vp(s_in) if s_in else None, vp(q) if q else None,
+                                          vp(sc) if sc else None, vp(ro) if ro else None,
+                                          n, H, dt, None)
+
+
+def test_argument_errors(L):
+    assert call(L, dt=2) == rq.ERR_INVALID_ARG
+    assert call(L, mode=7) == rq.ERR_INVALID_ARG
+    assert call(L, mode=-1) == rq.ERR_INVALID_ARG
+    assert call(L, n=-1) == rq.ERR_INVALID_ARG
+    assert call(L, H=0) == rq.ERR_INVALID_ARG
+    assert call(L, eps=-1.0) == rq.ERR_INVALID_ARG
+    assert call(L, eps=float("nan")) == rq.ERR_INVALID_ARG
+    assert call(L, eps=float("inf")) == rq.ERR_INVALID_ARG
+    assert call(L, x=0) == rq.ERR_INVALID_ARG
+    assert call(L, w=0) == rq.ERR_INVALID_ARG
+    assert call(L, q=0) == rq.ERR_INVALID_ARG
+    assert call(L, ro=0) == rq.ERR_INVALID_ARG           # residual without residual_out
+    assert call(L, res=0) == rq.ERR_INVALID_ARG          # residual_out without residual
+    assert call(L, sc=0) == rq.ERR_INVALID_ARG           # dynamic mode needs out_scales
+    assert call(L, mode=0) == rq.ERR_INVALID_ARG         # static needs scale_in
+    assert call(L, mode=6, H=64) == rq.ERR_INVALID_ARG   # NVFP4 needs scale_in
+
+
+def test_shape_errors(L):
+    assert call(L, H=60) == rq.ERR_UNSUPPORTED_SHAPE
+    assert call(L, H=16392) == rq.ERR_UNSUPPORTED_SHAPE
+    assert call(L, mode=2, H=64) == rq.ERR_UNSUPPORTED_SHAPE
+    assert call(L, mode=4, H=96) == rq.ERR_UNSUPPORTED_SHAPE
+    assert call(L, mode=6, H=24, s_in=0x7000000) == rq.ERR_UNSUPPORTED_SHAPE
+    assert call(L, n=2 ** 31) == rq.ERR_UNSUPPORTED_SHAPE
+
+
+def test_empty_input_is_ok_without_pointers(L):
+    assert call(L, n=0, x=0, res=0, w=0, q=0, sc=0, ro=0) == rq.OK
+
+
+def test_alignment_errors(L):
+    assert call(L, x=A + 8) == rq.ERR_ALIGNMENT
+    assert call(L, res=B + 2) == rq.ERR_ALIGNMENT
+    assert call(L, w=C + 4) == rq.ERR_ALIGNMENT
+    assert call(L, q=D + 8) == rq.ERR_ALIGNMENT
+    assert call(L, ro=F + 8) == rq.ERR_ALIGNMENT
+    assert call(L, sc=E + 2) == rq.ERR_ALIGNMENT
+    assert call(L, mode=0, s_in=E + 2, sc=0) == rq.ERR_ALIGNMENT
+
+
+def test_alias_errors(L):
+    act = 4 * 64 * 2
+    assert call(L, ro=B + 16) == rq.ERR_ALIAS               # partial overlap with residual
+    assert call(L, res=A + 16, ro=F) == rq.ERR_ALIAS        # x and residual partially overlap
+    assert call(L, q=A + act - 16) == rq.ERR_ALIAS          # codes over x
+    assert call(L, sc=D + 128) == rq.ERR_ALIAS              # scales over codes
+    assert call(L, ro=C) == rq.ERR_ALIAS                    # residual_out over weight
+    assert call(L, q=F + 64) == rq.ERR_ALIAS                # codes over residual_out
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_valid_call_without_device_reports_no_device(L):
+    assert call(L) == rq.ERR_NO_DEVICE
+    assert call(L, ro=B) == rq.ERR_NO_DEVICE                 # in place: allowed
+    assert call(L, ro=A) == rq.ERR_NO_DEVICE                 # over x: allowed
+    assert call(L, mode=0, s_in=0x7000000, sc=0) == rq.ERR_NO_DEVICE
+    vp = ctypes.c_void_p
+    assert L.rmsq_debug_convert(0, vp(A), vp(B), 16, None) == rq.ERR_NO_DEVICE
+    assert L.rmsq_debug_convert(2, vp(A), vp(B), 16, None) == rq.ERR_INVALID_ARG

@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by
+element, on the same seeded inputs.
+
+Covers the five workloads of the path (the 64x512 static-FP8 case, the
+Llama-, DeepSeek-V3- and Qwen3-shaped layers, the fp16 decode sweep) at the
+sizes the benchmark launches, plus ragged / tiny / maximum shapes, in-place
+residual updates, and the hand-worked rows.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import _parity as P
+import oracle
+import residual_add_rmsnorm_rmsq_gb300 as rq
+import rmsq_inputs as ri
+
+pytestmark = pytest.mark.gpu
+
+ALL_MODES = list(rq.MODES)
+GROUP_MODES = ["fp8_group128_row", "fp8_group128_col", "fp8_group64_row", "fp8_group64_col"]
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(rmsq_gpu):
+    return rmsq_gpu
+
+
+# ---------------------------------------------------------------- worked rows
+def _golden():
+    return [e for e in json.load(open(GOLDEN))["examples"] if e["H"] % 8 == 0]
+
+
+@pytest.mark.parametrize("ex", _golden(), ids=lambda e: e["name"])
+def test_golden_rows_on_gpu(ex):
+    n, H = ex["n"], ex["H"]
+
+    def fill(v, shape):
+        a = np.asarray(v, np.float64)
+        return np.broadcast_to(a, shape).copy() if a.size == 1 else a.reshape(shape)
+
+    x = ri.to_bits(fill(ex["x"], (n, H)), ex["dtype"]).reshape(n, H)
+    r = None if ex["residual"] is None else ri.to_bits(fill(ex["residual"], (n, H)), ex["dtype"]).reshape(n, H)
+    w = ri.to_bits(fill(ex["weight"], (H,)), ex["dtype"])
+    wl = ri.Workload(ex["name"], n, H, ex["dtype"], ex["eps"], x, r, w)
+    got = P.run_gpu(wl, ex["mode"], ex["scale_in"])
+    q = got["q"].ravel()
+    b = bytes.fromhex(ex["expect"]["q_hex"])
+    want = np.frombuffer(b * (q.size // len(b)) if len(b) < q.size else b, np.uint8)
+    assert np.array_equal(q, want), (q.tobytes().hex(), ex["expect"]["q_hex"])
+    e = ex["expect"]
+    if "residual_out_hex" in e:
+        assert np.all(got["residual_out"] == int(e["residual_out_hex"], 16))
+    if "scales_f32_bits" in e:
+        assert np.all(got["scales"].view(np.uint32) == int(e["scales_f32_bits"][0], 16))
+    if "scales_u8_hex" in e:
+        assert np.all(got["scales"] == int(e["scales_u8_hex"][0], 16))
+
+
+# ---------------------------------------------------------------- the five workloads
+def test_pr1_static_fp8():
+    P.check(ri.pr1(), "fp8_static")
+
+
+@pytest.mark.parametrize("residual", [True, False], ids=["res", "nores"])
+def test_llama_per_token_full_size(residual):
+    P.check(ri.llama(4096, residual=residual), "fp8_per_token", nthreads=16)
+
+
+@pytest.mark.parametrize("mode", ALL_MODES)
+def test_llama_shape_every_mode(mode):
+    P.check(ri.llama(512), mode, scale_in=0.1 if mode == "fp8_static" else None)
+
+
+@pytest.mark.parametrize("mode", GROUP_MODES)
+def test_dsv3_groups_full_size(mode):
+    P.check(_dsv3_full(), mode, nthreads=16)
+
+
+_DSV3 = {}
+
+
+def _dsv3_full():
+    if "wl" not in _DSV3:
+        _DSV3["wl"] = ri.dsv3(8192)
+    return _DSV3["wl"]
+
+
+@pytest.mark.parametrize("n", ri.QWEN_TOKENS)
+def test_qwen_nvfp4(n):
+    P.check(ri.qwen_nvfp4(n), "nvfp4", nthreads=16)
+
+
+@pytest.mark.parametrize("residual", [True, False], ids=["res", "nores"])
+@pytest.mark.parametrize("mode", ["fp8_static", "fp8_per_token", "fp8_group128_row", "nvfp4"])
+def test_decode_sweep(mode, residual):
+    for n in ri.DECODE_TOKENS:
+        P.check(ri.decode(n, residual=residual), mode, label=f"decode_{n}/{mode}/{residual}")
+
+
+# ---------------------------------------------------------------- edges
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("H", [8, 16, 24, 136, 1000, 4104, 8200, 16384])
+def test_ragged_and_maximum_hidden(dtype, H):
+    for n in (1, 3, 33):
+        wl = ri.make_workload(f"rag_{n}x{H}", n, H, dtype=dtype, res_sigma=1.5, seed=H + n)
+        for mode in ALL_MODES:
+            if mode == "nvfp4" and H % 16:
+                continue
+            if mode in GROUP_MODES and H % (128 if "128" in mode else 64):
+                continue
+            P.check(wl, mode, scale_in=0.07 if mode == "fp8_static" else None,
+                    label=f"{wl.name}/{dtype}/{mode}")
+
+
+def test_empty_input_launches_nothing():
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    q, sc, ro = rq.fused_add_rmsnorm_quant(x, x, w, 1e-6, "fp8_per_token")
+    assert q.numel() == 0 and sc.numel() == 0 and ro.numel() == 0
+
+
+def test_in_place_residual_update():
+    wl = ri.make_workload("inplace", 40, 2048, seed=31)
+    for mode in ("fp8_per_token", "nvfp4", "fp8_group64_col"):
+        P.check(wl, mode, in_place=True, label=f"inplace/{mode}")
+
+
+def test_residual_out_over_x():
+    wl = ri.make_workload("over_x", 9, 1024, seed=32)
+    want = oracle.run_workload(wl, "fp8_per_token")
+    x = P.dev_act(wl.x, "bf16")
+    r = P.dev_act(wl.residual, "bf16")
+    w = P.dev_act(wl.weight, "bf16")
+    q, sc, ro = rq.fused_add_rmsnorm_quant(x, r, w, wl.eps, "fp8_per_token", residual_out=x)
+    torch.cuda.synchronize()
+    assert ro.data_ptr() == x.data_ptr()
+    P.compare({"q": q.cpu().numpy(), "scales": sc.cpu().numpy(), "residual_out": P.host_bits(x)},
+              want, "fp8_per_token", "residual_out=x")
+
+
+def test_guard_bands_and_determinism():
+    """Outputs inside larger sentinel-filled buffers: nothing outside the
+    documented extents is written, and two runs give identical bytes."""
+    n, H = 77, 2048
+    wl = ri.make_workload("guard", n, H, seed=33)
+    x = P.dev_act(wl.x, "bf16")
+    r = P.dev_act(wl.residual, "bf16")
+    w = P.dev_act(wl.weight, "bf16")
+    G = 4096
+    for mode in ALL_MODES:
+        qb, sb = rq.query_sizes(mode, n, H)
+        outs = []
+        for rep in range(2):
+            qbuf = torch.full((qb + 2 * G,), 0xA5, dtype=torch.uint8, device="cuda")
+            sbuf = torch.full((sb + 2 * G,), 0x5A, dtype=torch.uint8, device="cuda")
+            rbuf = torch.full((n * H + 2 * G,), -12345, dtype=torch.int16, device="cuda")
+            q = qbuf[G:G + qb].view(n, -1)
+            sc = None if sb == 0 else sbuf[G:G + sb]
+            if sc is not None and mode != "nvfp4":
+                sc = sc.view(torch.float32)
+            ro = rbuf[G:G + n * H].view(torch.bfloat16).view(n, H)
+            s_in = torch.tensor([0.05 if mode == "fp8_static" else 300.0], device="cuda")
+            rq.fused_add_rmsnorm_quant(x, r, w, 1e-6, mode, s_in, out_q=q, out_scales=sc, residual_out=ro)
+            torch.cuda.synchronize()
+            for buf, fill in ((qbuf, 0xA5), (sbuf, 0x5A)):
+                assert torch.all(buf[:G] == fill) and torch.all(buf[-G:] == fill), mode
+            assert torch.all(rbuf[:G] == -12345) and torch.all(rbuf[-G:] == -12345), mode
+            outs.append((qbuf.cpu(), sbuf.cpu(), rbuf.cpu()))
+        for a, b in zip(outs[0], outs[1]):
+            assert torch.equal(a, b), mode
+
+
+def test_misaligned_pointers_rejected_before_launch():
+    x = torch.zeros(4 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rq.RmsqError) as ei:
+        rq.fused_add_rmsnorm_quant(x[4:4 + 256].view(4, 64), None, w, 1e-6, "fp8_per_token")
+    assert ei.value.status == rq.ERR_ALIGNMENT
+
+
+def test_non_default_stream():
+    wl = ri.make_workload("stream", 50, 4096, seed=34)
+    s = torch.cuda.Stream()
+    want = oracle.run_workload(wl, "fp8_group128_row")
+    with torch.cuda.stream(s):
+        got = P.run_gpu(wl, "fp8_group128_row", None, stream=s)
+    P.compare(got, want, "fp8_group128_row", "side stream")
