@@ -133,6 +133,35 @@ int rmsq_fused_add_rmsnorm_quant(const void *x, const void *residual, const void
                                  int64_t n_tokens, int64_t hidden, int dtype, void *stream);
 
 /*
+ * Kernel variants.  Both compute bit-identical results; AUTO picks by batch
+ * size.  DIRECT: one CTA per row, loads straight into registers (lowest
+ * latency for a few rows).  PIPELINED: persistent CTAs with several rows per
+ * CTA in flight as bulk asynchronous copies into shared memory (highest
+ * bandwidth for large batches).
+ */
+typedef enum { RMSQ_VARIANT_AUTO = 0, RMSQ_VARIANT_DIRECT = 1, RMSQ_VARIANT_PIPELINED = 2 } rmsq_variant;
+
+/*
+ * rmsq_fused_add_rmsnorm_quant_ex — rmsq_fused_add_rmsnorm_quant with an
+ * explicit rmsq_variant (RMSQ_ERR_INVALID_ARG for any other value).  Same
+ * arguments, rules and results otherwise.
+ */
+int rmsq_fused_add_rmsnorm_quant_ex(const void *x, const void *residual, const void *weight,
+                                    float eps, int quant_mode, const float *scale_in,
+                                    void *out_q, void *out_scales, void *residual_out,
+                                    int64_t n_tokens, int64_t hidden, int dtype, void *stream,
+                                    int variant);
+
+/*
+ * rmsq_take_fault_flags — reads and clears, on the current device, the flag a
+ * pipelined launch sets if it ever gives up waiting (after 100 ms) for its
+ * own shared-memory copies; the outputs of such a launch are incomplete.
+ * *flags = 0 when no launch gave up.  Synchronous with respect to the device:
+ * call it after the launches of interest have completed.
+ */
+int rmsq_take_fault_flags(uint32_t *flags);
+
+/*
  * rmsq_query_sizes — bytes of out_q and out_scales for a mode and shape (host
  * only, no device needed).  scale_bytes is 0 for FP8_STATIC.
  */

@@ -34,8 +34,11 @@ MODES = {
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 MAX_HIDDEN = 16384
 
-EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_query_sizes", "rmsq_debug_convert",
-           "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
+VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
+
+EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex", "rmsq_take_fault_flags",
+           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_status_string", "rmsq_last_cuda_error",
+           "rmsq_version")
 
 
 class RmsqError(RuntimeError):
@@ -64,6 +67,11 @@ def load(path: str | None = None):
         vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
         L.rmsq_fused_add_rmsnorm_quant.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci, vp]
         L.rmsq_fused_add_rmsnorm_quant.restype = ci
+        L.rmsq_fused_add_rmsnorm_quant_ex.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci,
+                                                      vp, ci]
+        L.rmsq_fused_add_rmsnorm_quant_ex.restype = ci
+        L.rmsq_take_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        L.rmsq_take_fault_flags.restype = ci
         L.rmsq_query_sizes.argtypes = [ci, i64, i64, ctypes.POINTER(ctypes.c_size_t),
                                        ctypes.POINTER(ctypes.c_size_t)]
         L.rmsq_query_sizes.restype = ci
@@ -122,13 +130,15 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
                             eps: float, mode: str, scale_in: torch.Tensor | None = None, *,
                             out_q: torch.Tensor | None = None,
                             out_scales: torch.Tensor | None = None,
-                            residual_out: torch.Tensor | None = None, stream=None):
+                            residual_out: torch.Tensor | None = None, stream=None,
+                            variant: str = "auto"):
     """rmsq_fused_add_rmsnorm_quant on torch CUDA tensors.
 
     x, residual, residual_out: [n, H] bf16/fp16, contiguous; weight: [H];
     scale_in: fp32 device tensor with one element (FP8 static scale / NVFP4
     global scale).  Missing outputs are allocated.  Pass
     ``residual_out=residual`` for the in-place update.
+    ``variant``: "auto", "direct" or "pipelined" (identical results).
     Returns (q, scales, residual_out).
     """
     L = load()
@@ -144,12 +154,22 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
         out_scales = scales_like(mode, n, H, x.device)
     if residual is not None and residual_out is None:
         residual_out = torch.empty_like(residual)
-    st = L.rmsq_fused_add_rmsnorm_quant(_p(x), _p(residual), _p(weight), ctypes.c_float(eps),
-                                        MODES[mode], _p(scale_in), _p(out_q), _p(out_scales),
-                                        _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream))
+    st = L.rmsq_fused_add_rmsnorm_quant_ex(_p(x), _p(residual), _p(weight), ctypes.c_float(eps),
+                                           MODES[mode], _p(scale_in), _p(out_q), _p(out_scales),
+                                           _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream),
+                                           VARIANTS[variant])
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
+
+
+def take_fault_flags() -> int:
+    """Read and clear the pipelined kernels' give-up flag (0 = none)."""
+    f = ctypes.c_uint32()
+    st = load().rmsq_take_fault_flags(ctypes.byref(f))
+    if st:
+        raise RmsqError(st, "rmsq_take_fault_flags")
+    return f.value
 
 
 def debug_convert(kind: str, values: torch.Tensor, stream=None) -> torch.Tensor:

@@ -98,11 +98,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 extern "C" {
 
-int rmsq_fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps,
-                                 int quant_mode, const float* scale_in, void* out_q, void* out_scales,
-                                 void* residual_out, int64_t n_tokens, int64_t hidden, int dtype,
-                                 void* stream) {
+int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const void* weight, float eps,
+                                    int quant_mode, const float* scale_in, void* out_q, void* out_scales,
+                                    void* residual_out, int64_t n_tokens, int64_t hidden, int dtype,
+                                    void* stream, int variant) {
     if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (variant != RMSQ_VARIANT_AUTO && variant != RMSQ_VARIANT_DIRECT && variant != RMSQ_VARIANT_PIPELINED)
+        return RMSQ_ERR_INVALID_ARG;
     int st = check_shape(quant_mode, n_tokens, hidden);
     if (st != RMSQ_OK) return st;
     if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
@@ -155,9 +157,32 @@ int rmsq_fused_add_rmsnorm_quant(const void* x, const void* residual, const void
     la.mode = quant_mode;
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(hidden);
+    la.variant = variant == RMSQ_VARIANT_DIRECT ? rmsq::kVariantDirect
+                 : variant == RMSQ_VARIANT_PIPELINED ? rmsq::kVariantPipelined : rmsq::kVariantAuto;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::launch_rows_bf16(la, s) : rmsq::launch_rows_fp16(la, s);
     if (e != cudaSuccess) return fail_cuda(e);
+    return RMSQ_OK;
+}
+
+int rmsq_fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps,
+                                 int quant_mode, const float* scale_in, void* out_q, void* out_scales,
+                                 void* residual_out, int64_t n_tokens, int64_t hidden, int dtype,
+                                 void* stream) {
+    return rmsq_fused_add_rmsnorm_quant_ex(x, residual, weight, eps, quant_mode, scale_in, out_q,
+                                           out_scales, residual_out, n_tokens, hidden, dtype, stream,
+                                           RMSQ_VARIANT_AUTO);
+}
+
+int rmsq_take_fault_flags(uint32_t* flags) {
+    if (!flags) return RMSQ_ERR_INVALID_ARG;
+    const int st = check_device();
+    if (st != RMSQ_OK) return st;
+    unsigned int a = 0, b = 0;
+    cudaError_t e = rmsq::take_pipe_fault_bf16(&a);
+    if (e == cudaSuccess) e = rmsq::take_pipe_fault_fp16(&b);
+    if (e != cudaSuccess) return fail_cuda(e);
+    *flags = a | b;
     return RMSQ_OK;
 }
 

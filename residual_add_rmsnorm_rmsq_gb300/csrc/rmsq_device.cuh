@@ -125,14 +125,21 @@ __device__ __forceinline__ uint32_t fp8_pair(float y0, float y1, float rdn, floa
     return e4m3x2(__fdiv_rn(y0, s), __fdiv_rn(y1, s));
 }
 
-// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.
-__device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s) {
+// Bracketing reciprocals of a scale s for fp8_pair.
+struct Fp8Recips {
+    float rdn, rup;
+};
+__device__ __forceinline__ Fp8Recips fp8_recips(float s) {
     const float r = __fdiv_rn(1.0f, s);
-    const float rdn = __fmul_rn(r, 0.99999904632568359375f);   // 1 - 2^-20
-    const float rup = __fmul_rn(r, 1.00000095367431640625f);   // 1 + 2^-20
+    return {__fmul_rn(r, 0.99999904632568359375f),     // 1 - 2^-20
+            __fmul_rn(r, 1.00000095367431640625f)};    // 1 + 2^-20
+}
+
+// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.
+__device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s, Fp8Recips rc) {
     uint2 out;
-    out.x = fp8_pair(v[0], v[1], rdn, rup, s) | (fp8_pair(v[2], v[3], rdn, rup, s) << 16);
-    out.y = fp8_pair(v[4], v[5], rdn, rup, s) | (fp8_pair(v[6], v[7], rdn, rup, s) << 16);
+    out.x = fp8_pair(v[0], v[1], rc.rdn, rc.rup, s) | (fp8_pair(v[2], v[3], rc.rdn, rc.rup, s) << 16);
+    out.y = fp8_pair(v[4], v[5], rc.rdn, rc.rup, s) | (fp8_pair(v[6], v[7], rc.rdn, rc.rup, s) << 16);
     return out;
 }
 
@@ -159,6 +166,73 @@ __device__ __forceinline__ float lanes_max(float v) {
 #pragma unroll
     for (int o = 1; o < LANES; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     return v;
+}
+
+// ---------------------------------------------------------------------------
+// Bulk asynchronous copies (TMA, 1-D) into shared memory with mbarrier
+// completion.  Addresses are 16-byte aligned and sizes multiples of 16.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the other threads and to the
+// asynchronous (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Global -> shared bulk copy, completion counted on `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete; gives up (returns false) after
+// kWaitLimitNs of wall time or 2^24 polls, whichever comes first.
+constexpr uint64_t kWaitLimitNs = 100ull * 1000 * 1000;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return false;
 }
 
 }  // namespace rmsq

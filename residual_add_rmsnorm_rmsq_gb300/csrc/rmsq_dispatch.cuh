@@ -1,36 +1,108 @@
-// Picks the row-kernel instantiation for (mode, residual, chunks per thread)
-// and launches it: one CTA per row, ceil(hidden / 8 / J) threads rounded up
-// to whole warps.
+// Picks and launches a row-kernel instantiation for (mode, residual, chunks
+// per thread J, variant).  Included once per activation type.
+//
+//  direct:    one CTA per row, ceil(hidden / 8 / J) threads (J = 1 up to
+//             hidden 8192, else 2), loads straight into registers.
+//  pipelined: persistent CTAs (as many as fit on the SMs), `stages` rows of
+//             x / residual in flight per CTA through the shared-memory ring.
+//             J = 1 up to hidden 2048, 2 up to 4096, else 4 (<= 512 threads).
 #pragma once
 
+#include <atomic>
+#include <mutex>
+
 #include "rmsq_launch.h"
+#include "rmsq_pipe.cuh"
 #include "rmsq_rows.cuh"
 
 namespace rmsq {
 
+// Set by a pipelined CTA that gave up waiting for its copies (this unit's
+// instantiations only).
+static __device__ unsigned int g_pipe_fault;
+
+template <class E, int MODE, bool RES, int J>
+__global__ void __launch_bounds__(kPipeMaxThreads, 1) pipe_entry(const RowArgs a, const int stages) {
+    pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
+}
+
 template <class E, int MODE, bool RES>
-const void* pick_j(int J) {
+const void* pick_direct(int J) {
     if (J == 1) return reinterpret_cast<const void*>(&rows_kernel<E, MODE, RES, 1>);
     return reinterpret_cast<const void*>(&rows_kernel<E, MODE, RES, 2>);
 }
 
+template <class E, int MODE, bool RES>
+const void* pick_pipe(int J) {
+    if (J == 1) return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1>);
+    if (J == 2) return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2>);
+    return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 4>);
+}
+
 template <class E, int MODE>
-const void* pick_res(bool res, int J) {
-    return res ? pick_j<E, MODE, true>(J) : pick_j<E, MODE, false>(J);
+const void* pick_res(bool res, bool pipe, int J) {
+    if (pipe) return res ? pick_pipe<E, MODE, true>(J) : pick_pipe<E, MODE, false>(J);
+    return res ? pick_direct<E, MODE, true>(J) : pick_direct<E, MODE, false>(J);
 }
 
 template <class E>
-const void* pick_kernel(int mode, bool res, int J) {
+const void* pick_kernel(int mode, bool res, bool pipe, int J) {
     switch (mode) {
-    case kFp8Static: return pick_res<E, kFp8Static>(res, J);
-    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, J);
-    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, J);
-    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, J);
-    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, J);
-    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, J);
-    case kNvfp4: return pick_res<E, kNvfp4>(res, J);
+    case kFp8Static: return pick_res<E, kFp8Static>(res, pipe, J);
+    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, pipe, J);
+    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, pipe, J);
+    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, pipe, J);
+    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J);
+    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J);
+    case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J);
     default: return nullptr;
     }
+}
+
+// Occupancy of a pipelined instantiation for a given ring size, cached.
+struct OccEntry {
+    const void* fn;
+    int smem;
+    int threads;
+    int blocks;
+};
+
+inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t* err) {
+    static std::mutex mu;
+    static OccEntry cache[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].smem == smem && cache[i].threads == threads) return cache[i].blocks;
+    *err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (*err != cudaSuccess) return 0;
+    int blocks = 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, smem);
+    if (*err != cudaSuccess) return 0;
+    if (used < 64) cache[used++] = {fn, smem, threads, blocks};
+    return blocks;
+}
+
+inline int sm_count(cudaError_t* err) {
+    static std::atomic<int> cached[128];
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess || dev < 0 || dev >= 128) return 0;
+    int v = cached[dev].load(std::memory_order_acquire);
+    if (v == 0) {
+        *err = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (*err != cudaSuccess) return 0;
+        cached[dev].store(v, std::memory_order_release);
+    }
+    return v;
+}
+
+// Shared-memory ring per CTA: as many stages (2..8) as fit in ~110 KB, so that
+// two CTAs share an SM; a single stage for rows wider than that.
+inline int pipe_stages(int stage_bytes) {
+    const int budget = 110 * 1024;
+    int s = budget / stage_bytes;
+    return s < 1 ? 1 : (s > kMaxStages ? kMaxStages : s);
 }
 
 template <class E>
@@ -47,12 +119,44 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     a.n = la.n;
     a.hidden = la.hidden;
     a.chunks = la.hidden / 8;
+    const bool res = la.res != nullptr;
+
+    cudaError_t err = cudaSuccess;
+    const int sms = sm_count(&err);
+    if (err != cudaSuccess) return err;
+    bool pipe = la.variant == kVariantPipelined ||
+                (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
+
+    if (pipe) {
+        const int J = a.chunks <= 256 ? 1 : (a.chunks <= 512 ? 2 : 4);
+        const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
+        const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);
+        const int stages = pipe_stages(stage_bytes);
+        const int smem = stages * stage_bytes;
+        const void* fn = pick_kernel<E>(la.mode, res, true, J);
+        if (!fn) return cudaErrorInvalidValue;
+        const int per_sm = pipe_blocks_per_sm(fn, threads, smem, &err);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        const int grid = a.n < per_sm * sms ? a.n : per_sm * sms;
+        int st = stages;
+        void* params[] = {&a, &st};
+        return cudaLaunchKernel(fn, dim3(grid), dim3(threads), params, smem, stream);
+    }
     const int J = a.chunks <= 1024 ? 1 : 2;
     const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
-    const void* fn = pick_kernel<E>(la.mode, la.res != nullptr, J);
+    const void* fn = pick_kernel<E>(la.mode, res, false, J);
     if (!fn) return cudaErrorInvalidValue;
     void* params[] = {&a};
     return cudaLaunchKernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+}
+
+// Reads and clears this unit's pipeline fault flag (current device).
+inline cudaError_t take_pipe_fault(unsigned int* out) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_pipe_fault, sizeof(unsigned int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_pipe_fault, &zero, sizeof(unsigned int));
+    return e;
 }
 
 }  // namespace rmsq

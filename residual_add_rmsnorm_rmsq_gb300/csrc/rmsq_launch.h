@@ -18,11 +18,21 @@ struct LaunchArgs {
     int mode;
     int n;
     int hidden;
+    int variant;            // kVariant*
 };
+
+constexpr int kVariantAuto = 0;
+constexpr int kVariantDirect = 1;
+constexpr int kVariantPipelined = 2;
+// The pipelined kernel is chosen automatically from this many rows per SM.
+constexpr int kPipeMinRowsPerSm = 4;
 
 // One launch of the row kernel for bf16 / fp16 activations.
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);
+// Read and clear the pipelined kernels' fault flags (current device).
+cudaError_t take_pipe_fault_bf16(unsigned int* out);
+cudaError_t take_pipe_fault_fp16(unsigned int* out);
 cudaError_t launch_convert(int kind, const float* in, uint8_t* out, int64_t n, cudaStream_t stream);
 
 }  // namespace rmsq

@@ -1,0 +1,188 @@
+// Per-row arithmetic shared by the row kernels of the fused residual-add +
+// RMSNorm + quantisation op.
+//
+// Operation (vLLM docs "Fusion torch.compile passes", section "RMSNorm +
+// Quantization (fuse_norm_quant)"; NVFP4 variant from the vLLM PR #51925
+// summary, "Motivation"): per row, h = T(x + residual) written back as the
+// updated residual, y = h * (1 / sqrt(mean(h^2) + eps)) * w, and y quantised
+// to FP8 E4M3 (static / per-token / per-group scale) or NVFP4.
+//
+// Data-to-thread mapping used by every kernel: thread t owns the J
+// consecutive 16-byte chunks t*J .. t*J+J-1 (8 elements each) of a row.  That
+// realises the canonical pairwise tree of the sum of squares without any
+// reordering: tree over the 8 elements of a chunk, over the J chunks of a
+// thread, over lanes (xor butterfly), over warps (one warp's butterfly over
+// the zero-padded warp sums).  Zero padding is exact.
+#pragma once
+
+#include "rmsq_device.cuh"
+
+namespace rmsq {
+
+enum Mode : int {
+    kFp8Static = 0,
+    kFp8PerToken = 1,
+    kFp8G128Row = 2,
+    kFp8G128Col = 3,
+    kFp8G64Row = 4,
+    kFp8G64Col = 5,
+    kNvfp4 = 6,
+};
+
+struct RowArgs {
+    const uint4* x;
+    const uint4* res;
+    const uint4* w;
+    uint4* res_out;
+    uint8_t* q;
+    void* scales;
+    const float* scale_in;
+    float eps;
+    int n;        // rows
+    int hidden;   // elements per row
+    int chunks;   // hidden / 8
+};
+
+template <int MODE> struct ModeTraits {
+    static constexpr int group = (MODE == kFp8G128Row || MODE == kFp8G128Col) ? 128
+                               : (MODE == kFp8G64Row || MODE == kFp8G64Col) ? 64 : 0;
+    static constexpr bool col = (MODE == kFp8G128Col || MODE == kFp8G64Col);
+    static constexpr bool needs_scale_in = (MODE == kFp8Static || MODE == kNvfp4);
+};
+
+// h = T(x + r) for the thread's chunks (h = x without a residual), the
+// residual write-back, and the thread's partial of the sum-of-squares tree.
+// Chunks at or beyond `chunks` hold zeros and are not stored.
+template <class E, bool RES, int J>
+__device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
+                                                uint32_t (&hw)[J][4], uint4* res_out_row,
+                                                int c0, int chunks) {
+    float part[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        if constexpr (RES) {
+            const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                hw[j][k] = E::pack(__fadd_rn(E::lo(xs[k]), E::lo(rs[k])),
+                                   __fadd_rn(E::hi(xs[k]), E::hi(rs[k])));
+            if (c0 + j < chunks)
+                st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) hw[j][k] = xs[k];
+        }
+        float h[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { h[2 * k] = E::lo(hw[j][k]); h[2 * k + 1] = E::hi(hw[j][k]); }
+        part[j] = leaf8_sumsq(h);
+    }
+    static_assert(J == 1 || J == 2 || J == 4, "J must be 1, 2 or 4");
+    if constexpr (J == 1) return part[0];
+    else if constexpr (J == 2) return __fadd_rn(part[0], part[1]);
+    else return __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+}
+
+// 1 / sqrt(S / hidden + eps), each step correctly rounded.
+__device__ __forceinline__ float inv_rms(float total, int hidden, float eps) {
+    const float ms = __fdiv_rn(total, (float)hidden);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+}
+
+// y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
+// `sin` is the static scale (FP8 static) or the global scale (NVFP4).
+// FP8 per-token does a CTA-wide amax through `s_max` (32 floats) and one
+// __syncthreads; every thread of the CTA must call this.
+template <class E, int MODE, int J>
+__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
+                                             const uint4 (&wv)[J], float inv, float sin,
+                                             float* s_max, int tid, int nwarps) {
+    const int lane = tid & 31, warp = tid >> 5;
+    const int c0 = tid * J;
+    float y[J][8];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
+            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
+        }
+    }
+
+    if constexpr (MODE == kNvfp4) {
+        // 16-element blocks = chunk pairs (2m, 2m+1): a lane pair when J == 1,
+        // inside the thread otherwise.
+        const float gs = sin;
+        uint8_t* bsc = static_cast<uint8_t*>(a.scales) + (int64_t)row * (a.hidden / 16);
+        uint32_t* qrow = reinterpret_cast<uint32_t*>(a.q + (int64_t)row * (a.hidden / 2));
+#pragma unroll
+        for (int j = 0; j < J; j += (J == 1 ? 1 : 2)) {
+            float m = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+            if constexpr (J == 1) {
+                m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j + 1][k]));
+            }
+            const uint32_t sb = e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), gs), 0.0f) & 0xffu;
+            const float d = e4m3_value_nonneg(sb);
+            const float r = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+            const int c = c0 + j;
+            constexpr int NC = (J == 1) ? 1 : 2;
+#pragma unroll
+            for (int u = 0; u < NC; ++u) {
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(y[j + u][k], r);
+                if (c + u < a.chunks) st_stream(qrow + c + u, e2m1x8(v));
+            }
+            if (c < a.chunks && (c & 1) == 0) bsc[c >> 1] = (uint8_t)sb;
+        }
+    } else {
+        float s;
+        if constexpr (MODE == kFp8Static) {
+            s = sin;
+        } else if constexpr (MODE == kFp8PerToken) {
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+            m = lanes_max<32>(m);
+            if (lane == 0) s_max[warp] = m;
+            __syncthreads();
+            m = lanes_max<32>(lane < nwarps ? s_max[lane] : 0.0f);
+            s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+            if (tid == 0) static_cast<float*>(a.scales)[row] = s;
+        } else {
+            constexpr int G = ModeTraits<MODE>::group;
+            constexpr int LANES = G / 8 / J;   // threads sharing one group
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+            m = lanes_max<LANES>(m);
+            s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+            if (c0 < a.chunks && (c0 % (G / 8)) == 0) {
+                const int g = c0 / (G / 8);
+                float* sc = static_cast<float*>(a.scales);
+                if constexpr (ModeTraits<MODE>::col) sc[(int64_t)g * a.n + row] = s;
+                else sc[(int64_t)row * (a.hidden / G) + g] = s;
+            }
+        }
+        const Fp8Recips rc = fp8_recips(s);
+        uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const uint2 codes = fp8_chunk(y[j], s, rc);
+            if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
+        }
+    }
+}
+
+}  // namespace rmsq

@@ -5,4 +5,6 @@ namespace rmsq {
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream) {
     return launch_rows<Bf16T>(a, stream);
 }
+
+cudaError_t take_pipe_fault_bf16(unsigned int* out) { return take_pipe_fault(out); }
 }  // namespace rmsq

@@ -5,6 +5,8 @@ Bar (the stated tolerance of the path): residual_out and scales bit-exact;
 quantised codes bit-exact except at most 1 code step on at most 1e-4 of the
 elements.  The CUDA path is designed to be bit-exact everywhere, so the
 mismatch counts are reported and the tests also require them to be zero.
+Every check runs both kernel variants (direct and pipelined) on the same
+inputs.
 """
 from __future__ import annotations
 
@@ -16,6 +18,7 @@ import residual_add_rmsnorm_rmsq_gb300 as rq
 
 MAX_MISMATCH_FRAC = 1e-4
 MAX_STEP = 1
+VARIANTS = ("direct", "pipelined")
 _TDT = {"bf16": torch.bfloat16, "fp16": torch.float16}
 
 
@@ -27,15 +30,17 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run_gpu(wl, mode: str, scale_in: float | None, *, in_place: bool = False, stream=None):
+def run_gpu(wl, mode: str, scale_in: float | None, *, in_place: bool = False, stream=None,
+            variant: str = "auto"):
     x = dev_act(wl.x, wl.dtype)
     r = None if wl.residual is None else dev_act(wl.residual, wl.dtype)
     w = dev_act(wl.weight, wl.dtype)
     s = torch.tensor([scale_in if scale_in is not None else 0.0], dtype=torch.float32, device="cuda")
     q, sc, ro = rq.fused_add_rmsnorm_quant(x, r, w, wl.eps, mode, s,
                                            residual_out=r if (in_place and r is not None) else None,
-                                           stream=stream)
+                                           stream=stream, variant=variant)
     torch.cuda.synchronize()
+    assert rq.take_fault_flags() == 0, "a pipelined CTA gave up waiting for its copies"
     return {"q": q.cpu().numpy(), "scales": None if sc is None else sc.cpu().numpy(),
             "residual_out": None if ro is None else host_bits(ro)}
 
@@ -80,7 +85,10 @@ def compare(got: dict, want: dict, mode: str, label: str = "") -> dict:
 
 
 def check(wl, mode: str, *, scale_in: float | None = None, nthreads: int = 8,
-          in_place: bool = False, label: str | None = None) -> dict:
+          in_place: bool = False, label: str | None = None, variants=VARIANTS) -> list:
     want = oracle.run_workload(wl, mode, scale_in=scale_in, nthreads=nthreads)
-    got = run_gpu(wl, mode, want["scale_in"], in_place=in_place)
-    return compare(got, want, mode, label or f"{wl.name}/{mode}")
+    reports = []
+    for v in variants:
+        got = run_gpu(wl, mode, want["scale_in"], in_place=in_place, variant=v)
+        reports.append(compare(got, want, mode, f"{label or wl.name + '/' + mode}/{v}"))
+    return reports

@@ -47,18 +47,19 @@ def test_golden_rows_on_gpu(ex):
     r = None if ex["residual"] is None else ri.to_bits(fill(ex["residual"], (n, H)), ex["dtype"]).reshape(n, H)
     w = ri.to_bits(fill(ex["weight"], (H,)), ex["dtype"])
     wl = ri.Workload(ex["name"], n, H, ex["dtype"], ex["eps"], x, r, w)
-    got = P.run_gpu(wl, ex["mode"], ex["scale_in"])
-    q = got["q"].ravel()
-    b = bytes.fromhex(ex["expect"]["q_hex"])
-    want = np.frombuffer(b * (q.size // len(b)) if len(b) < q.size else b, np.uint8)
-    assert np.array_equal(q, want), (q.tobytes().hex(), ex["expect"]["q_hex"])
-    e = ex["expect"]
-    if "residual_out_hex" in e:
-        assert np.all(got["residual_out"] == int(e["residual_out_hex"], 16))
-    if "scales_f32_bits" in e:
-        assert np.all(got["scales"].view(np.uint32) == int(e["scales_f32_bits"][0], 16))
-    if "scales_u8_hex" in e:
-        assert np.all(got["scales"] == int(e["scales_u8_hex"][0], 16))
+    for variant in P.VARIANTS:
+        got = P.run_gpu(wl, ex["mode"], ex["scale_in"], variant=variant)
+        q = got["q"].ravel()
+        b = bytes.fromhex(ex["expect"]["q_hex"])
+        want = np.frombuffer(b * (q.size // len(b)) if len(b) < q.size else b, np.uint8)
+        assert np.array_equal(q, want), (variant, q.tobytes().hex(), ex["expect"]["q_hex"])
+        e = ex["expect"]
+        if "residual_out_hex" in e:
+            assert np.all(got["residual_out"] == int(e["residual_out_hex"], 16))
+        if "scales_f32_bits" in e:
+            assert np.all(got["scales"].view(np.uint32) == int(e["scales_f32_bits"][0], 16))
+        if "scales_u8_hex" in e:
+            assert np.all(got["scales"] == int(e["scales_u8_hex"][0], 16))
 
 
 # ---------------------------------------------------------------- the five workloads
