@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused add-RMSNorm+quant HBM GB/s and tokens/s on 1 GB300 vs ~8 TB/s peak"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
+VARIANT = "auto"       # kernel variant for every launch (set by --variant)
 
 
 # --------------------------------------------------------------------------- bytes
@@ -209,7 +210,7 @@ def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
         k = i % bufs.sets
         rq.fused_add_rmsnorm_quant(bufs.x[k], bufs.r[k], bufs.w, wl.eps, mode, bufs.scale_in,
                                    out_q=bufs.q[k], out_scales=bufs.sc[k], residual_out=bufs.ro[k],
-                                   stream=stream)
+                                   stream=stream, variant=VARIANT)
     with torch.cuda.stream(stream):
         for i in range(warmup):
             launch(i)
@@ -243,7 +244,7 @@ def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
             bufs.r[0].copy_(hr, non_blocking=True)
         rq.fused_add_rmsnorm_quant(bufs.x[0], bufs.r[0], bufs.w, wl.eps, mode, bufs.scale_in,
                                    out_q=bufs.q[0], out_scales=bufs.sc[0], residual_out=bufs.ro[0],
-                                   stream=stream)
+                                   stream=stream, variant=VARIANT)
         hq.copy_(bufs.q[0], non_blocking=True)
         if hs is not None:
             hs.copy_(bufs.sc[0], non_blocking=True)
@@ -395,7 +396,7 @@ def run_ours(args, rank, world, dist):
         "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, shapes of the pages' workloads)",
         "tokens_per_s": round(tokens_s, 1),
         "config": {"workload": args.workload, "n_tokens": wl.n_tokens, "hidden": wl.hidden,
-                   "quant_mode": mode, "residual": bufs.res, "eps": wl.eps,
+                   "quant_mode": mode, "residual": bufs.res, "eps": wl.eps, "variant": VARIANT,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"rotating {bufs.sets} buffer sets ({bufs.sets * per_launch / 1e6:.0f} MB > 4x L2)",
                    "bytes_per_step": per_launch},
@@ -451,7 +452,10 @@ def main():
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--variant", choices=["auto", "direct", "pipelined"], default="auto")
     args = ap.parse_args()
+    global VARIANT
+    VARIANT = args.variant
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
