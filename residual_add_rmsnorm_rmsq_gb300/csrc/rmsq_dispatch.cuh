@@ -67,15 +67,33 @@ struct OccEntry {
     int blocks;
 };
 
+// Shared-memory ring budget per CTA (two CTAs per SM).
+constexpr int kPipeSmemBudget = 110 * 1024;
+
+// The opt-in dynamic shared memory limit of a pipelined instantiation is set
+// once, to the full ring budget, so that no later launch ever lowers it below
+// what another launch of the same function needs.
+inline cudaError_t ensure_smem_limit(const void* fn) {
+    static std::mutex mu;
+    static const void* done[256];
+    static int used = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (done[i] == fn) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
+    if (e == cudaSuccess && used < 256) done[used++] = fn;
+    return e;
+}
+
 inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t* err) {
     static std::mutex mu;
     static OccEntry cache[64];
     static int used = 0;
+    *err = ensure_smem_limit(fn);
+    if (*err != cudaSuccess) return 0;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (cache[i].fn == fn && cache[i].smem == smem && cache[i].threads == threads) return cache[i].blocks;
-    *err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (*err != cudaSuccess) return 0;
     int blocks = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, smem);
     if (*err != cudaSuccess) return 0;
@@ -100,8 +118,7 @@ inline int sm_count(cudaError_t* err) {
 // Shared-memory ring per CTA: as many stages (2..8) as fit in ~110 KB, so that
 // two CTAs share an SM; a single stage for rows wider than that.
 inline int pipe_stages(int stage_bytes) {
-    const int budget = 110 * 1024;
-    int s = budget / stage_bytes;
+    int s = kPipeSmemBudget / stage_bytes;
     return s < 1 ? 1 : (s > kMaxStages ? kMaxStages : s);
 }
 

@@ -191,3 +191,10 @@ def test_non_default_stream():
     with torch.cuda.stream(s):
         got = P.run_gpu(wl, "fp8_group128_row", None, stream=s)
     P.compare(got, want, "fp8_group128_row", "side stream")
+
+
+def test_pipelined_ring_sizes_in_any_order():
+    """One pipelined instantiation launched with shrinking and growing rings."""
+    for H in (16, 8, 2048, 8, 16, 2048):
+        wl = ri.make_workload(f"ring_{H}", 5, H, seed=35 + H)
+        P.check(wl, "fp8_per_token", variants=("pipelined",), label=f"ring/{H}")
