@@ -205,20 +205,46 @@ class Buffers:
 
 
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
-    """Mean device time per launch (ms) over `steps` launches, CUDA events on `stream`."""
+    """Mean device time per launch (ms) over exactly `steps` launches, CUDA
+    events on `stream`.
+
+    The launches (one per buffer set, in rotation order) are captured once in
+    a CUDA graph through the same public call; the timed region replays it
+    steps // sets times plus a graph of the remaining launches, so the device
+    runs the K kernels back to back instead of waiting on Python between
+    them.  Eager warm-up launches come first (they also fill the library's
+    per-function caches before capture).
+    """
     def launch(i):
         k = i % bufs.sets
         rq.fused_add_rmsnorm_quant(bufs.x[k], bufs.r[k], bufs.w, wl.eps, mode, bufs.scale_in,
                                    out_q=bufs.q[k], out_scales=bufs.sc[k], residual_out=bufs.ro[k],
                                    stream=stream, variant=VARIANT)
+
+    def capture(count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(count):
+                launch(i)
+        return g
+
     with torch.cuda.stream(stream):
-        for i in range(warmup):
+        for i in range(max(warmup, bufs.sets)):
             launch(i)
+        torch.cuda.synchronize()
+        reps, rem = divmod(steps, bufs.sets)
+        g_full = capture(bufs.sets) if reps else None
+        g_rem = capture(rem) if rem else None
+        for g in (g_full, g_rem):          # one untimed replay of each graph
+            if g is not None:
+                g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(steps):
-            launch(warmup + i)
+        for _ in range(reps):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     return e0.elapsed_time(e1) / steps

@@ -36,9 +36,9 @@ MAX_HIDDEN = 16384
 
 VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 
-EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex", "rmsq_take_fault_flags",
-           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_status_string", "rmsq_last_cuda_error",
-           "rmsq_version")
+EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex", "rmsq_set_pipeline_config",
+           "rmsq_take_fault_flags", "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_status_string",
+           "rmsq_last_cuda_error", "rmsq_version")
 
 
 class RmsqError(RuntimeError):
@@ -70,6 +70,8 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm_quant_ex.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci,
                                                       vp, ci]
         L.rmsq_fused_add_rmsnorm_quant_ex.restype = ci
+        L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci]
+        L.rmsq_set_pipeline_config.restype = ci
         L.rmsq_take_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.rmsq_take_fault_flags.restype = ci
         L.rmsq_query_sizes.argtypes = [ci, i64, i64, ctypes.POINTER(ctypes.c_size_t),
@@ -161,6 +163,13 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
+
+
+def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm: int = 0) -> None:
+    """Tune the pipelined variant's launch shape (0 = automatic); results are unchanged."""
+    st = load().rmsq_set_pipeline_config(chunks_per_thread, stages, ctas_per_sm)
+    if st:
+        raise RmsqError(st, "rmsq_set_pipeline_config")
 
 
 def take_fault_flags() -> int:

@@ -145,16 +145,24 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
                 (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
 
     if (pipe) {
-        const int J = a.chunks <= 256 ? 1 : (a.chunks <= 512 ? 2 : 4);
-        const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
+        const PipeTuning tune = get_pipe_tuning();
+        auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
+        int J = a.chunks <= 256 ? 1 : (a.chunks <= 512 ? 2 : 4);
+        if ((tune.chunks_per_thread == 1 || tune.chunks_per_thread == 2 || tune.chunks_per_thread == 4) &&
+            threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
+            J = tune.chunks_per_thread;
+        const int threads = threads_for(J);
         const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);
-        const int stages = pipe_stages(stage_bytes);
+        int stages = pipe_stages(stage_bytes);
+        if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
+            stages = tune.stages;
         const int smem = stages * stage_bytes;
         const void* fn = pick_kernel<E>(la.mode, res, true, J);
         if (!fn) return cudaErrorInvalidValue;
-        const int per_sm = pipe_blocks_per_sm(fn, threads, smem, &err);
+        int per_sm = pipe_blocks_per_sm(fn, threads, smem, &err);
         if (err != cudaSuccess) return err;
         if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        if (tune.ctas_per_sm >= 1 && tune.ctas_per_sm < per_sm) per_sm = tune.ctas_per_sm;
         const int grid = a.n < per_sm * sms ? a.n : per_sm * sms;
         int st = stages;
         void* params[] = {&a, &st};

@@ -27,6 +27,15 @@ constexpr int kVariantPipelined = 2;
 // The pipelined kernel is chosen automatically from this many rows per SM.
 constexpr int kPipeMinRowsPerSm = 4;
 
+// Process-wide overrides of the pipelined launch shape (0 = automatic).
+struct PipeTuning {
+    int chunks_per_thread;
+    int stages;
+    int ctas_per_sm;
+};
+PipeTuning get_pipe_tuning();
+void set_pipe_tuning(const PipeTuning& t);
+
 // One launch of the row kernel for bf16 / fp16 activations.
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);

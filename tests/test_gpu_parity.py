@@ -193,6 +193,18 @@ def test_non_default_stream():
     P.compare(got, want, "fp8_group128_row", "side stream")
 
 
+def test_pipelined_launch_shapes_do_not_change_results():
+    wl = ri.make_workload("shapes", 700, 4096, res_sigma=2.0, seed=36)
+    want = oracle.run_workload(wl, "fp8_group64_col", nthreads=8)
+    try:
+        for J, stages, cps in ((1, 2, 1), (2, 1, 2), (4, 8, 3), (2, 6, 0), (0, 3, 4)):
+            rq.set_pipeline_config(J, stages, cps)
+            got = P.run_gpu(wl, "fp8_group64_col", None, variant="pipelined")
+            P.compare(got, want, "fp8_group64_col", f"shape J{J} s{stages} c{cps}")
+    finally:
+        rq.set_pipeline_config(0, 0, 0)
+
+
 def test_pipelined_ring_sizes_in_any_order():
     """One pipelined instantiation launched with shrinking and growing rings."""
     for H in (16, 8, 2048, 8, 16, 2048):
