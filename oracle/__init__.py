@@ -48,31 +48,58 @@ def compile_oracle(force: bool = False) -> str:
 
 
 def lib():
+    """The oracle library; ORACLE_LIB=<path> loads another build of the same
+    source instead (used by the planted-mistake tests)."""
     global _lib
     with _lock:
         if _lib is None:
-            L = ctypes.CDLL(compile_oracle())
-            f32, u8, u16, i64, vp = (ctypes.c_float, ctypes.c_uint8, ctypes.c_uint16,
-                                     ctypes.c_int64, ctypes.c_void_p)
-            L.oracle_bf16_to_float.argtypes, L.oracle_bf16_to_float.restype = [u16], f32
-            L.oracle_fp16_to_float.argtypes, L.oracle_fp16_to_float.restype = [u16], f32
-            L.oracle_float_to_bf16.argtypes, L.oracle_float_to_bf16.restype = [f32], u16
-            L.oracle_float_to_fp16.argtypes, L.oracle_float_to_fp16.restype = [f32], u16
-            L.oracle_e4m3_encode.argtypes, L.oracle_e4m3_encode.restype = [f32], u8
-            L.oracle_e4m3_decode.argtypes, L.oracle_e4m3_decode.restype = [u8], f32
-            L.oracle_e2m1_encode.argtypes, L.oracle_e2m1_encode.restype = [f32], u8
-            L.oracle_e2m1_decode.argtypes, L.oracle_e2m1_decode.restype = [u8], f32
-            L.oracle_tree_sum.argtypes, L.oracle_tree_sum.restype = [vp, i64], f32
-            for name in ("oracle_e4m3_encode_array", "oracle_e2m1_encode_array",
-                         "oracle_float_to_bf16_array", "oracle_float_to_fp16_array"):
-                getattr(L, name).argtypes = [vp, vp, i64]
-                getattr(L, name).restype = None
-            L.oracle_fused_add_rmsnorm_quant.argtypes = [
-                vp, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int,
-                ctypes.c_int]
-            L.oracle_fused_add_rmsnorm_quant.restype = ctypes.c_int
-            _lib = L
+            path = os.environ.get("ORACLE_LIB") or compile_oracle()
+            _lib = _configure(ctypes.CDLL(path))
     return _lib
+
+
+class use_library:
+    """Context manager: route every oracle call to another build of the C
+    source (the tests use it to plant mistakes and check the pins catch them)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        lib()
+        self.saved = _lib
+        _lib = _configure(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def _configure(L):
+    """Declare the C signatures on a loaded oracle library."""
+    f32, u8, u16, i64, vp = (ctypes.c_float, ctypes.c_uint8, ctypes.c_uint16,
+                             ctypes.c_int64, ctypes.c_void_p)
+    L.oracle_bf16_to_float.argtypes, L.oracle_bf16_to_float.restype = [u16], f32
+    L.oracle_fp16_to_float.argtypes, L.oracle_fp16_to_float.restype = [u16], f32
+    L.oracle_float_to_bf16.argtypes, L.oracle_float_to_bf16.restype = [f32], u16
+    L.oracle_float_to_fp16.argtypes, L.oracle_float_to_fp16.restype = [f32], u16
+    L.oracle_e4m3_encode.argtypes, L.oracle_e4m3_encode.restype = [f32], u8
+    L.oracle_e4m3_decode.argtypes, L.oracle_e4m3_decode.restype = [u8], f32
+    L.oracle_e2m1_encode.argtypes, L.oracle_e2m1_encode.restype = [f32], u8
+    L.oracle_e2m1_decode.argtypes, L.oracle_e2m1_decode.restype = [u8], f32
+    L.oracle_tree_sum.argtypes, L.oracle_tree_sum.restype = [vp, i64], f32
+    for name in ("oracle_e4m3_encode_array", "oracle_e2m1_encode_array",
+                 "oracle_float_to_bf16_array", "oracle_float_to_fp16_array"):
+        getattr(L, name).argtypes = [vp, vp, i64]
+        getattr(L, name).restype = None
+    L.oracle_fused_add_rmsnorm_quant.argtypes = [
+        vp, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int,
+        ctypes.c_int]
+    L.oracle_fused_add_rmsnorm_quant.restype = ctypes.c_int
+    return L
 
 
 def _ptr(a):

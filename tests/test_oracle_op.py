@@ -100,6 +100,8 @@ def _small_workloads():
         ri.make_workload("fp16_t3", 9, 1024, dtype="fp16", dist="t3", t_clamp=500.0,
                          n_outliers=8, outlier_mult=50.0, eps=1e-5, seed=5),
         ri.make_workload("bf16_outl", 12, 768, n_outliers=8, outlier_mult=20.0, seed=6),
+        # mean square comparable to eps, so that eps visibly changes y
+        ri.make_workload("bf16_tiny", 10, 256, x_sigma=1e-3, res_sigma=1e-3, eps=1e-6, seed=7),
     ]
 
 
