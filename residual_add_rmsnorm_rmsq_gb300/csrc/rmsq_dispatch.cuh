@@ -5,7 +5,11 @@
 //             hidden 8192, else 2), loads straight into registers.
 //  pipelined: persistent CTAs (as many as fit on the SMs), `stages` rows of
 //             x / residual in flight per CTA through the shared-memory ring.
-//             J = 1 up to hidden 2048, 2 up to 4096, else 4 (<= 512 threads).
+//             J = 2 up to hidden 8192, else 4 (<= 512 threads); two stages
+//             per CTA by default, so that up to 3-4 CTAs share an SM: the
+//             per-row dependency chain (two block reductions, IEEE divide and
+//             square root) rather than bytes in flight limits a CTA, so more
+//             CTAs per SM beat a deeper ring (measured on GB300).
 #pragma once
 
 #include <atomic>
@@ -115,12 +119,9 @@ inline int sm_count(cudaError_t* err) {
     return v;
 }
 
-// Shared-memory ring per CTA: as many stages (2..8) as fit in ~110 KB, so that
-// two CTAs share an SM; a single stage for rows wider than that.
-inline int pipe_stages(int stage_bytes) {
-    int s = kPipeSmemBudget / stage_bytes;
-    return s < 1 ? 1 : (s > kMaxStages ? kMaxStages : s);
-}
+// Default ring: two stages (one row computed while the next is in flight),
+// one when two do not fit the budget.
+inline int pipe_stages(int stage_bytes) { return 2 * stage_bytes <= kPipeSmemBudget ? 2 : 1; }
 
 template <class E>
 cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
@@ -147,7 +148,7 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     if (pipe) {
         const PipeTuning tune = get_pipe_tuning();
         auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
-        int J = a.chunks <= 256 ? 1 : (a.chunks <= 512 ? 2 : 4);
+        int J = a.chunks <= 1024 ? 2 : 4;
         if ((tune.chunks_per_thread == 1 || tune.chunks_per_thread == 2 || tune.chunks_per_thread == 4) &&
             threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
             J = tune.chunks_per_thread;
