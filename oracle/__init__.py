@@ -99,6 +99,9 @@ def _configure(L):
         vp, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int,
         ctypes.c_int]
     L.oracle_fused_add_rmsnorm_quant.restype = ctypes.c_int
+    L.oracle_fused_add_rmsnorm_nvfp4_dynamic.argtypes = [
+        vp, vp, vp, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int]
+    L.oracle_fused_add_rmsnorm_nvfp4_dynamic.restype = ctypes.c_int
     return L
 
 
@@ -194,6 +197,26 @@ def run(x, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return {"q": q, "scales": scales, "residual_out": res_out, "y": y}
+
+
+def run_nvfp4_dynamic(x, residual, weight, *, eps: float, dtype: str = "bf16",
+                      nthreads: int = 1) -> dict:
+    """NVFP4 with gs = 2688 / amax(all y) computed inside the oracle (1 when
+    amax is 0).  Returns q, scales (block scales), residual_out and gs."""
+    x = np.ascontiguousarray(x, np.uint16)
+    n, H = x.shape
+    weight = np.ascontiguousarray(weight, np.uint16)
+    res = None if residual is None else np.ascontiguousarray(residual, np.uint16)
+    q = np.zeros((n, H // 2), np.uint8)
+    sc = np.zeros((n, H // 16), np.uint8)
+    ro = None if res is None else np.zeros((n, H), np.uint16)
+    gs = np.zeros(1, np.float32)
+    rc = lib().oracle_fused_add_rmsnorm_nvfp4_dynamic(
+        _ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), _ptr(q), _ptr(sc), _ptr(gs),
+        _ptr(ro), n, H, DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": sc, "residual_out": ro, "global_scale": gs}
 
 
 def nvfp4_global_scale(y_amax: float) -> float:

@@ -37,6 +37,7 @@
  *     block (0 when the block scale is 0); q = e2m1(y * r).
  *  R7 E2M1 nibble order: element 2j in the low nibble of byte j.
  *  R8 column-major group scales use stride n_tokens.
+ *  R14 dynamic NVFP4 global scale: gs = 1 when amax over the batch is 0.
  *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
  */
 #include <math.h>
@@ -376,6 +377,43 @@ int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
         if (!spans[i].ok) rc = -2;
     free(spans);
     free(th);
+    return rc;
+}
+
+/* NVFP4 with the global scale taken from the data: gs = 448 * 6 / amax over
+ * every y of the batch (the NVFP4 workload's definition of the global scale),
+ * reading R14: gs = 1 when that amax is 0 (an all-zero batch).  First pass: the
+ * op up to y for every row (residual written back) and the batch amax; second
+ * pass: the NVFP4 quantisation of y with that gs.  *out_gs receives gs.
+ * Returns 0, or -1 / -2 like oracle_fused_add_rmsnorm_quant. */
+int oracle_fused_add_rmsnorm_nvfp4_dynamic(const uint16_t *x, const uint16_t *residual,
+                                           const uint16_t *weight, float eps, uint8_t *out_q,
+                                           uint8_t *out_block_scales, float *out_gs,
+                                           uint16_t *residual_out, int64_t n, int64_t H, int dtype,
+                                           int nthreads)
+{
+    if (n < 0 || H <= 0 || H % 16 || !out_gs) return -1;
+    float *y = (float *)malloc((size_t)(n > 0 ? n : 1) * (size_t)H * sizeof(float));
+    if (!y) return -2;
+    /* pass 1: per-token FP8 run, only for its y (codes and scales discarded) */
+    uint8_t *tmp_q = (uint8_t *)malloc((size_t)(n > 0 ? n : 1) * (size_t)H);
+    float *tmp_s = (float *)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+    int rc = (tmp_q && tmp_s) ? 0 : -2;
+    if (!rc)
+        rc = oracle_fused_add_rmsnorm_quant(x, residual, weight, eps, OR_FP8_PER_TOKEN, 0.0f, tmp_q,
+                                            tmp_s, residual_out, y, n, H, dtype, nthreads);
+    float amax = 0.0f;
+    for (int64_t i = 0; !rc && i < n * H; ++i) amax = fmaxf(amax, fabsf(y[i]));
+    float gs = (amax > 0.0f) ? 2688.0f / amax : 1.0f;
+    /* pass 2: NVFP4 with gs, on the same inputs (y is recomputed identically) */
+    if (!rc)
+        rc = oracle_fused_add_rmsnorm_quant(x, residual, weight, eps, OR_NVFP4, gs, out_q,
+                                            out_block_scales, residual_out, NULL, n, H, dtype,
+                                            nthreads);
+    if (!rc) *out_gs = gs;
+    free(y);
+    free(tmp_q);
+    free(tmp_s);
     return rc;
 }
 

@@ -17,12 +17,22 @@ constexpr unsigned kFull = 0xffffffffu;
 // Activation types: unpack one 32-bit word (two elements, the lower-addressed
 // element in bits 0..15) to fp32, and pack two fp32 with round-to-nearest-even.
 // ---------------------------------------------------------------------------
+// add2: element-wise sum of two packed pairs, rounded once to nearest even.
+// That equals rounding the fp32 sum to T: two values of T (8 / 11 significant
+// bits) add exactly in fp32 unless their exponents are more than 15 / 13
+// apart, and then the smaller one is below half an ulp of T, so neither
+// rounding path can land on a tie of T and both give the larger operand.
 struct Bf16T {
     static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
     static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
     static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
         uint32_t r;
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
         return r;
     }
 };
@@ -41,6 +51,11 @@ struct Fp16T {
     static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
         uint32_t r;
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+        return r;
+    }
+    static __device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        uint32_t r;
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
         return r;
     }
 };
@@ -110,22 +125,16 @@ __device__ __forceinline__ float e4m3_value_nonneg(uint32_t c) {
                   : __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// E4M3 codes of y0/s and y1/s where each quotient is the correctly rounded
-// fp32 division.  Fast path: multiply by two bracketing reciprocals
-// rdn = RN(RN(1/s) * (1 - 2^-20)) and rup = RN(RN(1/s) * (1 + 2^-20)).  The
-// products lie strictly below / above the rounded quotient in magnitude (the
-// three roundings involved move a value by less than 3 * 2^-24 relative),
-// and the saturating nearest-even E4M3 cast is monotone, so equal codes at
-// both ends are the code of the quotient.  Otherwise (about one pair in
-// 2^15) the quotients are computed with __fdiv_rn.
-__device__ __forceinline__ uint32_t fp8_pair(float y0, float y1, float rdn, float rup, float s) {
-    const uint32_t cd = e4m3x2(__fmul_rn(y0, rdn), __fmul_rn(y1, rdn));
-    const uint32_t cu = e4m3x2(__fmul_rn(y0, rup), __fmul_rn(y1, rup));
-    if (cd == cu) return cd;
-    return e4m3x2(__fdiv_rn(y0, s), __fdiv_rn(y1, s));
-}
+// E4M3 codes of y/s where the quotient is the correctly rounded fp32
+// division, without a division per element: multiply by two bracketing
+// reciprocals rdn = RN(RN(1/s) * (1 - 2^-20)) and rup = RN(RN(1/s) * (1 + 2^-20)).
+// The products lie strictly below / above the rounded quotient in magnitude
+// (the three roundings involved move a value by less than 3 * 2^-24
+// relative), and the saturating nearest-even E4M3 cast is monotone, so equal
+// codes at both ends are the code of the quotient.  Otherwise (about one
+// element in 2^16) the quotient is computed with __fdiv_rn.
 
-// Bracketing reciprocals of a scale s for fp8_pair.
+// Bracketing reciprocals of a scale s.
 struct Fp8Recips {
     float rdn, rup;
 };
@@ -135,11 +144,28 @@ __device__ __forceinline__ Fp8Recips fp8_recips(float s) {
             __fmul_rn(r, 1.00000095367431640625f)};    // 1 + 2^-20
 }
 
-// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.
+// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.  The
+// bracketing test of fp8_pair is applied to the whole chunk at once (one
+// branch per eight elements); the rare chunk with a code that differs between
+// the two ends is redone with correctly rounded divisions.
 __device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s, Fp8Recips rc) {
+    uint32_t dn[4], up[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        dn[p] = e4m3x2(__fmul_rn(v[2 * p], rc.rdn), __fmul_rn(v[2 * p + 1], rc.rdn));
+        up[p] = e4m3x2(__fmul_rn(v[2 * p], rc.rup), __fmul_rn(v[2 * p + 1], rc.rup));
+    }
     uint2 out;
-    out.x = fp8_pair(v[0], v[1], rc.rdn, rc.rup, s) | (fp8_pair(v[2], v[3], rc.rdn, rc.rup, s) << 16);
-    out.y = fp8_pair(v[4], v[5], rc.rdn, rc.rup, s) | (fp8_pair(v[6], v[7], rc.rdn, rc.rup, s) << 16);
+    out.x = dn[0] | (dn[1] << 16);
+    out.y = dn[2] | (dn[3] << 16);
+    const uint32_t ux = up[0] | (up[1] << 16), uy = up[2] | (up[3] << 16);
+    if (((out.x ^ ux) | (out.y ^ uy)) != 0u) {
+        uint32_t ex[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) ex[p] = e4m3x2(__fdiv_rn(v[2 * p], s), __fdiv_rn(v[2 * p + 1], s));
+        out.x = ex[0] | (ex[1] << 16);
+        out.y = ex[2] | (ex[3] << 16);
+    }
     return out;
 }
 

@@ -71,7 +71,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         const uint32_t parity = static_cast<uint32_t>(k / stages) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity);
 
-        uint32_t hw[J][4];
+        float h[J][8];
         float acc = 0.0f;
         if (ok) {
             const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)s * stage_bytes);
@@ -84,7 +84,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                     if constexpr (RES) rv[j] = sx[a.chunks + c0 + j];
                 }
             }
-            acc = combine_chunks<E, RES, J>(xv, rv, hw, a.res_out + (int64_t)row * a.chunks, c0, a.chunks);
+            acc = combine_chunks<E, RES, J>(xv, rv, h, a.res_out + (int64_t)row * a.chunks, c0, a.chunks);
         }
         acc = warp_tree_sum(acc);
         if (lane == 0) s_sum[k & 1][warp] = acc;
@@ -105,7 +105,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         }
         const float total = warp_tree_sum(lane < nwarps ? s_sum[k & 1][lane] : 0.0f);
         const float inv = inv_rms(total, a.hidden, a.eps);
-        quantize_row<E, MODE, J>(a, row, hw, wv, inv, sin, s_max[k & 1], tid, nwarps);
+        quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_max[k & 1], tid, nwarps);
     }
 
     if (faulted && tid == 0) {

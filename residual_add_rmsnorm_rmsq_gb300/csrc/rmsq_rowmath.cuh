@@ -55,28 +55,22 @@ template <int MODE> struct ModeTraits {
 // Chunks at or beyond `chunks` hold zeros and are not stored.
 template <class E, bool RES, int J>
 __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
-                                                uint32_t (&hw)[J][4], uint4* res_out_row,
+                                                float (&h)[J][8], uint4* res_out_row,
                                                 int c0, int chunks) {
     float part[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        uint32_t hw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
         if constexpr (RES) {
             const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                hw[j][k] = E::pack(__fadd_rn(E::lo(xs[k]), E::lo(rs[k])),
-                                   __fadd_rn(E::hi(xs[k]), E::hi(rs[k])));
+            for (int k = 0; k < 4; ++k) hw[k] = E::add2(hw[k], rs[k]);
             if (c0 + j < chunks)
-                st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) hw[j][k] = xs[k];
+                st_stream(res_out_row + c0 + j, make_uint4(hw[0], hw[1], hw[2], hw[3]));
         }
-        float h[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) { h[2 * k] = E::lo(hw[j][k]); h[2 * k + 1] = E::hi(hw[j][k]); }
-        part[j] = leaf8_sumsq(h);
+        for (int k = 0; k < 4; ++k) { h[j][2 * k] = E::lo(hw[k]); h[j][2 * k + 1] = E::hi(hw[k]); }
+        part[j] = leaf8_sumsq(h[j]);
     }
     static_assert(J == 1 || J == 2 || J == 4, "J must be 1, 2 or 4");
     if constexpr (J == 1) return part[0];
@@ -95,7 +89,7 @@ __device__ __forceinline__ float inv_rms(float total, int hidden, float eps) {
 // FP8 per-token does a CTA-wide amax through `s_max` (32 floats) and one
 // __syncthreads; every thread of the CTA must call this.
 template <class E, int MODE, int J>
-__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
+__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const float (&h)[J][8],
                                              const uint4 (&wv)[J], float inv, float sin,
                                              float* s_max, int tid, int nwarps) {
     const int lane = tid & 31, warp = tid >> 5;
@@ -106,8 +100,8 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
         const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
-            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
+            y[j][2 * k] = __fmul_rn(__fmul_rn(h[j][2 * k], inv), E::lo(ws[k]));
+            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(h[j][2 * k + 1], inv), E::hi(ws[k]));
         }
     }
 

@@ -30,14 +30,14 @@ __global__ void __launch_bounds__(1024) rows_kernel(const RowArgs a) {
     }
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
 
-    uint32_t hw[J][4];
-    float acc = combine_chunks<E, RES, J>(xv, rv, hw, a.res_out + base, c0, a.chunks);
+    float h[J][8];
+    float acc = combine_chunks<E, RES, J>(xv, rv, h, a.res_out + base, c0, a.chunks);
     acc = warp_tree_sum(acc);
     if (lane == 0) s_sum[warp] = acc;
     __syncthreads();
     const float total = warp_tree_sum(lane < nwarps ? s_sum[lane] : 0.0f);
     const float inv = inv_rms(total, a.hidden, a.eps);
-    quantize_row<E, MODE, J>(a, row, hw, wv, inv, sin, s_max, tid, nwarps);
+    quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_max, tid, nwarps);
 }
 
 }  // namespace rmsq

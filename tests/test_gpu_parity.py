@@ -193,6 +193,27 @@ def test_non_default_stream():
     P.compare(got, want, "fp8_group128_row", "side stream")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_subnormal_zero_and_wide_range_inputs(dtype):
+    """Log-uniform magnitudes from the subnormal range of the activation type
+    up to 2^10, random signs, exact +-0: the packed residual add, the squares
+    and the quantisation must still match the oracle bit for bit."""
+    n, H = 64, 1024
+    u = ri.uniform(77, 1, 3 * n * H)
+    lo = -133.0 if dtype == "bf16" else -24.0
+    mag = 2.0 ** (lo + (10.0 - lo) * u[: 2 * n * H])
+    sign = np.where(u[n * H: 3 * n * H] < 0.5, -1.0, 1.0)
+    vals = mag * sign
+    vals[::97] = 0.0
+    vals[1::101] = -0.0
+    x = ri.to_bits(vals[: n * H], dtype).reshape(n, H)
+    r = ri.to_bits(vals[n * H:], dtype).reshape(n, H)
+    w = ri.to_bits(1.0 + 0.1 * ri.normal(78, 1, H), dtype)
+    wl = ri.Workload(f"wide_{dtype}", n, H, dtype, 1e-6, x, r, w)
+    for mode in ("fp8_static", "fp8_per_token", "fp8_group64_row", "nvfp4"):
+        P.check(wl, mode, scale_in=0.5 if mode == "fp8_static" else None, label=f"wide/{dtype}/{mode}")
+
+
 def test_pipelined_launch_shapes_do_not_change_results():
     wl = ri.make_workload("shapes", 700, 4096, res_sigma=2.0, seed=36)
     want = oracle.run_workload(wl, "fp8_group64_col", nthreads=8)

@@ -243,3 +243,40 @@ def test_static_scale_direction(orc):
     ratio = np.abs(a["y"] / np.float32(0.01))
     ok = (ratio >= 2.0 ** -5) & (ratio <= 440.0)
     assert np.all((a["q"] & 0x7f)[ok].astype(int) - (b["q"] & 0x7f)[ok].astype(int) == 8)
+
+
+# ------------------------------------------------------------------ NVFP4 with a data-derived global scale
+def test_nvfp4_dynamic_all_twos_row(orc):
+    """All-twos row: y = 1 everywhere, so amax = 1 and gs = 2688 = 0x45280000;
+    then exactly the hand-worked static row: block scale 0x7E, bytes 0x77."""
+    x = ri.to_bits(np.ones((3, 32)), "bf16").reshape(3, 32)
+    w = ri.to_bits(np.ones(32), "bf16")
+    out = orc.run_nvfp4_dynamic(x, x, w, eps=0.0)
+    assert out["global_scale"].view(np.uint32)[0] == 0x45280000
+    assert np.all(out["q"] == 0x77) and np.all(out["scales"] == 0x7E)
+    assert np.all(out["residual_out"] == 0x4000)
+
+
+def test_nvfp4_dynamic_all_zero_batch(orc):
+    """amax = 0: the global scale falls back to 1 and every code is +0."""
+    x = np.zeros((2, 64), np.uint16)
+    w = ri.to_bits(np.ones(64), "bf16")
+    out = orc.run_nvfp4_dynamic(x, None, w, eps=1e-6)
+    assert out["global_scale"][0] == 1.0
+    assert not out["q"].any() and not out["scales"].any()
+
+
+@pytest.mark.parametrize("wl", _small_workloads(), ids=lambda w: w.name)
+def test_nvfp4_dynamic_matches_static_with_batch_amax(orc, wl):
+    if wl.hidden % 16:
+        pytest.skip("hidden not a multiple of 16")
+    dyn = orc.run_nvfp4_dynamic(wl.x, wl.residual, wl.weight, eps=wl.eps, dtype=wl.dtype)
+    pre = orc.run(wl.x, wl.residual, wl.weight, eps=wl.eps, mode="fp8_per_token",
+                  dtype=wl.dtype, want_y=True)
+    amax = np.float32(np.abs(pre["y"]).max())
+    assert dyn["global_scale"][0] == np.float32(2688.0) / amax
+    assert abs(float(dyn["global_scale"][0]) * float(amax) - 2688.0) <= 2688.0 * 2.0 ** -23
+    st = orc.run(wl.x, wl.residual, wl.weight, eps=wl.eps, mode="nvfp4",
+                 scale_in=float(dyn["global_scale"][0]), dtype=wl.dtype)
+    for k in ("q", "scales", "residual_out"):
+        assert np.array_equal(dyn[k], st[k]) if st[k] is not None else dyn[k] is None
