@@ -160,21 +160,23 @@ def workload_spec(name: str):
         "dsv3_fp8_group64_col": (lambda: ri.dsv3(8192), "fp8_group64_col"),
         "qwen_nvfp4_4096": (lambda: ri.qwen_nvfp4(4096), "nvfp4"),
         "qwen_nvfp4_16384": (lambda: ri.qwen_nvfp4(16384), "nvfp4"),
+        "qwen_nvfp4_dynamic_4096": (lambda: ri.qwen_nvfp4(4096), "nvfp4_dynamic"),
+        "qwen_nvfp4_dynamic_16384": (lambda: ri.qwen_nvfp4(16384), "nvfp4_dynamic"),
     }
     return specs[name]
 
 
 def gpu_scale_in(torch, rq, wl, mode, x, r, w):
     """scale_in for the timed launches: the workload's static scale, or for
-    NVFP4 gs = 2688 / amax(y) with amax(y) taken from a per-token FP8 launch of
-    the library itself (amax(y) = 448 * max over rows of the row scale)."""
+    NVFP4 gs = 2688 / amax(y) over the batch, computed on the device by the
+    library's data-derived-scale entry point (outside the timed region)."""
     if mode == "fp8_static":
         return torch.tensor([wl.static_scale or 0.1], dtype=torch.float32, device="cuda")
     if mode != "nvfp4":
         return None
-    _, sc, _ = rq.fused_add_rmsnorm_quant(x, r, w, wl.eps, "fp8_per_token")
-    amax = float(sc.max().item()) * 448.0
-    return torch.tensor([np.float32(2688.0) / np.float32(amax)], dtype=torch.float32, device="cuda")
+    _, _, gs, _ = rq.fused_add_rmsnorm_nvfp4_dynamic(x, r, w, wl.eps)
+    torch.cuda.synchronize()
+    return gs
 
 
 class Buffers:
@@ -183,15 +185,20 @@ class Buffers:
     def __init__(self, torch, rq, wl, mode, min_total_bytes):
         tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
         n, H = wl.n_tokens, wl.hidden
+        self.rq, self.wl, self.mode = rq, wl, mode
+        self.dynamic = mode == "nvfp4_dynamic"
+        qmode = "nvfp4" if self.dynamic else mode
         self.es = 2
         self.res = wl.residual is not None
-        self.bytes = algorithmic_bytes(mode, n, H, 2, self.res)
+        # the data-derived global scale is one more 4-byte output; the second
+        # pass's re-read of h is not counted (it is not required by the op)
+        self.bytes = algorithmic_bytes(qmode, n, H, 2, self.res) + (4 if self.dynamic else 0)
         self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
         x0 = torch.from_numpy(wl.x.view(np.int16)).view(tdt).cuda()
         r0 = None if not self.res else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).cuda()
         self.w = torch.from_numpy(wl.weight.view(np.int16)).view(tdt).cuda()
-        self.scale_in = gpu_scale_in(torch, rq, wl, mode, x0, r0, self.w)
-        self.x, self.r, self.ro, self.q, self.sc = [], [], [], [], []
+        self.scale_in = None if self.dynamic else gpu_scale_in(torch, rq, wl, mode, x0, r0, self.w)
+        self.x, self.r, self.ro, self.q, self.sc, self.gs, self.ws = [], [], [], [], [], [], []
         for i in range(self.sets):
             self.x.append(x0 if i == 0 else x0.clone())
             if self.res:
@@ -200,8 +207,25 @@ class Buffers:
             else:
                 self.r.append(None)
                 self.ro.append(None)
-            self.q.append(torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device="cuda"))
-            self.sc.append(rq.scales_like(mode, n, H, "cuda"))
+            self.q.append(torch.empty(n, H // 2 if qmode == "nvfp4" else H, dtype=torch.uint8, device="cuda"))
+            self.sc.append(rq.scales_like(qmode, n, H, "cuda"))
+            if self.dynamic:
+                self.gs.append(torch.empty(1, dtype=torch.float32, device="cuda"))
+                self.ws.append(torch.empty(rq.nvfp4_dynamic_workspace_bytes(n), dtype=torch.uint8,
+                                           device="cuda"))
+
+    def launch(self, k, stream):
+        """One call of the public API on buffer set k."""
+        if self.dynamic:
+            self.rq.fused_add_rmsnorm_nvfp4_dynamic(
+                self.x[k], self.r[k], self.w, self.wl.eps, out_q=self.q[k], out_scales=self.sc[k],
+                out_global_scale=self.gs[k], residual_out=self.ro[k], workspace=self.ws[k],
+                stream=stream, variant=VARIANT)
+        else:
+            self.rq.fused_add_rmsnorm_quant(
+                self.x[k], self.r[k], self.w, self.wl.eps, self.mode, self.scale_in,
+                out_q=self.q[k], out_scales=self.sc[k], residual_out=self.ro[k], stream=stream,
+                variant=VARIANT)
 
 
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
@@ -216,10 +240,7 @@ def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
     per-function caches before capture).
     """
     def launch(i):
-        k = i % bufs.sets
-        rq.fused_add_rmsnorm_quant(bufs.x[k], bufs.r[k], bufs.w, wl.eps, mode, bufs.scale_in,
-                                   out_q=bufs.q[k], out_scales=bufs.sc[k], residual_out=bufs.ro[k],
-                                   stream=stream, variant=VARIANT)
+        bufs.launch(i % bufs.sets, stream)
 
     def capture(count):
         g = torch.cuda.CUDAGraph()
@@ -268,9 +289,7 @@ def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
         bufs.x[0].copy_(hx, non_blocking=True)
         if hr is not None:
             bufs.r[0].copy_(hr, non_blocking=True)
-        rq.fused_add_rmsnorm_quant(bufs.x[0], bufs.r[0], bufs.w, wl.eps, mode, bufs.scale_in,
-                                   out_q=bufs.q[0], out_scales=bufs.sc[0], residual_out=bufs.ro[0],
-                                   stream=stream, variant=VARIANT)
+        bufs.launch(0, stream)
         hq.copy_(bufs.q[0], non_blocking=True)
         if hs is not None:
             hs.copy_(bufs.sc[0], non_blocking=True)
@@ -451,8 +470,8 @@ def sweep(torch, rq, stream, peak, args):
         (lambda: ri.llama(4096, False), ["llama_fp8_per_token_nores"]),
         (lambda: ri.dsv3(8192), ["dsv3_fp8_group128_row", "dsv3_fp8_group128_col",
                                  "dsv3_fp8_group64_row", "dsv3_fp8_group64_col"]),
-        (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096"]),
-        (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384"]),
+        (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096", "qwen_nvfp4_dynamic_4096"]),
+        (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384", "qwen_nvfp4_dynamic_16384"]),
     ]
     for make, names in groups:
         wl = make()

@@ -153,6 +153,37 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void *x, const void *residual, const v
                                     int variant);
 
 /*
+ * rmsq_fused_add_rmsnorm_nvfp4_dynamic — the NVFP4 mode with the global scale
+ * taken from the data instead of scale_in: gs = 448 * 6 / amax(|y|) over the
+ * whole batch (the NVFP4 workload's definition of the global scale; gs = 1
+ * when that amax is 0), then exactly the RMSQ_NVFP4 quantisation with that gs
+ * (vLLM PR #51925 summary, "Motivation": residual update + RMSNorm, block
+ * scales, FP4 values, fp32 global scale).  Two passes: the first computes the
+ * residual, the per-row inv_rms and the batch amax into `workspace`; the
+ * second re-reads h (residual_out, or x without a residual) and quantises.
+ *  out_global_scale  device, one fp32 (4-byte aligned): receives gs.
+ *  workspace         device, 16-byte aligned, at least
+ *                    rmsq_nvfp4_dynamic_workspace_bytes(n_tokens) bytes of
+ *                    caller-owned scratch; its contents on entry do not
+ *                    matter and are overwritten.  Two calls in flight at the
+ *                    same time must not share one workspace.
+ *  variant           an rmsq_variant for the first pass.
+ * Every other argument as in rmsq_fused_add_rmsnorm_quant with quant_mode
+ * RMSQ_NVFP4 (out_block_scales = its out_scales).  RMSQ_ERR_INVALID_ARG also
+ * for a NULL or too small workspace; no output may overlap the workspace.
+ */
+int rmsq_fused_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual, const void *weight,
+                                         float eps, void *out_q, void *out_block_scales,
+                                         float *out_global_scale, void *residual_out,
+                                         void *workspace, size_t workspace_bytes,
+                                         int64_t n_tokens, int64_t hidden, int dtype, void *stream,
+                                         int variant);
+
+/* Bytes of workspace rmsq_fused_add_rmsnorm_nvfp4_dynamic needs for n_tokens
+ * rows: 256 + 4 * n_tokens, rounded up to a multiple of 256 (0 for n < 0). */
+size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
+
+/*
  * rmsq_set_pipeline_config — process-wide tuning of the PIPELINED variant:
  * chunks_per_thread (16-byte chunks of a row per thread: 1, 2 or 4), stages
  * (rows in flight per CTA: 1..8) and ctas_per_sm (cap on resident CTAs per

@@ -36,9 +36,10 @@ MAX_HIDDEN = 16384
 
 VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 
-EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex", "rmsq_set_pipeline_config",
-           "rmsq_take_fault_flags", "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_status_string",
-           "rmsq_last_cuda_error", "rmsq_version")
+EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
+           "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
+           "rmsq_set_pipeline_config", "rmsq_take_fault_flags", "rmsq_query_sizes", "rmsq_debug_convert",
+           "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
 
 class RmsqError(RuntimeError):
@@ -70,6 +71,11 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm_quant_ex.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci,
                                                       vp, ci]
         L.rmsq_fused_add_rmsnorm_quant_ex.restype = ci
+        L.rmsq_fused_add_rmsnorm_nvfp4_dynamic.argtypes = [vp, vp, vp, f32, vp, vp, vp, vp, vp,
+                                                           ctypes.c_size_t, i64, i64, ci, vp, ci]
+        L.rmsq_fused_add_rmsnorm_nvfp4_dynamic.restype = ci
+        L.rmsq_nvfp4_dynamic_workspace_bytes.argtypes = [i64]
+        L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
         L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci]
         L.rmsq_set_pipeline_config.restype = ci
         L.rmsq_take_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -163,6 +169,50 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
+
+
+def nvfp4_dynamic_workspace_bytes(n_tokens: int) -> int:
+    return load().rmsq_nvfp4_dynamic_workspace_bytes(n_tokens)
+
+
+def fused_add_rmsnorm_nvfp4_dynamic(x: torch.Tensor, residual: torch.Tensor | None,
+                                    weight: torch.Tensor, eps: float, *,
+                                    out_q: torch.Tensor | None = None,
+                                    out_scales: torch.Tensor | None = None,
+                                    out_global_scale: torch.Tensor | None = None,
+                                    residual_out: torch.Tensor | None = None,
+                                    workspace: torch.Tensor | None = None, stream=None,
+                                    variant: str = "auto"):
+    """rmsq_fused_add_rmsnorm_nvfp4_dynamic on torch CUDA tensors: NVFP4 with
+    gs = 2688 / amax(all y) computed on the device.  Missing outputs and the
+    workspace are allocated.  Returns (q, block_scales, global_scale, residual_out)."""
+    L = load()
+    n, H = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {x.dtype}")
+    for t in (x, residual, weight, residual_out, out_q, out_scales, out_global_scale, workspace):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    dev = x.device
+    if out_q is None:
+        out_q = torch.empty(n, H // 2, dtype=torch.uint8, device=dev)
+    if out_scales is None:
+        out_scales = torch.empty(n, H // 16, dtype=torch.uint8, device=dev)
+    if out_global_scale is None:
+        out_global_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(residual)
+    ws_bytes = nvfp4_dynamic_workspace_bytes(n)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    st = L.rmsq_fused_add_rmsnorm_nvfp4_dynamic(
+        _p(x), _p(residual), _p(weight), ctypes.c_float(eps), _p(out_q), _p(out_scales),
+        _p(out_global_scale), _p(residual_out), _p(workspace),
+        workspace.numel() * workspace.element_size(), n, H, DTYPES[x.dtype], _stream(stream),
+        VARIANTS[variant])
+    if st:
+        raise RmsqError(st, "rmsq_fused_add_rmsnorm_nvfp4_dynamic")
+    return out_q, out_scales, out_global_scale, residual_out
 
 
 def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm: int = 0) -> None:

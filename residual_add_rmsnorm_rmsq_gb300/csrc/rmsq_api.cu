@@ -187,6 +187,73 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     return RMSQ_OK;
 }
 
+size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens) {
+    return n_tokens < 0 ? 0 : rmsq::nvfp4_dynamic_workspace_bytes(n_tokens);
+}
+
+int rmsq_fused_add_rmsnorm_nvfp4_dynamic(const void* x, const void* residual, const void* weight,
+                                         float eps, void* out_q, void* out_block_scales,
+                                         float* out_global_scale, void* residual_out, void* workspace,
+                                         size_t workspace_bytes, int64_t n_tokens, int64_t hidden,
+                                         int dtype, void* stream, int variant) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (variant != RMSQ_VARIANT_AUTO && variant != RMSQ_VARIANT_DIRECT && variant != RMSQ_VARIANT_PIPELINED)
+        return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(RMSQ_NVFP4, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return RMSQ_OK;
+    if (!x || !weight || !out_q || !out_block_scales || !out_global_scale || !workspace)
+        return RMSQ_ERR_INVALID_ARG;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSQ_ERR_INVALID_ARG;
+    const size_t ws_need = rmsq::nvfp4_dynamic_workspace_bytes(n_tokens);
+    if (workspace_bytes < ws_need) return RMSQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16) || !aligned(residual_out, 16) ||
+        !aligned(out_q, 16) || !aligned(out_global_scale, 4) || !aligned(workspace, 16))
+        return RMSQ_ERR_ALIGNMENT;
+    size_t q_bytes = 0, sc_bytes = 0;
+    sizes_of(RMSQ_NVFP4, n_tokens, hidden, &q_bytes, &sc_bytes);
+    const size_t act = static_cast<size_t>(n_tokens * hidden) * 2;
+    const Span X = span(x, act), R = span(residual, act), W = span(weight, hidden * 2),
+               RO = span(residual_out, act), Q = span(out_q, q_bytes), SC = span(out_block_scales, sc_bytes),
+               GS = span(out_global_scale, 4), WS = span(workspace, ws_need);
+    if (residual && X.lo != R.lo && overlaps(X, R)) return RMSQ_ERR_ALIAS;
+    if (residual_out) {
+        if (RO.lo != X.lo && overlaps(RO, X)) return RMSQ_ERR_ALIAS;
+        if (RO.lo != R.lo && overlaps(RO, R)) return RMSQ_ERR_ALIAS;
+        if (overlaps(RO, W)) return RMSQ_ERR_ALIAS;
+    }
+    const Span outs[4] = {Q, SC, GS, WS};
+    for (int i = 0; i < 4; ++i) {
+        const Span& o = outs[i];
+        if (overlaps(o, X) || overlaps(o, R) || overlaps(o, W) || overlaps(o, RO)) return RMSQ_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(o, outs[j])) return RMSQ_ERR_ALIAS;
+    }
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+
+    rmsq::LaunchArgs la;
+    la.x = x;
+    la.res = residual;
+    la.w = weight;
+    la.res_out = residual_out;
+    la.q = out_q;
+    la.scales = out_block_scales;
+    la.scale_in = nullptr;
+    la.eps = eps;
+    la.mode = RMSQ_NVFP4;
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    la.variant = variant == RMSQ_VARIANT_DIRECT ? rmsq::kVariantDirect
+                 : variant == RMSQ_VARIANT_PIPELINED ? rmsq::kVariantPipelined : rmsq::kVariantAuto;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == RMSQ_BF16
+                              ? rmsq::launch_nvfp4_dynamic_bf16(la, workspace, out_global_scale, s)
+                              : rmsq::launch_nvfp4_dynamic_fp16(la, workspace, out_global_scale, s);
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
 int rmsq_fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps,
                                  int quant_mode, const float* scale_in, void* out_q, void* out_scales,
                                  void* residual_out, int64_t n_tokens, int64_t hidden, int dtype,

@@ -125,6 +125,15 @@ __device__ __forceinline__ float e4m3_value_nonneg(uint32_t c) {
                   : __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
+// r = gs / decode(code) for every finite non-negative E4M3 code (0 for the
+// zero code; 0x7f is NaN and never produced), in shared memory, so that the
+// NVFP4 per-block division by the decoded block scale becomes a lookup.
+// Filled cooperatively by the CTA; a barrier must follow before use.
+__device__ __forceinline__ void fill_nvfp4_rtab(float* tab, float gs) {
+    for (int c = threadIdx.x; c < 128; c += blockDim.x)
+        tab[c] = (c == 0 || c == 127) ? 0.0f : __fdiv_rn(gs, e4m3_value_nonneg((uint32_t)c));
+}
+
 // E4M3 codes of y/s where the quotient is the correctly rounded fp32
 // division, without a division per element: multiply by two bracketing
 // reciprocals rdn = RN(RN(1/s) * (1 - 2^-20)) and rup = RN(RN(1/s) * (1 + 2^-20)).
@@ -134,14 +143,19 @@ __device__ __forceinline__ float e4m3_value_nonneg(uint32_t c) {
 // codes at both ends are the code of the quotient.  Otherwise (about one
 // element in 2^16) the quotient is computed with __fdiv_rn.
 
-// Bracketing reciprocals of a scale s.
+// Bracketing reciprocals of a scale s.  The argument above holds for any
+// approximation of 1/s with relative error below 2^-18.1 once the bracket is
+// widened to 1 -+ 2^-18, so the hardware's approximate reciprocal (documented
+// error about one ulp, 2^-23) serves; a wider bracket only makes the exact
+// fallback a little more frequent (about one chunk of eight in a thousand).
 struct Fp8Recips {
     float rdn, rup;
 };
 __device__ __forceinline__ Fp8Recips fp8_recips(float s) {
-    const float r = __fdiv_rn(1.0f, s);
-    return {__fmul_rn(r, 0.99999904632568359375f),     // 1 - 2^-20
-            __fmul_rn(r, 1.00000095367431640625f)};    // 1 + 2^-20
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return {__fmul_rn(r, 0.999996185302734375f),       // 1 - 2^-18
+            __fmul_rn(r, 1.000003814697265625f)};      // 1 + 2^-18
 }
 
 // Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.  The
@@ -185,6 +199,31 @@ __device__ __forceinline__ float warp_tree_sum(float v) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
     return v;
+}
+
+// Max over the 32 lanes of non-negative values: their bit patterns order like
+// the values, so one integer max reduction does it.
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+    return __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(v)));
+}
+
+// Pairwise tree over 16 / 32 consecutive floats of shared memory (16-byte
+// aligned), read with 128-bit loads: the top levels of the canonical tree
+// over warp sums, zero-padded.
+template <int N>
+__device__ __forceinline__ float smem_tree_sum(const float* p) {
+    static_assert(N == 16 || N == 32, "16 or 32 slots");
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+        const float4 f = reinterpret_cast<const float4*>(p)[i];
+        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+#pragma unroll
+    for (int len = N; len > 1; len >>= 1)
+#pragma unroll
+        for (int k = 0; k < len / 2; ++k) v[k] = __fadd_rn(v[2 * k], v[2 * k + 1]);
+    return v[0];
 }
 
 template <int LANES>

@@ -16,6 +16,7 @@
 #include <mutex>
 
 #include "rmsq_launch.h"
+#include "rmsq_nvfp4_dyn.cuh"
 #include "rmsq_pipe.cuh"
 #include "rmsq_rows.cuh"
 
@@ -59,6 +60,7 @@ const void* pick_kernel(int mode, bool res, bool pipe, int J) {
     case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J);
     case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J);
     case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J);
+    case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J);
     default: return nullptr;
     }
 }
@@ -175,6 +177,32 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     if (!fn) return cudaErrorInvalidValue;
     void* params[] = {&a};
     return cudaLaunchKernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+}
+
+// NVFP4 with a data-derived global scale: zero the workspace's amax word,
+// pass 1 (row kernel, mode kNormAmax), pass 2 (block quantisation).
+template <class E>
+cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* out_gs,
+                                 cudaStream_t stream) {
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), stream);
+    if (e != cudaSuccess) return e;
+    LaunchArgs first = la;
+    first.mode = kNormAmax;
+    first.q = nullptr;
+    first.scales = workspace;
+    first.scale_in = nullptr;
+    e = launch_rows<E>(first, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks_total = (int64_t)la.n * (la.hidden / 16);
+    const int sms = sm_count(&e);
+    if (e != cudaSuccess) return e;
+    int64_t grid = (blocks_total + 255) / 256;
+    if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
+    const void* h = la.res ? la.res_out : la.x;
+    nvfp4_dyn_quant_kernel<E><<<(int)grid, 256, 0, stream>>>(
+        static_cast<const uint4*>(h), static_cast<const uint4*>(la.w), static_cast<const float*>(workspace),
+        static_cast<uint2*>(la.q), static_cast<uint8_t*>(la.scales), out_gs, la.n, la.hidden);
+    return cudaGetLastError();
 }
 
 // Reads and clears this unit's pipeline fault flag (current device).

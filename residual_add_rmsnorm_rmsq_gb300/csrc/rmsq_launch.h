@@ -39,6 +39,16 @@ void set_pipe_tuning(const PipeTuning& t);
 // One launch of the row kernel for bf16 / fp16 activations.
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);
+// NVFP4 with a data-derived global scale (two passes); `workspace` holds the
+// batch amax word and the per-row inv_rms.
+cudaError_t launch_nvfp4_dynamic_bf16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
+cudaError_t launch_nvfp4_dynamic_fp16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
+// Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
+inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
+    const size_t raw = 256 + 4 * static_cast<size_t>(n);
+    return (raw + 255) / 256 * 256;
+}
+
 // Read and clear the pipelined kernels' fault flags (current device).
 cudaError_t take_pipe_fault_bf16(unsigned int* out);
 cudaError_t take_pipe_fault_fp16(unsigned int* out);

@@ -26,7 +26,7 @@ template <class E, int MODE, bool RES, int J>
 __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, unsigned int* fault) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
-    __shared__ float s_sum[2][32];
+    __shared__ __align__(16) float s_sum[2][32];
     __shared__ float s_max[2][32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -40,6 +40,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
+    if (tid < 64 && (tid & 31) >= nwarps) s_sum[tid >> 5][tid & 31] = 0.0f;   // absent warps: 0
     __syncthreads();
 
     uint64_t policy = 0;
@@ -61,9 +62,12 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     for (int j = 0; j < J; ++j)
         wv[j] = (c0 + j < a.chunks) ? ld_weight(a.w + c0 + j) : make_uint4(0u, 0u, 0u, 0u);
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
+    __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
+    if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the first row's barrier
 
     int k = 0;
     bool faulted = false;
+    float run_max = 0.0f;
     for (;; ++k) {
         const int row = blockIdx.x + k * G;
         if (row >= a.n) break;
@@ -71,7 +75,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         const uint32_t parity = static_cast<uint32_t>(k / stages) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity);
 
-        float h[J][8];
+        uint32_t h[J][4];
         float acc = 0.0f;
         if (ok) {
             const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)s * stage_bytes);
@@ -103,10 +107,11 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                     bulk_g2s(dst + row_bytes, a.res + (int64_t)nrow * a.chunks, row_bytes, &full[s], policy);
             }
         }
-        const float total = warp_tree_sum(lane < nwarps ? s_sum[k & 1][lane] : 0.0f);
+        const float total = smem_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1]);
         const float inv = inv_rms(total, a.hidden, a.eps);
-        quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_max[k & 1], tid, nwarps);
+        quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_rtab, s_max[k & 1], tid, nwarps, run_max);
     }
+    if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max[0], tid, nwarps);
 
     if (faulted && tid == 0) {
         atomicOr(fault, 1u);

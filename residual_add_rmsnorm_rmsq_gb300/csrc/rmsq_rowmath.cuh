@@ -27,7 +27,17 @@ enum Mode : int {
     kFp8G64Row = 4,
     kFp8G64Col = 5,
     kNvfp4 = 6,
+    // First pass of NVFP4 with a data-derived global scale: residual add,
+    // RMSNorm, the row's inv_rms stored in the workspace and the running
+    // amax of y folded into the workspace's amax word; no codes.
+    kNormAmax = 7,
 };
+
+// Workspace of the data-derived NVFP4 global scale: word 0 holds the bits of
+// the batch amax of |y| (non-negative floats order like their bit patterns,
+// so atomicMax on the bits is a max on the values); the fp32 inv_rms of row t
+// sits at float index kWsInvOffset + t.
+constexpr int kWsInvOffset = 64;
 
 struct RowArgs {
     const uint4* x;
@@ -55,22 +65,23 @@ template <int MODE> struct ModeTraits {
 // Chunks at or beyond `chunks` hold zeros and are not stored.
 template <class E, bool RES, int J>
 __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
-                                                float (&h)[J][8], uint4* res_out_row,
+                                                uint32_t (&hw)[J][4], uint4* res_out_row,
                                                 int c0, int chunks) {
     float part[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        uint32_t hw[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+        hw[j][0] = xv[j].x; hw[j][1] = xv[j].y; hw[j][2] = xv[j].z; hw[j][3] = xv[j].w;
         if constexpr (RES) {
             const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) hw[k] = E::add2(hw[k], rs[k]);
+            for (int k = 0; k < 4; ++k) hw[j][k] = E::add2(hw[j][k], rs[k]);
             if (c0 + j < chunks)
-                st_stream(res_out_row + c0 + j, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
         }
+        float h[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) { h[j][2 * k] = E::lo(hw[k]); h[j][2 * k + 1] = E::hi(hw[k]); }
-        part[j] = leaf8_sumsq(h[j]);
+        for (int k = 0; k < 4; ++k) { h[2 * k] = E::lo(hw[j][k]); h[2 * k + 1] = E::hi(hw[j][k]); }
+        part[j] = leaf8_sumsq(h);
     }
     static_assert(J == 1 || J == 2 || J == 4, "J must be 1, 2 or 4");
     if constexpr (J == 1) return part[0];
@@ -85,13 +96,15 @@ __device__ __forceinline__ float inv_rms(float total, int hidden, float eps) {
 }
 
 // y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
-// `sin` is the static scale (FP8 static) or the global scale (NVFP4).
+// `sin` is the static scale (FP8 static) or the global scale (NVFP4);
+// `rtab` the NVFP4 table of gs / decode(code) (fill_nvfp4_rtab), else unused.
 // FP8 per-token does a CTA-wide amax through `s_max` (32 floats) and one
 // __syncthreads; every thread of the CTA must call this.
 template <class E, int MODE, int J>
-__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const float (&h)[J][8],
+__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
                                              const uint4 (&wv)[J], float inv, float sin,
-                                             float* s_max, int tid, int nwarps) {
+                                             const float* rtab, float* s_max, int tid, int nwarps,
+                                             float& run_max) {
     const int lane = tid & 31, warp = tid >> 5;
     const int c0 = tid * J;
     float y[J][8];
@@ -100,12 +113,18 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const fl
         const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            y[j][2 * k] = __fmul_rn(__fmul_rn(h[j][2 * k], inv), E::lo(ws[k]));
-            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(h[j][2 * k + 1], inv), E::hi(ws[k]));
+            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
+            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
         }
     }
 
-    if constexpr (MODE == kNvfp4) {
+    if constexpr (MODE == kNormAmax) {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) run_max = fmaxf(run_max, fabsf(y[j][k]));
+        if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
+    } else if constexpr (MODE == kNvfp4) {
         // 16-element blocks = chunk pairs (2m, 2m+1): a lane pair when J == 1,
         // inside the thread otherwise.
         const float gs = sin;
@@ -123,8 +142,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const fl
                 for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j + 1][k]));
             }
             const uint32_t sb = e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), gs), 0.0f) & 0xffu;
-            const float d = e4m3_value_nonneg(sb);
-            const float r = (d == 0.0f) ? 0.0f : __fdiv_rn(gs, d);
+            const float r = rtab[sb];      // gs / decode(sb), 0 for a zero block scale
             const int c = c0 + j;
             constexpr int NC = (J == 1) ? 1 : 2;
 #pragma unroll
@@ -146,10 +164,10 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const fl
             for (int j = 0; j < J; ++j)
 #pragma unroll
                 for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
-            m = lanes_max<32>(m);
+            m = warp_max_nonneg(m);
             if (lane == 0) s_max[warp] = m;
             __syncthreads();
-            m = lanes_max<32>(lane < nwarps ? s_max[lane] : 0.0f);
+            m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
             s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
             if (tid == 0) static_cast<float*>(a.scales)[row] = s;
         } else {
@@ -170,12 +188,30 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const fl
             }
         }
         const Fp8Recips rc = fp8_recips(s);
+        (void)run_max;
         uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const uint2 codes = fp8_chunk(y[j], s, rc);
             if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
         }
+    }
+}
+
+// End of a kNormAmax launch: CTA-wide max of the threads' running amax, then
+// one atomicMax per CTA on the workspace's amax word.  Every thread of the
+// CTA calls it (two __syncthreads); `s_max` is 32 floats of shared memory.
+__device__ __forceinline__ void flush_amax(const RowArgs& a, float run_max, float* s_max, int tid,
+                                           int nwarps) {
+    const int lane = tid & 31, warp = tid >> 5;
+    const float m = warp_max_nonneg(run_max);
+    __syncthreads();
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < nwarps; ++w) t = fmaxf(t, s_max[w]);
+        if (t > 0.0f) atomicMax(static_cast<unsigned int*>(a.scales), __float_as_uint(t));
     }
 }
 

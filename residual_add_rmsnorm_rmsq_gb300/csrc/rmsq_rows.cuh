@@ -10,8 +10,10 @@ namespace rmsq {
 
 template <class E, int MODE, bool RES, int J>
 __global__ void __launch_bounds__(1024) rows_kernel(const RowArgs a) {
-    __shared__ float s_sum[32];
+    __shared__ __align__(16) float s_sum[32];
     __shared__ float s_max[32];
+    // Slots of absent warps read as 0 (ordered before the reads by the barrier below).
+    if (threadIdx.x < 32 && (int)threadIdx.x >= (int)(blockDim.x >> 5)) s_sum[threadIdx.x] = 0.0f;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     const int row = blockIdx.x;
@@ -29,15 +31,19 @@ __global__ void __launch_bounds__(1024) rows_kernel(const RowArgs a) {
         }
     }
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
+    __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
+    if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the barrier below
 
-    float h[J][8];
+    uint32_t h[J][4];
     float acc = combine_chunks<E, RES, J>(xv, rv, h, a.res_out + base, c0, a.chunks);
     acc = warp_tree_sum(acc);
     if (lane == 0) s_sum[warp] = acc;
     __syncthreads();
-    const float total = warp_tree_sum(lane < nwarps ? s_sum[lane] : 0.0f);
+    const float total = smem_tree_sum<32>(s_sum);
     const float inv = inv_rms(total, a.hidden, a.eps);
-    quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_max, tid, nwarps);
+    float run_max = 0.0f;
+    quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_rtab, s_max, tid, nwarps, run_max);
+    if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max, tid, nwarps);
 }
 
 }  // namespace rmsq

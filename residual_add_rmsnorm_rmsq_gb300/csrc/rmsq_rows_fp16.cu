@@ -23,6 +23,10 @@ cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream) {
 
 cudaError_t take_pipe_fault_fp16(unsigned int* out) { return take_pipe_fault(out); }
 
+cudaError_t launch_nvfp4_dynamic_fp16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream) {
+    return launch_nvfp4_dynamic<Fp16T>(a, workspace, out_gs, stream);
+}
+
 cudaError_t launch_convert(int kind, const float* in, uint8_t* out, int64_t n, cudaStream_t stream) {
     const int64_t blocks64 = (n + 255) / 256;
     const int blocks = (int)(blocks64 < 152 * 64 ? blocks64 : 152 * 64);

@@ -26,7 +26,7 @@ def L():
 def _declared():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|const char \*)\s*(rmsq_\w+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char \*)\s*(rmsq_\w+)\s*\(", src, flags=re.M)))
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -126,3 +126,29 @@ def test_valid_call_without_device_reports_no_device(L):
     vp = ctypes.c_void_p
     assert L.rmsq_debug_convert(0, vp(A), vp(B), 16, None) == rq.ERR_NO_DEVICE
     assert L.rmsq_debug_convert(2, vp(A), vp(B), 16, None) == rq.ERR_INVALID_ARG
+
+
+def test_nvfp4_dynamic_argument_errors(L):
+    vp = ctypes.c_void_p
+    ws = rq.nvfp4_dynamic_workspace_bytes(4)
+    assert ws == 512 and rq.nvfp4_dynamic_workspace_bytes(64) == 512
+    assert rq.nvfp4_dynamic_workspace_bytes(65) == 768
+
+    def dyn(x=A, res=B, w=C, q=D, sc=E, gs=0x70000000, ro=F, wsp=0x78000000, wsb=ws, n=4, H=64, dt=0, v=0):
+        return L.rmsq_fused_add_rmsnorm_nvfp4_dynamic(
+            vp(x) if x else None, vp(res) if res else None, vp(w) if w else None, ctypes.c_float(1e-6),
+            vp(q) if q else None, vp(sc) if sc else None, vp(gs) if gs else None, vp(ro) if ro else None,
+            vp(wsp) if wsp else None, wsb, n, H, dt, None, v)
+
+    assert dyn(H=40) == rq.ERR_UNSUPPORTED_SHAPE
+    assert dyn(wsp=0) == rq.ERR_INVALID_ARG
+    assert dyn(wsb=ws - 1) == rq.ERR_INVALID_ARG
+    assert dyn(gs=0) == rq.ERR_INVALID_ARG
+    assert dyn(v=3) == rq.ERR_INVALID_ARG
+    assert dyn(wsp=0x78000000 + 8) == rq.ERR_ALIGNMENT
+    assert dyn(gs=0x70000000 + 2) == rq.ERR_ALIGNMENT
+    assert dyn(wsp=D) == rq.ERR_ALIAS                      # workspace over the codes
+    assert dyn(gs=E + 4) == rq.ERR_ALIAS                    # global scale inside block scales
+    assert dyn(n=0, x=0, res=0, w=0, q=0, sc=0, gs=0, ro=0, wsp=0) == rq.OK
+    if not torch.cuda.is_available():
+        assert dyn() == rq.ERR_NO_DEVICE

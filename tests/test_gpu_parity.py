@@ -214,6 +214,16 @@ def test_subnormal_zero_and_wide_range_inputs(dtype):
         P.check(wl, mode, scale_in=0.5 if mode == "fp8_static" else None, label=f"wide/{dtype}/{mode}")
 
 
+def test_static_scale_sweep():
+    """Many static scales (including subnormal-ratio and saturating ones):
+    exercises the bracketing reciprocal and its exact fallback across scales."""
+    wl = ri.make_workload("sweep", 16, 512, res_sigma=1.3, seed=37)
+    u = ri.uniform(38, 1, 120)
+    scales = np.float32(10.0) ** (-8.0 + 14.0 * u).astype(np.float32)
+    for s in list(scales) + [np.float32(1.0), np.float32(0.1), np.float32(2.0 ** -20)]:
+        P.check(wl, "fp8_static", scale_in=float(s), label=f"static s={float(s):.3e}")
+
+
 def test_pipelined_launch_shapes_do_not_change_results():
     wl = ri.make_workload("shapes", 700, 4096, res_sigma=2.0, seed=36)
     want = oracle.run_workload(wl, "fp8_group64_col", nthreads=8)
