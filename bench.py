@@ -182,7 +182,7 @@ def gpu_scale_in(torch, rq, wl, mode, x, r, w):
 class Buffers:
     """Rotating device buffer sets for one workload and mode."""
 
-    def __init__(self, torch, rq, wl, mode, min_total_bytes):
+    def __init__(self, torch, rq, wl, mode, min_total_bytes, max_sets=None):
         tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
         n, H = wl.n_tokens, wl.hidden
         self.rq, self.wl, self.mode = rq, wl, mode
@@ -194,6 +194,8 @@ class Buffers:
         # pass's re-read of h is not counted (it is not required by the op)
         self.bytes = algorithmic_bytes(qmode, n, H, 2, self.res) + (4 if self.dynamic else 0)
         self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        if max_sets is not None:
+            self.sets = min(self.sets, max_sets)
         x0 = torch.from_numpy(wl.x.view(np.int16)).view(tdt).cuda()
         r0 = None if not self.res else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).cuda()
         self.w = torch.from_numpy(wl.weight.view(np.int16)).view(tdt).cuda()
@@ -456,9 +458,29 @@ def run_ours(args, rank, world, dist):
     }
     if not args.no_sweep:
         line["modes"] = sweep(torch, rq, stream, peak, args)
+        line["decode_us_per_call"] = decode_sweep(torch, rq, stream, args)
     if not args.no_cpu and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, mode)
     print(json.dumps(line), flush=True)
+
+
+def decode_sweep(torch, rq, stream, args):
+    """Decode batches (fp16, hidden 8192, n = 1 .. 256): device microseconds
+    per call, back to back from a CUDA graph, every quant mode +- residual.
+    Eight buffer sets rotate (at most 15 MB in all), so these inputs are
+    L2-resident, as a decode step's activations usually are."""
+    import rmsq_inputs as ri
+    out = {}
+    for residual in (True, False):
+        for n in ri.DECODE_TOKENS:
+            wl = ri.decode(n, residual=residual)
+            for mode in ("fp8_static", "fp8_per_token", "fp8_group128_row", "nvfp4"):
+                bufs = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1, max_sets=8)
+                ms = time_launches(torch, rq, wl, mode, bufs, args.decode_steps, 5, stream)
+                out.setdefault(f"{mode}{'' if residual else '_nores'}", {})[str(n)] = round(ms * 1e3, 3)
+                del bufs
+    torch.cuda.empty_cache()
+    return out
 
 
 def sweep(torch, rq, stream, peak, args):
@@ -496,6 +518,7 @@ def main():
     ap.add_argument("--workload", default="llama_fp8_per_token")
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--variant", choices=["auto", "direct", "pipelined"], default="auto")
     args = ap.parse_args()
