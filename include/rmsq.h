@@ -183,6 +183,39 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual, co
  * rows: 256 + 4 * n_tokens, rounded up to a multiple of 256 (0 for n < 0). */
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
 
+/* Largest batch rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc accepts. */
+#define RMSQ_NOALLOC_MAX_TOKENS 65536
+
+/*
+ * rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc — rmsq_fused_add_rmsnorm_nvfp4_dynamic
+ * without a caller workspace and without any device allocation.  The pages
+ * have no counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory themselves — for instance a plugin inside an engine
+ * that owns all device memory through its own pool and hands the plugin none,
+ * or latency-critical code that must not call cudaMalloc because it can
+ * synchronise the device.  The caller still passes every input and output.
+ *
+ * The workspace lives in a fixed device array inside the library (256 + 4 *
+ * RMSQ_NOALLOC_MAX_TOKENS bytes, about 257 KiB), present on every device that
+ * loads the library until the process exits.  n_tokens above
+ * RMSQ_NOALLOC_MAX_TOKENS returns RMSQ_ERR_UNSUPPORTED_SHAPE (use the entry
+ * point with a workspace for larger batches).  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress with that device
+ * current); make that first call before any stream capture.  Every call on a
+ * device shares the one array and leaves its contents behind; the call zeroes
+ * what must start at zero (the amax word) itself.  Calls whose work overlaps on
+ * the GPU (other streams, or other host threads) race on the array: order them.
+ * Arguments, results and every other rule are those of
+ * rmsq_fused_add_rmsnorm_nvfp4_dynamic; without a CUDA device it returns
+ * RMSQ_ERR_NO_DEVICE.
+ */
+int rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc(const void *x, const void *residual,
+                                                 const void *weight, float eps, void *out_q,
+                                                 void *out_block_scales, float *out_global_scale,
+                                                 void *residual_out, int64_t n_tokens,
+                                                 int64_t hidden, int dtype, void *stream,
+                                                 int variant);
+
 /*
  * rmsq_set_pipeline_config — process-wide tuning of the PIPELINED variant:
  * chunks_per_thread (16-byte chunks of a row per thread: 1, 2 or 4), stages

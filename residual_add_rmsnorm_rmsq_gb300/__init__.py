@@ -38,6 +38,7 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
+           "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc",
            "rmsq_set_pipeline_config", "rmsq_take_fault_flags", "rmsq_query_sizes", "rmsq_debug_convert",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
