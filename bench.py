@@ -55,6 +55,25 @@ def algorithmic_bytes(mode: str, n: int, H: int, es: int, residual: bool) -> int
     return n * per_tok + fixed
 
 
+def max_over_ranks(ms: float, dist, device: str) -> float:
+    """The slowest rank's time per step (every rank gets it); `dist` is
+    torch.distributed (any backend) or None for a single process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rates(bytes_per_rank_step: int, tokens_per_rank_step: int, world: int, ms: float):
+    """Whole-job GB/s and tokens/s: every rank processes its own batch (the
+    rows are independent, so ranks shard by tokens with no collective on the
+    data path) and the job takes as long as its slowest rank."""
+    sec = ms / 1e3
+    return bytes_per_rank_step * world / sec / 1e9, tokens_per_rank_step * world / sec
+
+
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples (host timestamped) of SM clock and throttle reasons."""
@@ -413,17 +432,13 @@ def run_ours(args, rank, world, dist):
     ms = time_launches(torch, rq, wl, mode, bufs, args.steps, 0, stream)
     t_wall1 = time.time()
     barrier()
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, "cuda")
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     if sampler:
         sampler.stop()
 
     per_launch = bufs.bytes
-    value = per_launch * world / (ms / 1e3) / 1e9
-    tokens_s = wl.n_tokens * world / (ms / 1e3)
+    value, tokens_s = whole_job_rates(per_launch, wl.n_tokens, world, ms)
 
     if rank != 0:
         return

@@ -1,0 +1,58 @@
+"""The N>1 path of the benchmark on CPU: gloo ranks (world size 2) exercise
+the max-over-ranks timing and the whole-job rate the benchmark reports.  The
+op itself shards by tokens with no collective on the data path, so this
+host logic is all that multi-GPU runs add."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, times, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = bench.max_over_ranks(times[rank], dist, "cpu")
+        value, tok = bench.whole_job_rates(1_000_000, 4096, world, ms)
+        out[rank] = (ms, value, tok)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2])
+def test_max_over_ranks_and_whole_job_rate(world):
+    times = [0.020, 0.025][:world]
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(world, _free_port(), times, out), nprocs=world, join=True)
+    for r in range(world):
+        ms, value, tok = out[r]
+        assert ms == max(times)
+        assert value == pytest.approx(1_000_000 * world / (max(times) / 1e3) / 1e9)
+        assert tok == pytest.approx(4096 * world / (max(times) / 1e3))
+
+
+def test_single_process_passthrough():
+    assert bench.max_over_ranks(1.5, None, "cpu") == 1.5
+    v, t = bench.whole_job_rates(2_000_000_000, 1000, 1, 1000.0)
+    assert v == pytest.approx(2.0) and t == pytest.approx(1000.0)
+
+
+def test_reference_arm_prints_on_rank_zero_only(capsys):
+    class A:
+        workload, steps, warmup = "llama_fp8_per_token", 3, 3
+    bench.run_reference(A, rank=1, world=2)
+    assert capsys.readouterr().out == ""
