@@ -167,6 +167,21 @@ def profiled_traffic(kernel_name: str, digest: str):
     return e.get("dram_bytes_per_launch")
 
 
+def kernel_name(wl, mode: str, residual: bool, torch) -> str:
+    """Name (as ncu prints it, without the namespace) of the row kernel the
+    library launches for this workload: the pipelined kernel from 4 rows per SM
+    on (direct kernel below), 2 chunks of 8 per thread up to hidden 8192."""
+    import residual_add_rmsnorm_rmsq_gb300 as rq
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pipelined = VARIANT == "pipelined" or (VARIANT == "auto" and wl.n_tokens >= 4 * sms)
+    e = "Bf16T" if wl.dtype == "bf16" else "Fp16T"
+    m = rq.MODES["nvfp4" if mode == "nvfp4_dynamic" else mode]
+    chunks = wl.hidden // 8
+    if pipelined:
+        return f"pipe_entry<{e}, {m}, {int(residual)}, {2 if chunks <= 1024 else 4}>"
+    return f"rows_kernel<{e}, {m}, {int(residual)}, {1 if chunks <= 1024 else 2}>"
+
+
 def workload_spec(name: str):
     import rmsq_inputs as ri
     specs = {
@@ -445,7 +460,7 @@ def run_ours(args, rank, world, dist):
     peak, peak_kind = measured_peak()
     achieved = per_launch / (ms / 1e3) / 1e9
     digest = kernel_digest()
-    kname = f"rows_kernel<{wl.dtype},{mode},{'res' if bufs.res else 'nores'}>"
+    kname = kernel_name(wl, mode, bufs.res, torch)
     traffic = profiled_traffic(kname, digest)
 
     e2e_ms, h2d, d2h = e2e_measure(torch, rq, wl, mode, bufs, min(args.steps, 50), stream)
