@@ -27,7 +27,7 @@ namespace rmsq {
 static __device__ unsigned int g_pipe_fault;
 
 template <class E, int MODE, bool RES, int J>
-__global__ void __launch_bounds__(kPipeMaxThreads, 1) pipe_entry(const RowArgs a, const int stages) {
+__global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : 2)) pipe_entry(const RowArgs a, const int stages) {
     pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
 }
 
@@ -86,7 +86,12 @@ inline cudaError_t ensure_smem_limit(const void* fn) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (done[i] == fn) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
+    // Prefer the largest shared-memory carve-out so that the rings of several
+    // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && used < 256) done[used++] = fn;
     return e;
 }
@@ -139,6 +144,7 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     a.n = la.n;
     a.hidden = la.hidden;
     a.chunks = la.hidden / 8;
+    a.inv_hidden_pow2 = (la.hidden & (la.hidden - 1)) == 0 ? 1.0f / (float)la.hidden : 0.0f;
     const bool res = la.res != nullptr;
 
     cudaError_t err = cudaSuccess;
@@ -196,7 +202,7 @@ cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* o
     const int64_t blocks_total = (int64_t)la.n * (la.hidden / 16);
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
-    int64_t grid = (blocks_total + 255) / 256;
+    int64_t grid = (blocks_total + 256 * kDynUnroll - 1) / (256 * kDynUnroll);
     if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
     const void* h = la.res ? la.res_out : la.x;
     nvfp4_dyn_quant_kernel<E><<<(int)grid, 256, 0, stream>>>(

@@ -38,6 +38,8 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const float (&y)[16], float gs
     return sb;
 }
 
+constexpr int kDynUnroll = 4;
+
 template <class E>
 __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, const uint4* w,
                                                               const float* ws, uint2* q,
@@ -52,29 +54,45 @@ __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, co
     const int bpr = hidden / 16;
     const int chunks = hidden / 8;
     const int64_t total = (int64_t)n * bpr;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
-         b += (int64_t)gridDim.x * blockDim.x) {
-        const int row = (int)(b / bpr);
-        const int cb = (int)(b - (int64_t)row * bpr);
-        const float inv = ws[kWsInvOffset + row];
-        const uint4 hv[2] = {ld_act(h + (int64_t)row * chunks + 2 * cb),
-                             ld_act(h + (int64_t)row * chunks + 2 * cb + 1)};
-        const uint4 wv[2] = {ld_weight(w + 2 * cb), ld_weight(w + 2 * cb + 1)};
-        float y[16];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    // kDynUnroll blocks per thread and iteration, all loads issued first.
+    for (int64_t b0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b0 < total;
+         b0 += kDynUnroll * stride) {
+        uint4 hv[kDynUnroll][2], wv[kDynUnroll][2];
+        float inv[kDynUnroll];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const uint32_t hs[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-            const uint32_t wsv[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                y[8 * u + 2 * k] = __fmul_rn(__fmul_rn(E::lo(hs[k]), inv), E::lo(wsv[k]));
-                y[8 * u + 2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hs[k]), inv), E::hi(wsv[k]));
+        for (int u = 0; u < kDynUnroll; ++u) {
+            const int64_t b = b0 + u * stride;
+            if (b < total) {
+                const int row = (int)(b / bpr);
+                const int cb = (int)(b - (int64_t)row * bpr);
+                inv[u] = ws[kWsInvOffset + row];
+                hv[u][0] = ld_act(h + (int64_t)row * chunks + 2 * cb);
+                hv[u][1] = ld_act(h + (int64_t)row * chunks + 2 * cb + 1);
+                wv[u][0] = ld_weight(w + 2 * cb);
+                wv[u][1] = ld_weight(w + 2 * cb + 1);
             }
         }
-        uint2 codes;
-        const uint32_t sb = nvfp4_block16(y, gs, s_rtab, codes);
-        st_stream(q + b, codes);
-        bscale[b] = (uint8_t)sb;
+#pragma unroll
+        for (int u = 0; u < kDynUnroll; ++u) {
+            const int64_t b = b0 + u * stride;
+            if (b >= total) break;
+            float y[16];
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const uint32_t hs[4] = {hv[u][v].x, hv[u][v].y, hv[u][v].z, hv[u][v].w};
+                const uint32_t wsv[4] = {wv[u][v].x, wv[u][v].y, wv[u][v].z, wv[u][v].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    y[8 * v + 2 * k] = __fmul_rn(__fmul_rn(E::lo(hs[k]), inv[u]), E::lo(wsv[k]));
+                    y[8 * v + 2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hs[k]), inv[u]), E::hi(wsv[k]));
+                }
+            }
+            uint2 codes;
+            const uint32_t sb = nvfp4_block16(y, gs, s_rtab, codes);
+            st_stream(q + b, codes);
+            bscale[b] = (uint8_t)sb;
+        }
     }
 }
 

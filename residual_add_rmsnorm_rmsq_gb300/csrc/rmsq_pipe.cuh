@@ -108,7 +108,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
             }
         }
         const float total = smem_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1]);
-        const float inv = inv_rms(total, a.hidden, a.eps);
+        const float inv = inv_rms(total, a);
         quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_rtab, s_max[k & 1], tid, nwarps, run_max);
     }
     if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max[0], tid, nwarps);

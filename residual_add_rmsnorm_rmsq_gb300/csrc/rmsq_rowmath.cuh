@@ -51,6 +51,7 @@ struct RowArgs {
     int n;        // rows
     int hidden;   // elements per row
     int chunks;   // hidden / 8
+    float inv_hidden_pow2;   // 2^-k when hidden = 2^k, else 0
 };
 
 template <int MODE> struct ModeTraits {
@@ -89,10 +90,13 @@ __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint
     else return __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
 }
 
-// 1 / sqrt(S / hidden + eps), each step correctly rounded.
-__device__ __forceinline__ float inv_rms(float total, int hidden, float eps) {
-    const float ms = __fdiv_rn(total, (float)hidden);
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+// 1 / sqrt(S / hidden + eps), each step correctly rounded.  For hidden = 2^k
+// the division is the exact scaling S * 2^-k: the same real number, so the
+// same correctly rounded result, without the divide.
+__device__ __forceinline__ float inv_rms(float total, const RowArgs& a) {
+    const float ms = a.inv_hidden_pow2 != 0.0f ? __fmul_rn(total, a.inv_hidden_pow2)
+                                               : __fdiv_rn(total, (float)a.hidden);
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 }
 
 // y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
