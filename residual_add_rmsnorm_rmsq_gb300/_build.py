@@ -48,9 +48,9 @@ def source_digest() -> str:
     return h.hexdigest()
 
 
-def _compile(unit: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
-    cmd = [nvcc()] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + \
+def _compile(unit: str, verbose: bool, build_dir: str = BUILD, extra: list | None = None) -> str:
+    obj = os.path.join(build_dir, unit.replace(".cu", ".o"))
+    cmd = [nvcc()] + NVCC_FLAGS + (extra or []) + (["-Xptxas", "-v"] if verbose else []) + \
         ["-c", os.path.join(CSRC, unit), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -80,6 +80,24 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with open(stamp, "w") as fh:
         fh.write(digest + "\n")
     return LIB
+
+
+def build_variant(name: str, defines: dict) -> str:
+    """Build a separately named copy of the library with compile-time tuning
+    macros set (e.g. {"RMSQ_PIPE_MIN_BLOCKS": 2}), for launch-shape
+    experiments; returns its path.  Results do not depend on these macros."""
+    bdir = os.path.join(BUILD, name)
+    os.makedirs(bdir, exist_ok=True)
+    os.makedirs(LIBDIR, exist_ok=True)
+    extra = [f"-D{k}={v}" for k, v in sorted(defines.items())]
+    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+        objs = list(ex.map(lambda u: _compile(u, False, bdir, extra), UNITS))
+    out = os.path.join(LIBDIR, f"librmsq_{name}.so")
+    cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", out] + objs
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    return out
 
 
 if __name__ == "__main__":

@@ -26,8 +26,20 @@ namespace rmsq {
 // instantiations only).
 static __device__ unsigned int g_pipe_fault;
 
+// Compile-time tuning (results never depend on these): the minimum number of
+// resident CTAs the pipelined kernel is compiled for when a thread owns one
+// or two chunks (the register budget follows from it), and whether the
+// largest shared-memory carve-out is requested.
+#ifndef RMSQ_PIPE_MIN_BLOCKS
+#define RMSQ_PIPE_MIN_BLOCKS 1
+#endif
+#ifndef RMSQ_MAX_SMEM_CARVEOUT
+#define RMSQ_MAX_SMEM_CARVEOUT 1
+#endif
+
 template <class E, int MODE, bool RES, int J>
-__global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : 2)) pipe_entry(const RowArgs a, const int stages) {
+__global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : RMSQ_PIPE_MIN_BLOCKS))
+pipe_entry(const RowArgs a, const int stages) {
     pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
 }
 
@@ -89,7 +101,7 @@ inline cudaError_t ensure_smem_limit(const void* fn) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
     // Prefer the largest shared-memory carve-out so that the rings of several
     // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && RMSQ_MAX_SMEM_CARVEOUT)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && used < 256) done[used++] = fn;

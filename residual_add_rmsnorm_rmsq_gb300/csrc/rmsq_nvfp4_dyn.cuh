@@ -38,7 +38,12 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const float (&y)[16], float gs
     return sb;
 }
 
-constexpr int kDynUnroll = 4;
+// Blocks of 16 each thread of pass 2 loads before computing (compile-time
+// tuning; results do not depend on it).
+#ifndef RMSQ_DYN_UNROLL
+#define RMSQ_DYN_UNROLL 4
+#endif
+constexpr int kDynUnroll = RMSQ_DYN_UNROLL;
 
 template <class E>
 __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, const uint4* w,
