@@ -77,7 +77,7 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm_nvfp4_dynamic.restype = ci
         L.rmsq_nvfp4_dynamic_workspace_bytes.argtypes = [i64]
         L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
-        L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci]
+        L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci, ci]
         L.rmsq_set_pipeline_config.restype = ci
         L.rmsq_take_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.rmsq_take_fault_flags.restype = ci
@@ -216,9 +216,10 @@ def fused_add_rmsnorm_nvfp4_dynamic(x: torch.Tensor, residual: torch.Tensor | No
     return out_q, out_scales, out_global_scale, residual_out
 
 
-def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm: int = 0) -> None:
+def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm: int = 0,
+                        rows_per_iter: int = 0) -> None:
     """Tune the pipelined variant's launch shape (0 = automatic); results are unchanged."""
-    st = load().rmsq_set_pipeline_config(chunks_per_thread, stages, ctas_per_sm)
+    st = load().rmsq_set_pipeline_config(chunks_per_thread, stages, ctas_per_sm, rows_per_iter)
     if st:
         raise RmsqError(st, "rmsq_set_pipeline_config")
 

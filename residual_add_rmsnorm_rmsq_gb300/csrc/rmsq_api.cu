@@ -94,29 +94,31 @@ bool overlaps(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-std::atomic<int> g_tune_j{0}, g_tune_stages{0}, g_tune_cps{0};
+std::atomic<int> g_tune_j{0}, g_tune_stages{0}, g_tune_cps{0}, g_tune_rows{0};
 
 }  // namespace
 
 namespace rmsq {
 PipeTuning get_pipe_tuning() {
     return {g_tune_j.load(std::memory_order_relaxed), g_tune_stages.load(std::memory_order_relaxed),
-            g_tune_cps.load(std::memory_order_relaxed)};
+            g_tune_cps.load(std::memory_order_relaxed), g_tune_rows.load(std::memory_order_relaxed)};
 }
 void set_pipe_tuning(const PipeTuning& t) {
     g_tune_j.store(t.chunks_per_thread, std::memory_order_relaxed);
     g_tune_stages.store(t.stages, std::memory_order_relaxed);
     g_tune_cps.store(t.ctas_per_sm, std::memory_order_relaxed);
+    g_tune_rows.store(t.rows_per_iter, std::memory_order_relaxed);
 }
 }  // namespace rmsq
 
 extern "C" {
 
-int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm) {
+int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm, int rows_per_iter) {
     if (chunks_per_thread != 0 && chunks_per_thread != 1 && chunks_per_thread != 2 && chunks_per_thread != 4)
         return RMSQ_ERR_INVALID_ARG;
     if (stages < 0 || stages > 8 || ctas_per_sm < 0 || ctas_per_sm > 8) return RMSQ_ERR_INVALID_ARG;
-    rmsq::set_pipe_tuning({chunks_per_thread, stages, ctas_per_sm});
+    if (rows_per_iter < 0 || rows_per_iter > 2) return RMSQ_ERR_INVALID_ARG;
+    rmsq::set_pipe_tuning({chunks_per_thread, stages, ctas_per_sm, rows_per_iter});
     return RMSQ_OK;
 }
 

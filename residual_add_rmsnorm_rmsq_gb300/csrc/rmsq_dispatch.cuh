@@ -37,10 +37,10 @@ static __device__ unsigned int g_pipe_fault;
 #define RMSQ_MAX_SMEM_CARVEOUT 1
 #endif
 
-template <class E, int MODE, bool RES, int J>
+template <class E, int MODE, bool RES, int J, int R>
 __global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : RMSQ_PIPE_MIN_BLOCKS))
 pipe_entry(const RowArgs a, const int stages) {
-    pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
+    pipe_body<E, MODE, RES, J, R>(a, stages, &g_pipe_fault);
 }
 
 template <class E, int MODE, bool RES>
@@ -49,30 +49,33 @@ const void* pick_direct(int J) {
     return reinterpret_cast<const void*>(&rows_kernel<E, MODE, RES, 2>);
 }
 
+// Two rows per iteration exist for one and two chunks per thread.
 template <class E, int MODE, bool RES>
-const void* pick_pipe(int J) {
-    if (J == 1) return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1>);
-    if (J == 2) return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2>);
-    return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 4>);
+const void* pick_pipe(int J, int R) {
+    if (J == 1) return R == 2 ? reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1, 2>)
+                              : reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1, 1>);
+    if (J == 2) return R == 2 ? reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2, 2>)
+                              : reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2, 1>);
+    return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 4, 1>);
 }
 
 template <class E, int MODE>
-const void* pick_res(bool res, bool pipe, int J) {
-    if (pipe) return res ? pick_pipe<E, MODE, true>(J) : pick_pipe<E, MODE, false>(J);
+const void* pick_res(bool res, bool pipe, int J, int R) {
+    if (pipe) return res ? pick_pipe<E, MODE, true>(J, R) : pick_pipe<E, MODE, false>(J, R);
     return res ? pick_direct<E, MODE, true>(J) : pick_direct<E, MODE, false>(J);
 }
 
 template <class E>
-const void* pick_kernel(int mode, bool res, bool pipe, int J) {
+const void* pick_kernel(int mode, bool res, bool pipe, int J, int R = 1) {
     switch (mode) {
-    case kFp8Static: return pick_res<E, kFp8Static>(res, pipe, J);
-    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, pipe, J);
-    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, pipe, J);
-    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, pipe, J);
-    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J);
-    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J);
-    case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J);
-    case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J);
+    case kFp8Static: return pick_res<E, kFp8Static>(res, pipe, J, R);
+    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, pipe, J, R);
+    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, pipe, J, R);
+    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, pipe, J, R);
+    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J, R);
+    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J, R);
+    case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J, R);
+    case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J, R);
     default: return nullptr;
     }
 }
@@ -173,12 +176,14 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
             threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
             J = tune.chunks_per_thread;
         const int threads = threads_for(J);
-        const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);
+        const int row_slot = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
+        const int R = (tune.rows_per_iter == 2 && J <= 2 && 2 * row_slot <= kPipeSmemBudget) ? 2 : 1;
+        const int stage_bytes = R * row_slot;
         int stages = pipe_stages(stage_bytes);
         if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
             stages = tune.stages;
         const int smem = stages * stage_bytes;
-        const void* fn = pick_kernel<E>(la.mode, res, true, J);
+        const void* fn = pick_kernel<E>(la.mode, res, true, J, R);
         if (!fn) return cudaErrorInvalidValue;
         int per_sm = pipe_blocks_per_sm(fn, threads, smem, &err);
         if (err != cudaSuccess) return err;

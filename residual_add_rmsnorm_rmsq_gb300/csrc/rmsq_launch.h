@@ -32,6 +32,7 @@ struct PipeTuning {
     int chunks_per_thread;
     int stages;
     int ctas_per_sm;
+    int rows_per_iter;      // 1 or 2 (0 = automatic)
 };
 PipeTuning get_pipe_tuning();
 void set_pipe_tuning(const PipeTuning& t);

@@ -41,7 +41,7 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const float (&y)[16], float gs
 // Blocks of 16 each thread of pass 2 loads before computing (compile-time
 // tuning; results do not depend on it).
 #ifndef RMSQ_DYN_UNROLL
-#define RMSQ_DYN_UNROLL 4
+#define RMSQ_DYN_UNROLL 1
 #endif
 constexpr int kDynUnroll = RMSQ_DYN_UNROLL;
 

@@ -99,6 +99,58 @@ __device__ __forceinline__ float inv_rms(float total, const RowArgs& a) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 }
 
+// y = (h * inv) * w in fp32 for the thread's chunks.
+template <class E, int J>
+__device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const uint4 (&wv)[J], float inv,
+                                          float (&y)[J][8]) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
+            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
+        }
+    }
+}
+
+// E4M3 codes of y / s for the thread's chunks of `row`, stored.
+template <int J>
+__device__ __forceinline__ void store_fp8_codes(const RowArgs& a, int row, const float (&y)[J][8], float s,
+                                                int c0) {
+    const Fp8Recips rc = fp8_recips(s);
+    uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint2 codes = fp8_chunk(y[j], s, rc);
+        if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
+    }
+}
+
+// FP8 per-token, before the CTA barrier: the warp's amax of |y| into s_max[warp].
+template <int J>
+__device__ __forceinline__ void per_token_warp_amax(const float (&y)[J][8], float* s_max, int lane, int warp) {
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+    m = warp_max_nonneg(m);
+    if (lane == 0) s_max[warp] = m;
+}
+
+// FP8 per-token, after the barrier: s = max(amax / 448, 1e-12) from the warp
+// slots, stored by thread 0, and the row's codes.
+template <int J>
+__device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, const float (&y)[J][8],
+                                                 const float* s_max, int tid, int nwarps) {
+    const int lane = tid & 31;
+    const float m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
+    const float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+    if (tid == 0) static_cast<float*>(a.scales)[row] = s;
+    store_fp8_codes<J>(a, row, y, s, tid * J);
+}
+
 // y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
 // `sin` is the static scale (FP8 static) or the global scale (NVFP4);
 // `rtab` the NVFP4 table of gs / decode(code) (fill_nvfp4_rtab), else unused.
@@ -112,17 +164,13 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
     const int lane = tid & 31, warp = tid >> 5;
     const int c0 = tid * J;
     float y[J][8];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
-            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
-        }
-    }
+    compute_y<E, J>(hw, wv, inv, y);
 
-    if constexpr (MODE == kNormAmax) {
+    if constexpr (MODE == kFp8PerToken) {
+        per_token_warp_amax<J>(y, s_max, lane, warp);
+        __syncthreads();
+        per_token_finish<J>(a, row, y, s_max, tid, nwarps);
+    } else if constexpr (MODE == kNormAmax) {
 #pragma unroll
         for (int j = 0; j < J; ++j)
 #pragma unroll
@@ -162,18 +210,6 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
         float s;
         if constexpr (MODE == kFp8Static) {
             s = sin;
-        } else if constexpr (MODE == kFp8PerToken) {
-            float m = 0.0f;
-#pragma unroll
-            for (int j = 0; j < J; ++j)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
-            m = warp_max_nonneg(m);
-            if (lane == 0) s_max[warp] = m;
-            __syncthreads();
-            m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
-            s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
-            if (tid == 0) static_cast<float*>(a.scales)[row] = s;
         } else {
             constexpr int G = ModeTraits<MODE>::group;
             constexpr int LANES = G / 8 / J;   // threads sharing one group
@@ -191,14 +227,8 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
                 else sc[(int64_t)row * (a.hidden / G) + g] = s;
             }
         }
-        const Fp8Recips rc = fp8_recips(s);
         (void)run_max;
-        uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            const uint2 codes = fp8_chunk(y[j], s, rc);
-            if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
-        }
+        store_fp8_codes<J>(a, row, y, s, c0);
     }
 }
 

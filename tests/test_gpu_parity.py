@@ -224,16 +224,37 @@ def test_static_scale_sweep():
         P.check(wl, "fp8_static", scale_in=float(s), label=f"static s={float(s):.3e}")
 
 
-def test_pipelined_launch_shapes_do_not_change_results():
-    wl = ri.make_workload("shapes", 700, 4096, res_sigma=2.0, seed=36)
-    want = oracle.run_workload(wl, "fp8_group64_col", nthreads=8)
+@pytest.mark.parametrize("mode", ["fp8_group64_col", "fp8_per_token", "nvfp4", "fp8_static"])
+def test_pipelined_launch_shapes_do_not_change_results(mode):
+    """Chunks per thread, ring depth, CTAs per SM and rows per iteration
+    (including an odd row count, so the last two-row group has one row)."""
+    wl = ri.make_workload("shapes", 701, 4096, res_sigma=2.0, seed=36)
+    s_in = 0.05 if mode == "fp8_static" else None
+    want = oracle.run_workload(wl, mode, scale_in=s_in, nthreads=8)
     try:
-        for J, stages, cps in ((1, 2, 1), (2, 1, 2), (4, 8, 3), (2, 6, 0), (0, 3, 4)):
-            rq.set_pipeline_config(J, stages, cps)
-            got = P.run_gpu(wl, "fp8_group64_col", None, variant="pipelined")
-            P.compare(got, want, "fp8_group64_col", f"shape J{J} s{stages} c{cps}")
+        for J, stages, cps, rows in ((1, 2, 1, 1), (2, 1, 2, 1), (4, 8, 3, 1), (2, 6, 0, 0), (0, 3, 4, 1),
+                                     (2, 2, 0, 2), (1, 1, 2, 2), (2, 3, 1, 2), (4, 2, 0, 2)):
+            rq.set_pipeline_config(J, stages, cps, rows)
+            got = P.run_gpu(wl, mode, want["scale_in"], variant="pipelined")
+            P.compare(got, want, mode, f"{mode} shape J{J} s{stages} c{cps} r{rows}")
     finally:
-        rq.set_pipeline_config(0, 0, 0)
+        rq.set_pipeline_config(0, 0, 0, 0)
+
+
+def test_nvfp4_dynamic_with_two_rows_per_iteration():
+    wl = ri.make_workload("dyn_r2", 1233, 2048, res_sigma=1.5, seed=39)
+    want = oracle.run_nvfp4_dynamic(wl.x, wl.residual, wl.weight, eps=wl.eps, nthreads=8)
+    x, r, w = P.dev_act(wl.x, "bf16"), P.dev_act(wl.residual, "bf16"), P.dev_act(wl.weight, "bf16")
+    try:
+        for rows in (1, 2):
+            rq.set_pipeline_config(0, 0, 0, rows)
+            q, sc, gs, ro = rq.fused_add_rmsnorm_nvfp4_dynamic(x, r, w, wl.eps, variant="pipelined")
+            torch.cuda.synchronize()
+            assert gs.cpu().numpy().view(np.uint32)[0] == want["global_scale"].view(np.uint32)[0]
+            P.compare({"q": q.cpu().numpy(), "scales": sc.cpu().numpy(), "residual_out": P.host_bits(ro)},
+                      want, "nvfp4", f"dynamic r{rows}")
+    finally:
+        rq.set_pipeline_config(0, 0, 0, 0)
 
 
 def test_pipelined_ring_sizes_in_any_order():
