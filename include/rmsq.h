@@ -219,14 +219,14 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc(const void *x, const void *resi
 /*
  * rmsq_set_pipeline_config — process-wide tuning of the PIPELINED variant:
  * chunks_per_thread (16-byte chunks of a row per thread: 1, 2 or 4), stages
- * (shared-memory ring stages per CTA, each holding rows_per_iter rows: 2..8;
- * 1 is accepted and treated as automatic), ctas_per_sm (cap on resident CTAs
- * per SM: 1..8) and rows_per_iter (rows a CTA works on together: 1 or 2; two
+ * (rows in flight per CTA: 1..8) and ctas_per_sm (cap on resident CTAs per
+ * SM: 1..8) and rows_per_iter (rows a CTA works on together: 1 or 2; two
  * share each block reduction's barrier).  0 keeps the automatic choice for
- * that parameter.  A choice that does not fit the row (more than 512
- * threads, or a ring larger than 220 KiB) falls back to the automatic one.
- * Results do not depend on these settings.  Not synchronised with launches
- * running concurrently on other host threads.
+ * that parameter.  A choice that
+ * does not fit the row (more than 512 threads, or a ring larger than the
+ * shared memory budget) falls back to the automatic one.  Results do not
+ * depend on these settings.  Not synchronised with launches running
+ * concurrently on other host threads.
  */
 int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm, int rows_per_iter);
 

@@ -5,11 +5,11 @@
 //             hidden 8192, else 2), loads straight into registers.
 //  pipelined: persistent CTAs (as many as fit on the SMs), `stages` rows of
 //             x / residual in flight per CTA through the shared-memory ring.
-//             J = 2 up to hidden 8192, else 4 (<= 512 threads); three stages
-//             per CTA when they fit ~110 KB (so that 2-3 CTAs share an SM),
-//             else two: the per-row dependency chain (two block reductions,
-//             IEEE divide and square root) rather than bytes in flight limits
-//             a CTA, so more CTAs per SM beat a deeper ring (measured on GB300).
+//             J = 2 up to hidden 8192, else 4 (<= 512 threads); two stages
+//             per CTA by default, so that up to 3-4 CTAs share an SM: the
+//             per-row dependency chain (two block reductions, IEEE divide and
+//             square root) rather than bytes in flight limits a CTA, so more
+//             CTAs per SM beat a deeper ring (measured on GB300).
 #pragma once
 
 #include <atomic>
@@ -90,9 +90,6 @@ struct OccEntry {
 
 // Shared-memory ring budget per CTA (two CTAs per SM).
 constexpr int kPipeSmemBudget = 110 * 1024;
-// Largest ring: two stages of the widest rows (16384 x 2 B x, residual), one
-// CTA per SM.
-constexpr int kPipeSmemMax = 220 * 1024;
 
 // The opt-in dynamic shared memory limit of a pipelined instantiation is set
 // once, to the full ring budget, so that no later launch ever lowers it below
@@ -104,7 +101,7 @@ inline cudaError_t ensure_smem_limit(const void* fn) {
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (done[i] == fn) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemMax);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
     // Prefer the largest shared-memory carve-out so that the rings of several
     // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
     if (e == cudaSuccess && RMSQ_MAX_SMEM_CARVEOUT)
@@ -144,10 +141,9 @@ inline int sm_count(cudaError_t* err) {
     return v;
 }
 
-// Default ring: three stages (a stage is refilled one iteration after its
-// use, once its bulk stores have read it, so three keep two groups in
-// flight) when they fit the per-CTA budget, else two (the minimum).
-inline int pipe_stages(int stage_bytes) { return 3 * stage_bytes <= kPipeSmemBudget ? 3 : 2; }
+// Default ring: two stages (one row computed while the next is in flight),
+// one when two do not fit the budget.
+inline int pipe_stages(int stage_bytes) { return 2 * stage_bytes <= kPipeSmemBudget ? 2 : 1; }
 
 template <class E>
 cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
@@ -181,10 +177,10 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
             J = tune.chunks_per_thread;
         const int threads = threads_for(J);
         const int row_slot = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
-        const int R = (tune.rows_per_iter == 2 && J <= 2 && 4 * row_slot <= kPipeSmemMax) ? 2 : 1;
+        const int R = (tune.rows_per_iter == 2 && J <= 2 && 2 * row_slot <= kPipeSmemBudget) ? 2 : 1;
         const int stage_bytes = R * row_slot;
         int stages = pipe_stages(stage_bytes);
-        if (tune.stages >= 2 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemMax)
+        if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
             stages = tune.stages;
         const int smem = stages * stage_bytes;
         const void* fn = pick_kernel<E>(la.mode, res, true, J, R);

@@ -1,20 +1,14 @@
 // Pipelined row kernel: persistent CTAs, each walking groups of R rows
-// (rows blockIdx.x + (k*R + r) * gridDim.x for r < R).
+// (rows blockIdx.x + (k*R + r) * gridDim.x for r < R); the x and residual rows
+// of the next `stages` groups are in flight as bulk asynchronous copies (TMA,
+// 1-D) into a ring of shared-memory stages while the current group is
+// computed.  One elected thread issues the copies; a stage is refilled right
+// after the CTA barrier that follows its last shared-memory read.  The weight
+// row is loaded once into registers (every row of the launch uses it).
 //
-// Loads: the x and residual rows of the next groups are in flight as bulk
-// asynchronous copies (TMA, 1-D) into a ring of shared-memory stages (at
-// least two) while the current group is computed; one elected thread issues
-// them.  The weight row is loaded once into registers.
-//
-// Stores: the updated residual h is written back into the stage over the x
-// row it came from, and the codes over the residual row (over x without a
-// residual); each warp then writes its contiguous slice of both with one
-// bulk copy per tensor, so HBM sees whole lines instead of the half-sector
-// pieces that per-thread stores of consecutive chunks would produce.  A stage
-// is refilled one iteration later, after every warp has seen its bulk stores
-// finish reading it (cp.async.bulk.wait_group.read before the barrier).
-//
-// R = 2 interleaves two rows: their reductions share each CTA barrier.
+// R = 2 interleaves two rows: their reductions share each CTA barrier, so the
+// latency of the per-row dependency chain (block reductions, IEEE divide and
+// square root) is paid once per two rows.
 //
 // Per row the arithmetic is the same as the direct kernel's (rmsq_rowmath.cuh):
 // the canonical pairwise tree for the sum of squares, correctly rounded
@@ -46,15 +40,6 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     const uint32_t row_bytes = static_cast<uint32_t>(a.chunks) * 16u;
     const uint32_t slot_bytes = RES ? 2u * row_bytes : row_bytes;   // one row of x (+ residual)
     const uint32_t stage_bytes = R * slot_bytes;
-
-    // This warp's slice of a row: chunks [w0, w0 + wn).
-    const int w0 = warp * 32 * J;
-    const int wn = min(32 * J, a.chunks - w0);
-    // Codes go out by bulk copy when every warp slice starts on 16 bytes.
-    constexpr bool HAS_Q = MODE != kNormAmax;
-    constexpr int QB = MODE == kNvfp4 ? 4 : 8;   // code bytes per chunk
-    const bool bulk_q = HAS_Q && (a.hidden % 32) == 0;
-    const int64_t q_row_bytes = (int64_t)a.chunks * QB;
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
@@ -109,7 +94,6 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         const int s = k % stages;
         const uint32_t parity = static_cast<uint32_t>(k / stages) & 1u;
         const bool ok = mbar_wait_bounded(&full[s], parity);
-        unsigned char* stage = ring + (size_t)s * stage_bytes;
 
         uint32_t hw[R][J][4];
         float acc[R];
@@ -120,7 +104,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
 #pragma unroll
             for (int j = 0; j < J; ++j) hw[r][j][0] = hw[r][j][1] = hw[r][j][2] = hw[r][j][3] = 0u;
             if (ok && row < a.n) {
-                uint4* sx = reinterpret_cast<uint4*>(stage + (size_t)r * slot_bytes);
+                const uint4* sx =
+                    reinterpret_cast<const uint4*>(ring + (size_t)s * stage_bytes + (size_t)r * slot_bytes);
                 uint4 xv[J], rv[J];
 #pragma unroll
                 for (int j = 0; j < J; ++j) {
@@ -130,24 +115,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                         if constexpr (RES) rv[j] = sx[a.chunks + c0 + j];
                     }
                 }
-                // h goes back over this thread's own x chunks of the stage.
                 acc[r] = combine_chunks<E, RES, J>(xv, rv, hw[r], a.res_out + (int64_t)row * a.chunks, c0,
-                                                   a.chunks, RES ? sx : nullptr);
-            }
-        }
-        if constexpr (RES) {
-            // The warp's slices of h are complete: one bulk store per row.
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0 && ok) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = row0 + r * G;
-                    if (row < a.n)
-                        bulk_s2g(a.res_out + (int64_t)row * a.chunks + w0,
-                                 stage + (size_t)r * slot_bytes + (size_t)w0 * 16, (uint32_t)wn * 16u);
-                }
-                bulk_commit();
+                                                   a.chunks);
             }
         }
 #pragma unroll
@@ -155,28 +124,17 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
             acc[r] = warp_tree_sum(acc[r]);
             if (lane == 0) s_sum[k & 1][r][warp] = acc[r];
         }
-        // Every earlier bulk store of this warp has finished reading its stage
-        // (all but the h store just issued, with a residual).
-        if (lane == 0) {
-            if constexpr (RES) bulk_wait_read<1>();
-            else bulk_wait_read<0>();
-        }
+        // All reads of stage s are done once every thread is past this barrier.
         if (__syncthreads_or(!ok)) {
             faulted = true;
             break;
         }
-        // The previous iteration's stage is free: refill it.
-        if (tid == 0 && k > 0 && blockIdx.x + (k - 1 + stages) * R * G < a.n)
-            issue(k - 1 + stages, (k - 1) % stages);
+        if (tid == 0 && blockIdx.x + (k + stages) * R * G < a.n) issue(k + stages, s);
 
         float inv[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) inv[r] = inv_rms(smem_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1][r]), a);
 
-        // Codes are staged over the residual row (over x without a residual).
-        auto q_stage = [&](int r) -> uint8_t* {
-            return bulk_q ? stage + (size_t)r * slot_bytes + (RES ? row_bytes : 0u) : nullptr;
-        };
         if constexpr (MODE == kFp8PerToken && R > 1) {
             // The rows' amax reductions share one barrier.
             float y[R][J][8];
@@ -189,7 +147,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
 #pragma unroll
             for (int r = 0; r < R; ++r)
                 if (row0 + r * G < a.n)
-                    per_token_finish<J>(a, row0 + r * G, y[r], s_max[k & 1][r], tid, nwarps, q_stage(r));
+                    per_token_finish<J>(a, row0 + r * G, y[r], s_max[k & 1][r], tid, nwarps);
         } else {
             // No barrier inside quantize_row for these modes (per-token only with R == 1,
             // where every thread takes the r == 0 call).
@@ -197,32 +155,15 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
             for (int r = 0; r < R; ++r)
                 if (r == 0 || row0 + r * G < a.n)
                     quantize_row<E, MODE, J>(a, row0 + r * G, hw[r], wv, inv[r], sin, s_rtab, s_max[k & 1][r],
-                                             tid, nwarps, run_max, q_stage(r));
-        }
-        if (bulk_q) {
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int row = row0 + r * G;
-                    if (row < a.n)
-                        bulk_s2g(a.q + row * q_row_bytes + (int64_t)w0 * QB, q_stage(r) + (size_t)w0 * QB,
-                                 (uint32_t)(wn * QB));
-                }
-                bulk_commit();
-            }
+                                             tid, nwarps, run_max);
         }
     }
     if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max[0][0], tid, nwarps);
-    if (lane == 0) bulk_wait_all();   // stages stay valid until this warp's stores are done
 
     if (faulted && tid == 0) {
         atomicOr(fault, 1u);
-        // Loads issued for row groups k .. last may still be in flight: the
-        // prologue issued groups 0 .. stages-1, iteration i >= 1 group i-1+stages.
-        const int last = (k == 0) ? stages - 1 : k + stages - 2;
-        for (int kk = k; kk <= last; ++kk) {
+        // Copies issued for row groups k .. k + stages - 1 may still be in flight.
+        for (int kk = k; kk < k + stages; ++kk) {
             if (blockIdx.x + kk * R * G >= a.n) break;
             mbar_wait_bounded(&full[kk % stages], static_cast<uint32_t>(kk / stages) & 1u);
         }

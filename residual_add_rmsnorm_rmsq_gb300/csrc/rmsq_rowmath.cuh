@@ -63,13 +63,11 @@ template <int MODE> struct ModeTraits {
 
 // h = T(x + r) for the thread's chunks (h = x without a residual), the
 // residual write-back, and the thread's partial of the sum-of-squares tree.
-// The write-back goes to `h_stage` (shared memory, row-relative chunk index)
-// when given, for a later bulk store, else straight to `res_out_row`.
 // Chunks at or beyond `chunks` hold zeros and are not stored.
 template <class E, bool RES, int J>
 __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
                                                 uint32_t (&hw)[J][4], uint4* res_out_row,
-                                                int c0, int chunks, uint4* h_stage = nullptr) {
+                                                int c0, int chunks) {
     float part[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -78,11 +76,8 @@ __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint
             const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) hw[j][k] = E::add2(hw[j][k], rs[k]);
-            if (c0 + j < chunks) {
-                const uint4 v = make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]);
-                if (h_stage) h_stage[c0 + j] = v;
-                else st_stream(res_out_row + c0 + j, v);
-            }
+            if (c0 + j < chunks)
+                st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
         }
         float h[8];
 #pragma unroll
@@ -119,21 +114,16 @@ __device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const uint
     }
 }
 
-// E4M3 codes of y / s for the thread's chunks of `row`: into `q_stage`
-// (shared memory, row-relative) when given, for a later bulk store, else
-// straight to global memory.
+// E4M3 codes of y / s for the thread's chunks of `row`, stored.
 template <int J>
 __device__ __forceinline__ void store_fp8_codes(const RowArgs& a, int row, const float (&y)[J][8], float s,
-                                                int c0, uint8_t* q_stage) {
+                                                int c0) {
     const Fp8Recips rc = fp8_recips(s);
     uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const uint2 codes = fp8_chunk(y[j], s, rc);
-        if (c0 + j < a.chunks) {
-            if (q_stage) reinterpret_cast<uint2*>(q_stage)[c0 + j] = codes;
-            else st_stream(qrow + c0 + j, codes);
-        }
+        if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
     }
 }
 
@@ -153,12 +143,12 @@ __device__ __forceinline__ void per_token_warp_amax(const float (&y)[J][8], floa
 // slots, stored by thread 0, and the row's codes.
 template <int J>
 __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, const float (&y)[J][8],
-                                                 const float* s_max, int tid, int nwarps, uint8_t* q_stage) {
+                                                 const float* s_max, int tid, int nwarps) {
     const int lane = tid & 31;
     const float m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
     const float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
     if (tid == 0) static_cast<float*>(a.scales)[row] = s;
-    store_fp8_codes<J>(a, row, y, s, tid * J, q_stage);
+    store_fp8_codes<J>(a, row, y, s, tid * J);
 }
 
 // y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
@@ -170,7 +160,7 @@ template <class E, int MODE, int J>
 __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
                                              const uint4 (&wv)[J], float inv, float sin,
                                              const float* rtab, float* s_max, int tid, int nwarps,
-                                             float& run_max, uint8_t* q_stage = nullptr) {
+                                             float& run_max) {
     const int lane = tid & 31, warp = tid >> 5;
     const int c0 = tid * J;
     float y[J][8];
@@ -179,7 +169,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
     if constexpr (MODE == kFp8PerToken) {
         per_token_warp_amax<J>(y, s_max, lane, warp);
         __syncthreads();
-        per_token_finish<J>(a, row, y, s_max, tid, nwarps, q_stage);
+        per_token_finish<J>(a, row, y, s_max, tid, nwarps);
     } else if constexpr (MODE == kNormAmax) {
 #pragma unroll
         for (int j = 0; j < J; ++j)
@@ -212,11 +202,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
                 float v[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(y[j + u][k], r);
-                if (c + u < a.chunks) {
-                    const uint32_t codes = e2m1x8(v);
-                    if (q_stage) reinterpret_cast<uint32_t*>(q_stage)[c + u] = codes;
-                    else st_stream(qrow + c + u, codes);
-                }
+                if (c + u < a.chunks) st_stream(qrow + c + u, e2m1x8(v));
             }
             if (c < a.chunks && (c & 1) == 0) bsc[c >> 1] = (uint8_t)sb;
         }
@@ -242,7 +228,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
             }
         }
         (void)run_max;
-        store_fp8_codes<J>(a, row, y, s, c0, q_stage);
+        store_fp8_codes<J>(a, row, y, s, c0);
     }
 }
 
