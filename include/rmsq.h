@@ -231,6 +231,20 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc(const void *x, const void *resi
 int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm, int rows_per_iter);
 
 /*
+ * rmsq_set_programmatic_launch — process-wide: 1 (the default) launches every
+ * kernel with programmatic stream serialisation (programmatic dependent
+ * launch), 0 with plain stream order.  With it, a kernel may be scheduled
+ * while the previous kernel in the stream is still finishing, which hides the
+ * launch gap between back-to-back calls (in a CUDA graph as well); each
+ * kernel still waits for the previous one to complete, with its memory
+ * visible, before its first global memory access, so stream semantics and
+ * results are unchanged.  The pages have no counterpart: it is a launch
+ * detail of this implementation.  Returns RMSQ_ERR_INVALID_ARG for a value
+ * other than 0 or 1.  Not synchronised with launches on other host threads.
+ */
+int rmsq_set_programmatic_launch(int enable);
+
+/*
  * rmsq_take_fault_flags — reads and clears, on the current device, the flag a
  * pipelined launch sets if it ever gives up waiting (after 100 ms) for its
  * own shared-memory copies; the outputs of such a launch are incomplete.

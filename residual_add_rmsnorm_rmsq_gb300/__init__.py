@@ -39,7 +39,8 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc",
-           "rmsq_set_pipeline_config", "rmsq_take_fault_flags", "rmsq_query_sizes", "rmsq_debug_convert",
+           "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
+           "rmsq_query_sizes", "rmsq_debug_convert",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
 
@@ -79,6 +80,8 @@ def load(path: str | None = None):
         L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
         L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci, ci]
         L.rmsq_set_pipeline_config.restype = ci
+        L.rmsq_set_programmatic_launch.argtypes = [ci]
+        L.rmsq_set_programmatic_launch.restype = ci
         L.rmsq_take_fault_flags.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         L.rmsq_take_fault_flags.restype = ci
         L.rmsq_query_sizes.argtypes = [ci, i64, i64, ctypes.POINTER(ctypes.c_size_t),
@@ -222,6 +225,13 @@ def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm
     st = load().rmsq_set_pipeline_config(chunks_per_thread, stages, ctas_per_sm, rows_per_iter)
     if st:
         raise RmsqError(st, "rmsq_set_pipeline_config")
+
+
+def set_programmatic_launch(enable: bool) -> None:
+    """Launch with programmatic dependent launch (default) or plain stream order."""
+    st = load().rmsq_set_programmatic_launch(1 if enable else 0)
+    if st:
+        raise RmsqError(st, "rmsq_set_programmatic_launch")
 
 
 def take_fault_flags() -> int:

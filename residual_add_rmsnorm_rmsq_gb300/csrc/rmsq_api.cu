@@ -95,6 +95,7 @@ bool overlaps(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 std::atomic<int> g_tune_j{0}, g_tune_stages{0}, g_tune_cps{0}, g_tune_rows{0};
+std::atomic<bool> g_pdl{true};
 
 }  // namespace
 
@@ -109,6 +110,8 @@ void set_pipe_tuning(const PipeTuning& t) {
     g_tune_cps.store(t.ctas_per_sm, std::memory_order_relaxed);
     g_tune_rows.store(t.rows_per_iter, std::memory_order_relaxed);
 }
+bool programmatic_launch() { return g_pdl.load(std::memory_order_relaxed); }
+void set_programmatic_launch(bool on) { g_pdl.store(on, std::memory_order_relaxed); }
 }  // namespace rmsq
 
 extern "C" {
@@ -119,6 +122,12 @@ int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm,
     if (stages < 0 || stages > 8 || ctas_per_sm < 0 || ctas_per_sm > 8) return RMSQ_ERR_INVALID_ARG;
     if (rows_per_iter < 0 || rows_per_iter > 2) return RMSQ_ERR_INVALID_ARG;
     rmsq::set_pipe_tuning({chunks_per_thread, stages, ctas_per_sm, rows_per_iter});
+    return RMSQ_OK;
+}
+
+int rmsq_set_programmatic_launch(int enable) {
+    if (enable != 0 && enable != 1) return RMSQ_ERR_INVALID_ARG;
+    rmsq::set_programmatic_launch(enable == 1);
     return RMSQ_OK;
 }
 

@@ -84,12 +84,76 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Two adjacent 16-byte chunks as one 256-bit access (sm_100 and later): a
+// warp whose threads own chunk pairs then touches whole 32-byte sectors per
+// instruction instead of half a sector per thread.  p must be 32-byte aligned.
+__device__ __forceinline__ void ld_act_pair(const uint4* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_stream_pair(uint4* p, const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]),
+                    "r"(b[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
     asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
 __device__ __forceinline__ void st_stream(uint32_t* p, uint32_t v) {
     asm volatile("st.global.cs.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream is still
+// running.  grid_dependency_wait() returns once that kernel has completed and
+// its memory operations are visible; every global memory access of a kernel
+// comes after it.  (Launched without the attribute, it returns at once.)
+// allow_dependents() lets the next kernel of the stream start early; that
+// kernel in turn waits for this one to complete before touching memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (sm_100 and later): one instruction does two independent
+// IEEE operations, each rounded to nearest-even exactly as the scalar .rn
+// form (subnormals kept).  Without RMSQ_F32X2 the same pairs are done as two
+// scalar operations, with identical results.
+// ---------------------------------------------------------------------------
+#ifndef RMSQ_F32X2
+#define RMSQ_F32X2 1
+#endif
+
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+#if RMSQ_F32X2
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+#else
+    return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+#endif
+}
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+#if RMSQ_F32X2
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+#else
+    return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -158,38 +222,80 @@ __device__ __forceinline__ Fp8Recips fp8_recips(float s) {
             __fmul_rn(r, 1.000003814697265625f)};      // 1 + 2^-18
 }
 
-// Eight fp32 -> eight E4M3 codes of v[k] / s, element k in byte k.  The
-// bracketing test of fp8_pair is applied to the whole chunk at once (one
+// E4M3 codes of v[k] / s, element k in byte k, for the eight elements of a
+// chunk.  The bracketing test is applied to the whole chunk at once (one
 // branch per eight elements); the rare chunk with a code that differs between
 // the two ends is redone with correctly rounded divisions.
+__device__ __forceinline__ uint2 fp8_chunk_exact(const float (&v)[8], float s) {
+    uint32_t ex[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) ex[p] = e4m3x2(__fdiv_rn(v[2 * p], s), __fdiv_rn(v[2 * p + 1], s));
+    return make_uint2(ex[0] | (ex[1] << 16), ex[2] | (ex[3] << 16));
+}
+
+// One chunk; the bracket products are formed in packed pairs (k, k + 1) and
+// turned into codes right away.
 __device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s, Fp8Recips rc) {
     uint32_t dn[4], up[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        dn[p] = e4m3x2(__fmul_rn(v[2 * p], rc.rdn), __fmul_rn(v[2 * p + 1], rc.rdn));
-        up[p] = e4m3x2(__fmul_rn(v[2 * p], rc.rup), __fmul_rn(v[2 * p + 1], rc.rup));
+        const float2 e = make_float2(v[2 * p], v[2 * p + 1]);
+        const float2 d = mul2_rn(e, make_float2(rc.rdn, rc.rdn));
+        const float2 u = mul2_rn(e, make_float2(rc.rup, rc.rup));
+        dn[p] = e4m3x2(d.x, d.y);
+        up[p] = e4m3x2(u.x, u.y);
     }
-    uint2 out;
-    out.x = dn[0] | (dn[1] << 16);
-    out.y = dn[2] | (dn[3] << 16);
-    const uint32_t ux = up[0] | (up[1] << 16), uy = up[2] | (up[3] << 16);
-    if (((out.x ^ ux) | (out.y ^ uy)) != 0u) {
-        uint32_t ex[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) ex[p] = e4m3x2(__fdiv_rn(v[2 * p], s), __fdiv_rn(v[2 * p + 1], s));
-        out.x = ex[0] | (ex[1] << 16);
-        out.y = ex[2] | (ex[3] << 16);
-    }
+    uint2 out = make_uint2(dn[0] | (dn[1] << 16), dn[2] | (dn[3] << 16));
+    if (((out.x ^ (up[0] | (up[1] << 16))) | (out.y ^ (up[2] | (up[3] << 16)))) != 0u)
+        out = fp8_chunk_exact(v, s);
     return out;
 }
 
-// Pairwise tree over the squares of eight consecutive elements.
+// Two chunks a, b at once; the bracket products are formed in packed pairs
+// (a[k], b[k]) and turned into codes right away.
+__device__ __forceinline__ void fp8_chunk2(const float (&a)[8], const float (&b)[8], float s, Fp8Recips rc,
+                                           uint2& ca, uint2& cb) {
+    uint32_t dna[4], dnb[4], diff = 0u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 e0 = make_float2(a[2 * p], b[2 * p]), e1 = make_float2(a[2 * p + 1], b[2 * p + 1]);
+        const float2 d0 = mul2_rn(e0, make_float2(rc.rdn, rc.rdn)), d1 = mul2_rn(e1, make_float2(rc.rdn, rc.rdn));
+        const float2 u0 = mul2_rn(e0, make_float2(rc.rup, rc.rup)), u1 = mul2_rn(e1, make_float2(rc.rup, rc.rup));
+        dna[p] = e4m3x2(d0.x, d1.x);
+        dnb[p] = e4m3x2(d0.y, d1.y);
+        diff |= (dna[p] ^ e4m3x2(u0.x, u1.x)) | ((dnb[p] ^ e4m3x2(u0.y, u1.y)) << 16);
+    }
+    ca = make_uint2(dna[0] | (dna[1] << 16), dna[2] | (dna[3] << 16));
+    cb = make_uint2(dnb[0] | (dnb[1] << 16), dnb[2] | (dnb[3] << 16));
+    if (diff != 0u) {   // rare: redo both chunks exactly
+        ca = fp8_chunk_exact(a, s);
+        cb = fp8_chunk_exact(b, s);
+    }
+}
+
+// Pairwise tree over the squares of eight consecutive elements, in packed
+// pairs: (h0, h2) and (h1, h3) squared and added give the two level-1 nodes
+// h0^2 + h1^2 and h2^2 + h3^2 at once (likewise for h4..h7).
 __device__ __forceinline__ float leaf8_sumsq(const float (&h)[8]) {
-    const float a = __fadd_rn(__fmul_rn(h[0], h[0]), __fmul_rn(h[1], h[1]));
-    const float b = __fadd_rn(__fmul_rn(h[2], h[2]), __fmul_rn(h[3], h[3]));
-    const float c = __fadd_rn(__fmul_rn(h[4], h[4]), __fmul_rn(h[5], h[5]));
-    const float d = __fadd_rn(__fmul_rn(h[6], h[6]), __fmul_rn(h[7], h[7]));
-    return __fadd_rn(__fadd_rn(a, b), __fadd_rn(c, d));
+    const float2 p02 = make_float2(h[0], h[2]), p13 = make_float2(h[1], h[3]);
+    const float2 p46 = make_float2(h[4], h[6]), p57 = make_float2(h[5], h[7]);
+    const float2 ab = add2_rn(mul2_rn(p02, p02), mul2_rn(p13, p13));
+    const float2 cd = add2_rn(mul2_rn(p46, p46), mul2_rn(p57, p57));
+    return __fadd_rn(__fadd_rn(ab.x, ab.y), __fadd_rn(cd.x, cd.y));
+}
+
+// The leaf trees of two chunks a, b at once, element k of both in one packed
+// pair: returns (tree(a), tree(b)).
+__device__ __forceinline__ float2 leaf8_sumsq2(const float (&a)[8], const float (&b)[8]) {
+    float2 sq[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 p = make_float2(a[k], b[k]);
+        sq[k] = mul2_rn(p, p);
+    }
+    const float2 l0 = add2_rn(sq[0], sq[1]), l1 = add2_rn(sq[2], sq[3]);
+    const float2 l2 = add2_rn(sq[4], sq[5]), l3 = add2_rn(sq[6], sq[7]);
+    return add2_rn(add2_rn(l0, l1), add2_rn(l2, l3));
 }
 
 // Butterfly sum over the 32 lanes: at step k lanes differing in bit k add

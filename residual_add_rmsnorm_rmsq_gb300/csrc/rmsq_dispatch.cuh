@@ -36,6 +36,10 @@ static __device__ unsigned int g_pipe_fault;
 #ifndef RMSQ_MAX_SMEM_CARVEOUT
 #define RMSQ_MAX_SMEM_CARVEOUT 1
 #endif
+// Paired (32-byte) activation accesses where the buffers allow them.
+#ifndef RMSQ_PAIR_ACCESS
+#define RMSQ_PAIR_ACCESS 1
+#endif
 
 template <class E, int MODE, bool RES, int J, int R>
 __global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : RMSQ_PIPE_MIN_BLOCKS))
@@ -78,6 +82,24 @@ const void* pick_kernel(int mode, bool res, bool pipe, int J, int R = 1) {
     case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J, R);
     default: return nullptr;
     }
+}
+
+// One kernel launch, with programmatic stream serialisation unless it is
+// switched off: the kernel may then start while the previous kernel of the
+// stream finishes; the kernels wait for it before any memory access.
+inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, void** params, size_t smem,
+                                 cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic_launch() ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, params);
 }
 
 // Occupancy of a pipelined instantiation for a given ring size, cached.
@@ -161,6 +183,9 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     a.chunks = la.hidden / 8;
     a.inv_hidden_pow2 = (la.hidden & (la.hidden - 1)) == 0 ? 1.0f / (float)la.hidden : 0.0f;
     const bool res = la.res != nullptr;
+    auto on = [](const void* p, uintptr_t b) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % b == 0; };
+    a.pair = RMSQ_PAIR_ACCESS && a.chunks % 2 == 0 && on(la.x, 32) && on(la.res, 32) &&
+             on(la.res_out, 32) && on(la.q, 16);
 
     cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
@@ -192,14 +217,14 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
         const int grid = a.n < per_sm * sms ? a.n : per_sm * sms;
         int st = stages;
         void* params[] = {&a, &st};
-        return cudaLaunchKernel(fn, dim3(grid), dim3(threads), params, smem, stream);
+        return launch_kernel(fn, dim3(grid), dim3(threads), params, smem, stream);
     }
     const int J = a.chunks <= 1024 ? 1 : 2;
     const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
     const void* fn = pick_kernel<E>(la.mode, res, false, J);
     if (!fn) return cudaErrorInvalidValue;
     void* params[] = {&a};
-    return cudaLaunchKernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+    return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
 }
 
 // NVFP4 with a data-derived global scale: zero the workspace's amax word,
@@ -221,11 +246,15 @@ cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* o
     if (e != cudaSuccess) return e;
     int64_t grid = (blocks_total + 256 * kDynUnroll - 1) / (256 * kDynUnroll);
     if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
-    const void* h = la.res ? la.res_out : la.x;
-    nvfp4_dyn_quant_kernel<E><<<(int)grid, 256, 0, stream>>>(
-        static_cast<const uint4*>(h), static_cast<const uint4*>(la.w), static_cast<const float*>(workspace),
-        static_cast<uint2*>(la.q), static_cast<uint8_t*>(la.scales), out_gs, la.n, la.hidden);
-    return cudaGetLastError();
+    const uint4* h = static_cast<const uint4*>(la.res ? la.res_out : la.x);
+    const uint4* w = static_cast<const uint4*>(la.w);
+    const float* ws = static_cast<const float*>(workspace);
+    uint2* q = static_cast<uint2*>(la.q);
+    uint8_t* bs = static_cast<uint8_t*>(la.scales);
+    int n = la.n, hidden = la.hidden;
+    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden};
+    return launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_quant_kernel<E>), dim3((unsigned)grid),
+                         dim3(256), params, 0, stream);
 }
 
 // Reads and clears this unit's pipeline fault flag (current device).

@@ -37,6 +37,11 @@ struct PipeTuning {
 PipeTuning get_pipe_tuning();
 void set_pipe_tuning(const PipeTuning& t);
 
+// Whether the kernels are launched with programmatic stream serialisation
+// (process-wide, on by default).
+bool programmatic_launch();
+void set_programmatic_launch(bool on);
+
 // One launch of the row kernel for bf16 / fp16 activations.
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);

@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, co
                                                               const float* ws, uint2* q,
                                                               uint8_t* bscale, float* out_gs,
                                                               int n, int hidden) {
+    allow_dependents();
+    grid_dependency_wait();
     const float amax = __uint_as_float(reinterpret_cast<const unsigned int*>(ws)[0]);
     const float gs = amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 0) *out_gs = gs;

@@ -48,6 +48,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     if (tid < 64 && (tid & 31) >= nwarps)   // slots of absent warps read as 0
 #pragma unroll
         for (int r = 0; r < R; ++r) s_sum[tid >> 5][r][tid & 31] = 0.0f;
+    allow_dependents();
+    grid_dependency_wait();
     __syncthreads();
 
     // Thread 0: start the copies of row group k into stage s.
@@ -116,7 +118,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                     }
                 }
                 acc[r] = combine_chunks<E, RES, J>(xv, rv, hw[r], a.res_out + (int64_t)row * a.chunks, c0,
-                                                   a.chunks);
+                                                   a.chunks, a.pair);
             }
         }
 #pragma unroll

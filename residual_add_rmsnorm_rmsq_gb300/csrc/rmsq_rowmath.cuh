@@ -52,6 +52,10 @@ struct RowArgs {
     int hidden;   // elements per row
     int chunks;   // hidden / 8
     float inv_hidden_pow2;   // 2^-k when hidden = 2^k, else 0
+    // Chunk pairs (2m, 2m+1) of a row are stored (and, by the direct kernel,
+    // loaded) as one access: set when `chunks` is even, x / residual /
+    // residual_out start on 32 bytes and the codes on 16 bytes.
+    bool pair;
 };
 
 template <int MODE> struct ModeTraits {
@@ -64,10 +68,12 @@ template <int MODE> struct ModeTraits {
 // h = T(x + r) for the thread's chunks (h = x without a residual), the
 // residual write-back, and the thread's partial of the sum-of-squares tree.
 // Chunks at or beyond `chunks` hold zeros and are not stored.
+// With `pair` (J >= 2, chunks even) each chunk pair of the write-back is one
+// 32-byte store.
 template <class E, bool RES, int J>
 __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
                                                 uint32_t (&hw)[J][4], uint4* res_out_row,
-                                                int c0, int chunks) {
+                                                int c0, int chunks, bool pair) {
     float part[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -76,13 +82,34 @@ __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint
             const uint32_t rs[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) hw[j][k] = E::add2(hw[j][k], rs[k]);
-            if (c0 + j < chunks)
-                st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
         }
-        float h[8];
+    }
+    if constexpr (RES) {
+        if (J >= 2 && pair) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) { h[2 * k] = E::lo(hw[j][k]); h[2 * k + 1] = E::hi(hw[j][k]); }
-        part[j] = leaf8_sumsq(h);
+            for (int j = 0; j + 1 < J; j += 2)
+                if (c0 + j < chunks) st_stream_pair(res_out_row + c0 + j, hw[j], hw[j + 1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (c0 + j < chunks)
+                    st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
+        }
+    }
+    float h[J][8];
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { h[j][2 * k] = E::lo(hw[j][k]); h[j][2 * k + 1] = E::hi(hw[j][k]); }
+    if constexpr (J == 1) {
+        part[0] = leaf8_sumsq(h[0]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; j += 2) {   // two chunks' leaf trees in packed pairs
+            const float2 pp = leaf8_sumsq2(h[j], h[j + 1]);
+            part[j] = pp.x;
+            part[j + 1] = pp.y;
+        }
     }
     static_assert(J == 1 || J == 2 || J == 4, "J must be 1, 2 or 4");
     if constexpr (J == 1) return part[0];
@@ -99,18 +126,39 @@ __device__ __forceinline__ float inv_rms(float total, const RowArgs& a) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 }
 
-// y = (h * inv) * w in fp32 for the thread's chunks.
+// y = (h * inv) * w in fp32 for the thread's chunks, in packed pairs: element
+// k of chunks j and j + 1 (J >= 2), elements k and k + 2 of the chunk (J == 1).
 template <class E, int J>
 __device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const uint4 (&wv)[J], float inv,
                                           float (&y)[J][8]) {
+    float h[J][8], w[J][8];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            y[j][2 * k] = __fmul_rn(__fmul_rn(E::lo(hw[j][k]), inv), E::lo(ws[k]));
-            y[j][2 * k + 1] = __fmul_rn(__fmul_rn(E::hi(hw[j][k]), inv), E::hi(ws[k]));
+            h[j][2 * k] = E::lo(hw[j][k]); h[j][2 * k + 1] = E::hi(hw[j][k]);
+            w[j][2 * k] = E::lo(ws[k]); w[j][2 * k + 1] = E::hi(ws[k]);
         }
+    }
+    const float2 iv = make_float2(inv, inv);
+    if constexpr (J == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int k = (q & 1) + 4 * (q >> 1);
+            const float2 t = mul2_rn(mul2_rn(make_float2(h[0][k], h[0][k + 2]), iv),
+                                     make_float2(w[0][k], w[0][k + 2]));
+            y[0][k] = t.x; y[0][k + 2] = t.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; j += 2)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 t = mul2_rn(mul2_rn(make_float2(h[j][k], h[j + 1][k]), iv),
+                                         make_float2(w[j][k], w[j + 1][k]));
+                y[j][k] = t.x; y[j + 1][k] = t.y;
+            }
     }
 }
 
@@ -120,10 +168,23 @@ __device__ __forceinline__ void store_fp8_codes(const RowArgs& a, int row, const
                                                 int c0) {
     const Fp8Recips rc = fp8_recips(s);
     uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
+    uint2 codes[J];
+    if constexpr (J == 1) {
+        codes[0] = fp8_chunk(y[0], s, rc);
+    } else {
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const uint2 codes = fp8_chunk(y[j], s, rc);
-        if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes);
+        for (int j = 0; j < J; j += 2) fp8_chunk2(y[j], y[j + 1], s, rc, codes[j], codes[j + 1]);
+    }
+    if (J >= 2 && a.pair) {   // a chunk pair's 16 code bytes in one store
+#pragma unroll
+        for (int j = 0; j + 1 < J; j += 2)
+            if (c0 + j < a.chunks)
+                st_stream(reinterpret_cast<uint4*>(qrow + c0 + j),
+                          make_uint4(codes[j].x, codes[j].y, codes[j + 1].x, codes[j + 1].y));
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (c0 + j < a.chunks) st_stream(qrow + c0 + j, codes[j]);
     }
 }
 
@@ -197,12 +258,33 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
             const float r = rtab[sb];      // gs / decode(sb), 0 for a zero block scale
             const int c = c0 + j;
             constexpr int NC = (J == 1) ? 1 : 2;
-#pragma unroll
-            for (int u = 0; u < NC; ++u) {
+            uint32_t codes[NC];
+            const float2 rr = make_float2(r, r);
+            if constexpr (NC == 1) {
                 float v[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = __fmul_rn(y[j + u][k], r);
-                if (c + u < a.chunks) st_stream(qrow + c + u, e2m1x8(v));
+                for (int q = 0; q < 4; ++q) {
+                    const int k = (q & 1) + 4 * (q >> 1);
+                    const float2 t = mul2_rn(make_float2(y[j][k], y[j][k + 2]), rr);
+                    v[k] = t.x; v[k + 2] = t.y;
+                }
+                codes[0] = e2m1x8(v);
+            } else {
+                float v0[8], v1[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float2 t = mul2_rn(make_float2(y[j][k], y[j + 1][k]), rr);
+                    v0[k] = t.x; v1[k] = t.y;
+                }
+                codes[0] = e2m1x8(v0);
+                codes[NC - 1] = e2m1x8(v1);
+            }
+            if (NC == 2 && a.pair) {   // the block's 8 code bytes in one store
+                if (c < a.chunks) st_stream(reinterpret_cast<uint2*>(qrow + c), make_uint2(codes[0], codes[NC - 1]));
+            } else {
+#pragma unroll
+                for (int u = 0; u < NC; ++u)
+                    if (c + u < a.chunks) st_stream(qrow + c + u, codes[u]);
             }
             if (c < a.chunks && (c & 1) == 0) bsc[c >> 1] = (uint8_t)sb;
         }

@@ -152,3 +152,17 @@ def test_nvfp4_dynamic_argument_errors(L):
     assert dyn(n=0, x=0, res=0, w=0, q=0, sc=0, gs=0, ro=0, wsp=0) == rq.OK
     if not torch.cuda.is_available():
         assert dyn() == rq.ERR_NO_DEVICE
+
+
+def test_process_wide_switches(L):
+    """The tuning switches only store settings: valid values are accepted,
+    others rejected, and the defaults are put back."""
+    assert L.rmsq_set_programmatic_launch(2) == rq.ERR_INVALID_ARG
+    assert L.rmsq_set_programmatic_launch(-1) == rq.ERR_INVALID_ARG
+    assert L.rmsq_set_programmatic_launch(0) == 0
+    assert L.rmsq_set_programmatic_launch(1) == 0
+    assert L.rmsq_set_pipeline_config(3, 0, 0, 0) == rq.ERR_INVALID_ARG
+    assert L.rmsq_set_pipeline_config(0, 9, 0, 0) == rq.ERR_INVALID_ARG
+    assert L.rmsq_set_pipeline_config(0, 0, 0, 3) == rq.ERR_INVALID_ARG
+    assert L.rmsq_set_pipeline_config(2, 2, 1, 2) == 0
+    assert L.rmsq_set_pipeline_config(0, 0, 0, 0) == 0

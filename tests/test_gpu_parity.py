@@ -262,3 +262,86 @@ def test_pipelined_ring_sizes_in_any_order():
     for H in (16, 8, 2048, 8, 16, 2048):
         wl = ri.make_workload(f"ring_{H}", 5, H, seed=35 + H)
         P.check(wl, "fp8_per_token", variants=("pipelined",), label=f"ring/{H}")
+
+
+@pytest.mark.parametrize("mode", ["fp8_per_token", "fp8_group128_row", "nvfp4"])
+@pytest.mark.parametrize("H", [4096, 12288])
+def test_sixteen_byte_aligned_buffers(mode, H):
+    """Buffers that start on 16 but not 32 bytes take the per-chunk loads and
+    stores instead of the paired 32-byte accesses; results stay bit-exact."""
+    n = 700
+    wl = ri.make_workload("align16", n, H, seed=51)
+    want = oracle.run_workload(wl, mode)
+    scale_in = want["scale_in"]
+    qcols = H // 2 if mode == "nvfp4" else H
+
+    def shifted(numel, dtype):
+        # 16 bytes past a 256-byte aligned allocation
+        per = 16 // torch.empty((), dtype=dtype).element_size()
+        return torch.zeros(numel + per, dtype=dtype, device="cuda")[per:]
+
+    for variant in P.VARIANTS:
+        x = shifted(n * H, torch.bfloat16).view(n, H)
+        x.copy_(P.dev_act(wl.x, wl.dtype))
+        r = shifted(n * H, torch.bfloat16).view(n, H)
+        r.copy_(P.dev_act(wl.residual, wl.dtype))
+        ro = shifted(n * H, torch.bfloat16).view(n, H)
+        q = shifted(n * qcols, torch.uint8).view(n, qcols)
+        assert x.data_ptr() % 32 == 16 and q.data_ptr() % 32 == 16
+        w = P.dev_act(wl.weight, wl.dtype)
+        s = torch.tensor([scale_in or 0.0], dtype=torch.float32, device="cuda")
+        q, sc, ro = rq.fused_add_rmsnorm_quant(x, r, w, wl.eps, mode, s, out_q=q, residual_out=ro,
+                                               variant=variant)
+        torch.cuda.synchronize()
+        assert rq.take_fault_flags() == 0
+        got = {"q": q.cpu().numpy(), "scales": sc.cpu().numpy(), "residual_out": P.host_bits(ro)}
+        P.compare(got, want, mode, f"16-byte aligned {variant}")
+
+
+@pytest.mark.parametrize("n", [40, 1300], ids=["direct", "pipelined"])
+@pytest.mark.parametrize("pdl", [True, False], ids=["pdl", "plain"])
+def test_chained_layers_in_place(n, pdl):
+    """Four back-to-back calls on one stream, as consecutive layers: each
+    reads the residual the previous one wrote (odd layers update it in
+    place), with no host synchronisation in between.  With programmatic dependent launch each
+    kernel must still see the previous one's writes; the oracle applies the
+    layers one after the other."""
+    H, layers = 2048, 4
+    wls = [ri.make_workload(f"chain{i}", n, H, res_sigma=2.0, seed=90 + i) for i in range(layers)]
+    mode = "fp8_per_token"
+    # oracle: residual carried from layer to layer
+    res_bits = wls[0].residual
+    want = []
+    for wl in wls:
+        out = oracle.run(wl.x, res_bits, wl.weight, eps=wl.eps, mode=mode, dtype=wl.dtype)
+        want.append(out)
+        res_bits = out["residual_out"]
+    rq.set_programmatic_launch(pdl)
+    try:
+        s = torch.cuda.Stream()
+        xs = [P.dev_act(wl.x, wl.dtype) for wl in wls]
+        ws = [P.dev_act(wl.weight, wl.dtype) for wl in wls]
+        # even layers write a fresh buffer, odd layers update it in place
+        bufs = [P.dev_act(wls[0].residual, wls[0].dtype)] + [torch.empty_like(xs[0]) for _ in range(layers // 2)]
+        torch.cuda.synchronize()
+        outs = []
+        r = bufs[0]
+        with torch.cuda.stream(s):
+            for i in range(layers):
+                ro = bufs[i // 2 + 1]
+                q, sc, _ = rq.fused_add_rmsnorm_quant(xs[i], r, ws[i], wls[i].eps, mode, residual_out=ro,
+                                                      stream=s)
+                outs.append((q, sc, ro if i % 2 == 1 else None))
+                r = ro
+        torch.cuda.synchronize()
+    finally:
+        rq.set_programmatic_launch(True)
+    assert rq.take_fault_flags() == 0
+    for i, (q, sc, ro) in enumerate(outs):
+        # an even layer's write-back is overwritten in place by the next layer
+        got = {"q": q.cpu().numpy(), "scales": sc.cpu().numpy(),
+               "residual_out": None if ro is None else P.host_bits(ro)}
+        w = dict(want[i])
+        if ro is None:
+            w["residual_out"] = None
+        P.compare(got, w, mode, f"layer {i}")
