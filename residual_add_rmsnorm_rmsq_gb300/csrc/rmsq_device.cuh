@@ -100,6 +100,20 @@ __device__ __forceinline__ void st_stream_pair(uint4* p, const uint32_t (&a)[4],
                  : "memory");
 }
 
+// Stores of data that is read again shortly (by a later phase of the same
+// operation): plain write-back, the line stays in L2 at normal priority.
+__device__ __forceinline__ void st_keep(uint4* p, uint4 v) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ void st_keep_pair(uint4* p, const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]),
+                    "r"(b[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
     asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
@@ -366,6 +380,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -167,8 +167,7 @@ inline int sm_count(cudaError_t* err) {
 // one when two do not fit the budget.
 inline int pipe_stages(int stage_bytes) { return 2 * stage_bytes <= kPipeSmemBudget ? 2 : 1; }
 
-template <class E>
-cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
+inline RowArgs make_row_args(const LaunchArgs& la) {
     RowArgs a;
     a.x = static_cast<const uint4*>(la.x);
     a.res = static_cast<const uint4*>(la.res);
@@ -182,11 +181,56 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     a.hidden = la.hidden;
     a.chunks = la.hidden / 8;
     a.inv_hidden_pow2 = (la.hidden & (la.hidden - 1)) == 0 ? 1.0f / (float)la.hidden : 0.0f;
-    const bool res = la.res != nullptr;
     auto on = [](const void* p, uintptr_t b) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % b == 0; };
     a.pair = RMSQ_PAIR_ACCESS && a.chunks % 2 == 0 && on(la.x, 32) && on(la.res, 32) &&
              on(la.res_out, 32) && on(la.q, 16);
+    return a;
+}
 
+// Launch shape of the pipelined kernel: chunks per thread J, rows per
+// iteration R, threads, ring stages and bytes.
+struct PipePlan {
+    int J, R, threads, stages, smem;
+};
+
+inline PipePlan pipe_plan(const RowArgs& a, bool res) {
+    const PipeTuning tune = get_pipe_tuning();
+    auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
+    PipePlan p;
+    p.J = a.chunks <= 1024 ? 2 : 4;
+    if ((tune.chunks_per_thread == 1 || tune.chunks_per_thread == 2 || tune.chunks_per_thread == 4) &&
+        threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
+        p.J = tune.chunks_per_thread;
+    p.threads = threads_for(p.J);
+    const int row_slot = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
+    p.R = (tune.rows_per_iter == 2 && p.J <= 2 && 2 * row_slot <= kPipeSmemBudget) ? 2 : 1;
+    const int stage_bytes = p.R * row_slot;
+    p.stages = pipe_stages(stage_bytes);
+    if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
+        p.stages = tune.stages;
+    p.smem = p.stages * stage_bytes;
+    return p;
+}
+
+// Persistent grid of `fn` for a plan: as many CTAs as fit on the SMs at once
+// (capped by the tuning), at most one per row.
+inline cudaError_t pipe_grid(const void* fn, const PipePlan& p, int n, int* grid) {
+    cudaError_t err = cudaSuccess;
+    const int sms = sm_count(&err);
+    if (err != cudaSuccess) return err;
+    int per_sm = pipe_blocks_per_sm(fn, p.threads, p.smem, &err);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    const PipeTuning tune = get_pipe_tuning();
+    if (tune.ctas_per_sm >= 1 && tune.ctas_per_sm < per_sm) per_sm = tune.ctas_per_sm;
+    *grid = n < per_sm * sms ? n : per_sm * sms;
+    return cudaSuccess;
+}
+
+template <class E>
+cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
+    RowArgs a = make_row_args(la);
+    const bool res = la.res != nullptr;
     cudaError_t err = cudaSuccess;
     const int sms = sm_count(&err);
     if (err != cudaSuccess) return err;
@@ -194,30 +238,15 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
                 (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
 
     if (pipe) {
-        const PipeTuning tune = get_pipe_tuning();
-        auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
-        int J = a.chunks <= 1024 ? 2 : 4;
-        if ((tune.chunks_per_thread == 1 || tune.chunks_per_thread == 2 || tune.chunks_per_thread == 4) &&
-            threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
-            J = tune.chunks_per_thread;
-        const int threads = threads_for(J);
-        const int row_slot = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
-        const int R = (tune.rows_per_iter == 2 && J <= 2 && 2 * row_slot <= kPipeSmemBudget) ? 2 : 1;
-        const int stage_bytes = R * row_slot;
-        int stages = pipe_stages(stage_bytes);
-        if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
-            stages = tune.stages;
-        const int smem = stages * stage_bytes;
-        const void* fn = pick_kernel<E>(la.mode, res, true, J, R);
+        const PipePlan p = pipe_plan(a, res);
+        const void* fn = pick_kernel<E>(la.mode, res, true, p.J, p.R);
         if (!fn) return cudaErrorInvalidValue;
-        int per_sm = pipe_blocks_per_sm(fn, threads, smem, &err);
+        int grid = 0;
+        err = pipe_grid(fn, p, a.n, &grid);
         if (err != cudaSuccess) return err;
-        if (per_sm < 1) return cudaErrorInvalidConfiguration;
-        if (tune.ctas_per_sm >= 1 && tune.ctas_per_sm < per_sm) per_sm = tune.ctas_per_sm;
-        const int grid = a.n < per_sm * sms ? a.n : per_sm * sms;
-        int st = stages;
+        int st = p.stages;
         void* params[] = {&a, &st};
-        return launch_kernel(fn, dim3(grid), dim3(threads), params, smem, stream);
+        return launch_kernel(fn, dim3(grid), dim3(p.threads), params, p.smem, stream);
     }
     const int J = a.chunks <= 1024 ? 1 : 2;
     const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
@@ -228,7 +257,9 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
 }
 
 // NVFP4 with a data-derived global scale: zero the workspace's amax word,
-// pass 1 (row kernel, mode kNormAmax), pass 2 (block quantisation).
+// pass 1 (row kernel, mode kNormAmax, in the requested variant), pass 2
+// (block quantisation).  Both are launched with programmatic dependent launch
+// when it is on, so pass 2's launch overlaps the end of pass 1.
 template <class E>
 cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* out_gs,
                                  cudaStream_t stream) {
@@ -246,13 +277,15 @@ cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* o
     if (e != cudaSuccess) return e;
     int64_t grid = (blocks_total + 256 * kDynUnroll - 1) / (256 * kDynUnroll);
     if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
+    auto at32 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 32 == 0; };
     const uint4* h = static_cast<const uint4*>(la.res ? la.res_out : la.x);
     const uint4* w = static_cast<const uint4*>(la.w);
+    int pair = (RMSQ_PAIR_ACCESS && at32(h) && at32(w)) ? 1 : 0;
     const float* ws = static_cast<const float*>(workspace);
     uint2* q = static_cast<uint2*>(la.q);
     uint8_t* bs = static_cast<uint8_t*>(la.scales);
     int n = la.n, hidden = la.hidden;
-    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden};
+    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden, &pair};
     return launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_quant_kernel<E>), dim3((unsigned)grid),
                          dim3(256), params, 0, stream);
 }

@@ -71,8 +71,11 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                          &full[s], policy);
         }
     };
+    // The first pass of the data-derived NVFP4 scale is followed by a pass
+    // that reads h again: without a residual h is x, kept in L2.
+    constexpr bool KEEP = MODE == kNormAmax;
     if (tid == 0) {
-        policy = l2_policy_evict_first();
+        policy = (KEEP && !RES) ? l2_policy_evict_normal() : l2_policy_evict_first();
         for (int k = 0; k < stages; ++k) {
             if (blockIdx.x + k * R * G >= a.n) break;
             issue(k, k);
@@ -117,8 +120,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                         if constexpr (RES) rv[j] = sx[a.chunks + c0 + j];
                     }
                 }
-                acc[r] = combine_chunks<E, RES, J>(xv, rv, hw[r], a.res_out + (int64_t)row * a.chunks, c0,
-                                                   a.chunks, a.pair);
+                acc[r] = combine_chunks<E, RES, J, KEEP>(xv, rv, hw[r], a.res_out + (int64_t)row * a.chunks,
+                                                         c0, a.chunks, a.pair);
             }
         }
 #pragma unroll

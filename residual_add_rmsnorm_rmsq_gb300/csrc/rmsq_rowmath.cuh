@@ -69,8 +69,9 @@ template <int MODE> struct ModeTraits {
 // residual write-back, and the thread's partial of the sum-of-squares tree.
 // Chunks at or beyond `chunks` hold zeros and are not stored.
 // With `pair` (J >= 2, chunks even) each chunk pair of the write-back is one
-// 32-byte store.
-template <class E, bool RES, int J>
+// 32-byte store.  KEEP: the write-back is read again by a later phase, so it
+// is stored at normal L2 priority instead of streamed.
+template <class E, bool RES, int J, bool KEEP = false>
 __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint4 (&rv)[J],
                                                 uint32_t (&hw)[J][4], uint4* res_out_row,
                                                 int c0, int chunks, bool pair) {
@@ -88,12 +89,18 @@ __device__ __forceinline__ float combine_chunks(const uint4 (&xv)[J], const uint
         if (J >= 2 && pair) {
 #pragma unroll
             for (int j = 0; j + 1 < J; j += 2)
-                if (c0 + j < chunks) st_stream_pair(res_out_row + c0 + j, hw[j], hw[j + 1]);
+                if (c0 + j < chunks) {
+                    if constexpr (KEEP) st_keep_pair(res_out_row + c0 + j, hw[j], hw[j + 1]);
+                    else st_stream_pair(res_out_row + c0 + j, hw[j], hw[j + 1]);
+                }
         } else {
 #pragma unroll
             for (int j = 0; j < J; ++j)
-                if (c0 + j < chunks)
-                    st_stream(res_out_row + c0 + j, make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]));
+                if (c0 + j < chunks) {
+                    const uint4 v = make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]);
+                    if constexpr (KEEP) st_keep(res_out_row + c0 + j, v);
+                    else st_stream(res_out_row + c0 + j, v);
+                }
         }
     }
     float h[J][8];
@@ -327,7 +334,13 @@ __device__ __forceinline__ void flush_amax(const RowArgs& a, float run_max, floa
     if (tid == 0) {
         float t = 0.0f;
         for (int w = 0; w < nwarps; ++w) t = fmaxf(t, s_max[w]);
-        if (t > 0.0f) atomicMax(static_cast<unsigned int*>(a.scales), __float_as_uint(t));
+        // The word only grows during the launch: skip the atomic when it
+        // already holds t or more (most CTAs, once a few have merged), which
+        // keeps the one address from serialising every CTA's update.
+        unsigned int* word = static_cast<unsigned int*>(a.scales);
+        unsigned int cur;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(word) : "memory");
+        if (t > 0.0f && __float_as_uint(t) > cur) atomicMax(word, __float_as_uint(t));
     }
 }
 

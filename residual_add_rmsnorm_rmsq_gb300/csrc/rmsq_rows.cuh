@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(1024) rows_kernel(const RowArgs a) {
     if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the barrier below
 
     uint32_t h[J][4];
-    float acc = combine_chunks<E, RES, J>(xv, rv, h, a.res_out + base, c0, a.chunks, a.pair);
+    float acc = combine_chunks<E, RES, J, MODE == kNormAmax>(xv, rv, h, a.res_out + base, c0, a.chunks, a.pair);
     acc = warp_tree_sum(acc);
     if (lane == 0) s_sum[warp] = acc;
     __syncthreads();

@@ -80,3 +80,61 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(rq.RmsqError) as ei:
         rq.fused_add_rmsnorm_nvfp4_dynamic(x, None, w, 1e-6, workspace=ws)
     assert ei.value.status == rq.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("shape", [(1, 0), (2, 1), (0, 1)], ids=["one-cta-per-sm", "two-ctas-one-stage",
+                                                                 "one-stage"])
+def test_pipelined_first_pass_with_small_grids(shape):
+    """Pass 1 on the pipelined kernel with fewer resident CTAs or ring stages
+    than usual (many rows per CTA)."""
+    cps, stages = shape
+    wl = ri.qwen_nvfp4(4096)
+    want = oracle.run_nvfp4_dynamic(wl.x, wl.residual, wl.weight, eps=wl.eps, dtype=wl.dtype, nthreads=8)
+    rq.set_pipeline_config(0, stages, cps, 0)
+    try:
+        got = run_dyn(wl, "pipelined")
+    finally:
+        rq.set_pipeline_config(0, 0, 0, 0)
+    assert got["global_scale"].view(np.uint32)[0] == want["global_scale"].view(np.uint32)[0]
+    P.compare(got, want, "nvfp4", f"small grid {shape}")
+
+
+@pytest.mark.parametrize("variant", ["auto", "direct"])
+def test_graph_replay_resets_the_workspace(variant):
+    """Captured once into a CUDA graph and replayed on new inputs: each replay
+    zeroes the amax word again."""
+    wls = [ri.make_workload(f"graph{i}", 900, 2048, res_sigma=1.0 + i, seed=300 + i) for i in range(3)]
+    x = P.dev_act(wls[0].x, wls[0].dtype)
+    r = P.dev_act(wls[0].residual, wls[0].dtype)
+    w = P.dev_act(wls[0].weight, wls[0].dtype)
+    n, H = x.shape
+    q = torch.empty(n, H // 2, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(n, H // 16, dtype=torch.uint8, device="cuda")
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    ro = torch.empty_like(r)
+    ws = torch.empty(rq.nvfp4_dynamic_workspace_bytes(n), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def call():
+        rq.fused_add_rmsnorm_nvfp4_dynamic(x, r, w, wls[0].eps, out_q=q, out_scales=sc, out_global_scale=gs,
+                                           residual_out=ro, workspace=ws, stream=s, variant=variant)
+
+    with torch.cuda.stream(s):
+        call()   # first call outside capture (library set-up)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for wl in wls:
+        x.copy_(P.dev_act(wl.x, wl.dtype))
+        r.copy_(P.dev_act(wl.residual, wl.dtype))
+        w.copy_(P.dev_act(wl.weight, wl.dtype))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert rq.take_fault_flags() == 0
+        want = oracle.run_nvfp4_dynamic(wl.x, wl.residual, wl.weight, eps=wl.eps, dtype=wl.dtype, nthreads=8)
+        got = {"q": q.cpu().numpy(), "scales": sc.cpu().numpy(), "global_scale": gs.cpu().numpy(),
+               "residual_out": P.host_bits(ro)}
+        assert got["global_scale"].view(np.uint32)[0] == want["global_scale"].view(np.uint32)[0]
+        P.compare(got, want, "nvfp4", f"graph replay {wl.name}/{variant}")
