@@ -332,7 +332,7 @@ __device__ __forceinline__ float warp_max_nonneg(float v) {
 // over warp sums, zero-padded.
 template <int N>
 __device__ __forceinline__ float smem_tree_sum(const float* p) {
-    static_assert(N == 16 || N == 32, "16 or 32 slots");
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 slots");
     float v[N];
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) {
@@ -344,6 +344,34 @@ __device__ __forceinline__ float smem_tree_sum(const float* p) {
 #pragma unroll
         for (int k = 0; k < len / 2; ++k) v[k] = __fadd_rn(v[2 * k], v[2 * k + 1]);
     return v[0];
+}
+
+// The same tree over the slots of `nwarps` warps (slots up to the next of
+// 8 / 16 / MAX hold zeros): a zero-padded subtree adds only exact zeros, so
+// summing the smallest power-of-two prefix that holds every warp's slot gives
+// the full tree's value.
+template <int MAX>
+__device__ __forceinline__ float warp_slots_tree_sum(const float* p, int nwarps) {
+    if (nwarps <= 8) return smem_tree_sum<8>(p);
+    if constexpr (MAX >= 16) {
+        if (MAX == 16 || nwarps <= 16) return smem_tree_sum<16>(p);
+    }
+    if constexpr (MAX >= 32) return smem_tree_sum<32>(p);
+    return smem_tree_sum<MAX>(p);
+}
+
+// max(m, |a|, |b|) in one instruction; m >= 0.
+__device__ __forceinline__ float max_abs3(float m, float a, float b) {
+    float r;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(a), "f"(b));
+    return r;
+}
+
+// max(m, |v_0|, ..., |v_7|), m >= 0.
+__device__ __forceinline__ float max_abs8(float m, const float (&v)[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) m = max_abs3(m, v[k], v[k + 1]);
+    return m;
 }
 
 template <int LANES>

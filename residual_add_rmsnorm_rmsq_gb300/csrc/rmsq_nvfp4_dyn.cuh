@@ -28,7 +28,7 @@ __device__ __forceinline__ uint32_t nvfp4_block16(const float (&y)[16], float gs
                                                   uint2& codes) {
     float m = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(y[k]));
+    for (int k = 0; k < 16; k += 2) m = max_abs3(m, y[k], y[k + 1]);
     const uint32_t sb = e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), gs), 0.0f) & 0xffu;
     const float r = rtab[sb];      // gs / decode(sb), 0 for a zero block scale
     float lo[8], hi[8];

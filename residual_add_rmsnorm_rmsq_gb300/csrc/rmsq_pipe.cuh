@@ -82,10 +82,14 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         }
     }
 
-    uint4 wv[J];
+    float wv[J][8];
+    {
+        uint4 wraw[J];
 #pragma unroll
-    for (int j = 0; j < J; ++j)
-        wv[j] = (c0 + j < a.chunks) ? ld_weight(a.w + c0 + j) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < J; ++j)
+            wraw[j] = (c0 + j < a.chunks) ? ld_weight(a.w + c0 + j) : make_uint4(0u, 0u, 0u, 0u);
+        widen_weights<E, J>(wraw, wv);
+    }
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
     __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
     if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the first barrier
@@ -138,7 +142,8 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
 
         float inv[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) inv[r] = inv_rms(smem_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1][r]), a);
+        for (int r = 0; r < R; ++r)
+            inv[r] = inv_rms(warp_slots_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1][r], nwarps), a);
 
         if constexpr (MODE == kFp8PerToken && R > 1) {
             // The rows' amax reductions share one barrier.

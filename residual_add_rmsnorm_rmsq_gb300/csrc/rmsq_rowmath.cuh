@@ -133,21 +133,28 @@ __device__ __forceinline__ float inv_rms(float total, const RowArgs& a) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, a.eps)));
 }
 
-// y = (h * inv) * w in fp32 for the thread's chunks, in packed pairs: element
-// k of chunks j and j + 1 (J >= 2), elements k and k + 2 of the chunk (J == 1).
+// The weight chunks widened to fp32 (once per kernel in the pipelined
+// kernel, where every row of the CTA uses them).
 template <class E, int J>
-__device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const uint4 (&wv)[J], float inv,
-                                          float (&y)[J][8]) {
-    float h[J][8], w[J][8];
+__device__ __forceinline__ void widen_weights(const uint4 (&wv)[J], float (&w)[J][8]) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const uint32_t ws[4] = {wv[j].x, wv[j].y, wv[j].z, wv[j].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            h[j][2 * k] = E::lo(hw[j][k]); h[j][2 * k + 1] = E::hi(hw[j][k]);
-            w[j][2 * k] = E::lo(ws[k]); w[j][2 * k + 1] = E::hi(ws[k]);
-        }
+        for (int k = 0; k < 4; ++k) { w[j][2 * k] = E::lo(ws[k]); w[j][2 * k + 1] = E::hi(ws[k]); }
     }
+}
+
+// y = (h * inv) * w in fp32 for the thread's chunks, in packed pairs: element
+// k of chunks j and j + 1 (J >= 2), elements k and k + 2 of the chunk (J == 1).
+template <class E, int J>
+__device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const float (&w)[J][8], float inv,
+                                          float (&y)[J][8]) {
+    float h[J][8];
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { h[j][2 * k] = E::lo(hw[j][k]); h[j][2 * k + 1] = E::hi(hw[j][k]); }
     const float2 iv = make_float2(inv, inv);
     if constexpr (J == 1) {
 #pragma unroll
@@ -201,8 +208,7 @@ __device__ __forceinline__ void per_token_warp_amax(const float (&y)[J][8], floa
     float m = 0.0f;
 #pragma unroll
     for (int j = 0; j < J; ++j)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+        m = max_abs8(m, y[j]);
     m = warp_max_nonneg(m);
     if (lane == 0) s_max[warp] = m;
 }
@@ -226,7 +232,7 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
 // __syncthreads; every thread of the CTA must call this.
 template <class E, int MODE, int J>
 __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
-                                             const uint4 (&wv)[J], float inv, float sin,
+                                             const float (&wv)[J][8], float inv, float sin,
                                              const float* rtab, float* s_max, int tid, int nwarps,
                                              float& run_max) {
     const int lane = tid & 31, warp = tid >> 5;
@@ -241,8 +247,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
     } else if constexpr (MODE == kNormAmax) {
 #pragma unroll
         for (int j = 0; j < J; ++j)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) run_max = fmaxf(run_max, fabsf(y[j][k]));
+            run_max = max_abs8(run_max, y[j]);
         if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
     } else if constexpr (MODE == kNvfp4) {
         // 16-element blocks = chunk pairs (2m, 2m+1): a lane pair when J == 1,
@@ -253,13 +258,11 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
 #pragma unroll
         for (int j = 0; j < J; j += (J == 1 ? 1 : 2)) {
             float m = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+            m = max_abs8(m, y[j]);
             if constexpr (J == 1) {
                 m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
             } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j + 1][k]));
+                m = max_abs8(m, y[j + 1]);
             }
             const uint32_t sb = e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), gs), 0.0f) & 0xffu;
             const float r = rtab[sb];      // gs / decode(sb), 0 for a zero block scale
@@ -304,9 +307,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
             constexpr int LANES = G / 8 / J;   // threads sharing one group
             float m = 0.0f;
 #pragma unroll
-            for (int j = 0; j < J; ++j)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(y[j][k]));
+            for (int j = 0; j < J; ++j) m = max_abs8(m, y[j]);
             m = lanes_max<LANES>(m);
             s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
             if (c0 < a.chunks && (c0 % (G / 8)) == 0) {

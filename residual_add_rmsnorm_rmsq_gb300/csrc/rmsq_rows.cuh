@@ -50,10 +50,12 @@ __global__ void __launch_bounds__(1024) rows_kernel(const RowArgs a) {
     acc = warp_tree_sum(acc);
     if (lane == 0) s_sum[warp] = acc;
     __syncthreads();
-    const float total = smem_tree_sum<32>(s_sum);
+    const float total = warp_slots_tree_sum<32>(s_sum, nwarps);
     const float inv = inv_rms(total, a);
     float run_max = 0.0f;
-    quantize_row<E, MODE, J>(a, row, h, wv, inv, sin, s_rtab, s_max, tid, nwarps, run_max);
+    float wf[J][8];
+    widen_weights<E, J>(wv, wf);
+    quantize_row<E, MODE, J>(a, row, h, wf, inv, sin, s_rtab, s_max, tid, nwarps, run_max);
     if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max, tid, nwarps);
 }
 
