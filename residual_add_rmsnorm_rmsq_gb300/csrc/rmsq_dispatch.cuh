@@ -27,11 +27,18 @@ namespace rmsq {
 static __device__ unsigned int g_pipe_fault;
 
 // Compile-time tuning (results never depend on these): the minimum number of
-// resident CTAs the pipelined kernel is compiled for when a thread owns one
-// or two chunks (the register budget follows from it), and whether the
-// largest shared-memory carve-out is requested.
+// resident 512-thread CTAs the pipelined kernel is compiled for when a thread
+// owns one or two chunks, with and without a residual (the register budget
+// follows from it: 1 leaves up to 128 registers, 2 caps them at 64), and
+// whether the largest shared-memory carve-out is requested.  Without a
+// residual the kernel is bound by its instruction stream rather than by HBM,
+// and the extra resident CTAs of the tighter budget pay (measured on GB300);
+// with a residual they do not.
 #ifndef RMSQ_PIPE_MIN_BLOCKS
 #define RMSQ_PIPE_MIN_BLOCKS 1
+#endif
+#ifndef RMSQ_PIPE_MIN_BLOCKS_NORES
+#define RMSQ_PIPE_MIN_BLOCKS_NORES 2
 #endif
 #ifndef RMSQ_MAX_SMEM_CARVEOUT
 #define RMSQ_MAX_SMEM_CARVEOUT 1
@@ -42,7 +49,8 @@ static __device__ unsigned int g_pipe_fault;
 #endif
 
 template <class E, int MODE, bool RES, int J, int R>
-__global__ void __launch_bounds__(kPipeMaxThreads, (J == 4 ? 1 : RMSQ_PIPE_MIN_BLOCKS))
+__global__ void __launch_bounds__(kPipeMaxThreads,
+                                  (J == 4 ? 1 : RES ? RMSQ_PIPE_MIN_BLOCKS : RMSQ_PIPE_MIN_BLOCKS_NORES))
 pipe_entry(const RowArgs a, const int stages) {
     pipe_body<E, MODE, RES, J, R>(a, stages, &g_pipe_fault);
 }
