@@ -264,6 +264,50 @@ class Buffers:
                 variant=VARIANT)
 
 
+def act_algorithmic_bytes(mode: str, n: int, d: int, es: int) -> int:
+    """Bytes the SiLU+Mul + quantisation op must move: gate_up in, codes and
+    scales out, scale_in."""
+    per_tok = 2 * d * es + (d // 2 if mode == "nvfp4" else d)
+    if mode == "fp8_per_token":
+        per_tok += 4
+    elif mode.startswith("fp8_group"):
+        per_tok += 4 * d // (128 if "128" in mode else 64)
+    elif mode == "nvfp4":
+        per_tok += d // 16
+    return n * per_tok + (4 if mode in ("fp8_static", "nvfp4") else 0)
+
+
+class ActBuffers:
+    """Rotating device buffer sets for one SiLU+Mul + quantisation workload."""
+
+    def __init__(self, torch, rq, wl, mode, min_total_bytes):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        n, d = wl.n_tokens, wl.d
+        self.rq, self.mode = rq, mode
+        self.bytes = act_algorithmic_bytes(mode, n, d, 2)
+        self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        g0 = torch.from_numpy(wl.gate_up.view(np.int16)).view(tdt).cuda()
+        if mode == "fp8_static":
+            self.scale_in = torch.tensor([wl.static_scale or 0.05], dtype=torch.float32, device="cuda")
+        elif mode == "nvfp4":
+            # gs = 2688 / amax over the batch, from the library's per-token scales
+            # (amax = 448 * scale), computed once outside the timed region
+            _, sc = rq.silu_mul_quant(g0, "fp8_per_token")
+            self.scale_in = (2688.0 / (sc.max() * 448.0)).reshape(1).float()
+        else:
+            self.scale_in = None
+        self.gu, self.q, self.sc = [], [], []
+        for i in range(self.sets):
+            self.gu.append(g0 if i == 0 else g0.clone())
+            self.q.append(torch.empty(n, d // 2 if mode == "nvfp4" else d, dtype=torch.uint8, device="cuda"))
+            self.sc.append(rq.scales_like(mode, n, d, "cuda"))
+        torch.cuda.synchronize()
+
+    def launch(self, k, stream):
+        self.rq.silu_mul_quant(self.gu[k], self.mode, self.scale_in, out_q=self.q[k], out_scales=self.sc[k],
+                               stream=stream)
+
+
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
     """Mean device time per launch (ms) over exactly `steps` launches, CUDA
     events on `stream`.
@@ -514,7 +558,9 @@ def decode_sweep(torch, rq, stream, args):
 
 
 def sweep(torch, rq, stream, peak, args):
-    """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of peak)."""
+    """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of
+    peak), and SiLU+Mul + quantisation on a Llama-8B-shaped MLP activation
+    (4096 tokens, d = 14336)."""
     import rmsq_inputs as ri
     out = {}
     groups = [
@@ -525,6 +571,17 @@ def sweep(torch, rq, stream, peak, args):
         (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096", "qwen_nvfp4_dynamic_4096"]),
         (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384", "qwen_nvfp4_dynamic_16384"]),
     ]
+    act = ri.llama_mlp(4096)
+    for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):
+        name = f"llama_mlp_silu_mul_{mode}"
+        bufs = ActBuffers(torch, rq, act, mode, 4 * L2_BYTES + 1)
+        ms = time_launches(torch, rq, act, mode, bufs, args.sweep_steps, 5, stream)
+        gbs = bufs.bytes / (ms / 1e3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "tokens_per_s": round(act.n_tokens / (ms / 1e3), 1), "bytes": bufs.bytes}
+        del bufs
+        torch.cuda.empty_cache()
+    del act
     for make, names in groups:
         wl = make()
         for name in names:

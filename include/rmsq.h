@@ -216,6 +216,38 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc(const void *x, const void *resi
                                                  int64_t hidden, int dtype, void *stream,
                                                  int variant);
 
+/* Largest d (activation width) of rmsq_silu_mul_quant. */
+#define RMSQ_ACT_MAX_D 32768
+
+/*
+ * rmsq_silu_mul_quant — SiLU+Mul + activation quantisation in one kernel (vLLM
+ * docs "Fusion torch.compile passes", section "SiLU+Mul + Quantization
+ * (fuse_act_quant)": silu_and_mul on the gated up-projection followed by the
+ * quantisation, without the full-precision activation tensor in between).
+ * Per row t: a_i = silu(g_i) * u_i in fp32, silu(g) = g / (1 + e^-g) with
+ * g_i = gate_up[t, i] and u_i = gate_up[t, d + i]; then exactly the
+ * quantisation step of rmsq_fused_add_rmsnorm_quant with a in place of y
+ * (every quant_mode; scales and codes laid out the same way with hidden = d).
+ * e^x follows W. J. Cody and W. Waite's argument reduction with a degree-7
+ * Taylor polynomial, each step a correctly rounded binary32 operation (within
+ * 1.2 ulp of e^x over the normal range); the division and products are
+ * correctly rounded, so results are reproducible bit for bit.
+ *  gate_up     device, [n_tokens, 2 d] bf16/fp16, row-major, 16-byte aligned.
+ *  quant_mode  an rmsq_quant_mode.
+ *  scale_in    device fp32: FP8 static scale or NVFP4 global scale (else
+ *              ignored, may be NULL).
+ *  out_q       device: [n, d] E4M3 bytes, or [n, d/2] E2M1 pairs for NVFP4.
+ *  out_scales  device: as for rmsq_fused_add_rmsnorm_quant with hidden = d.
+ *  n_tokens    >= 0 (0 returns RMSQ_OK without a launch);
+ *  d           > 0, a multiple of 8 (16 for NVFP4, the group for group
+ *              modes), at most RMSQ_ACT_MAX_D (else
+ *              RMSQ_ERR_UNSUPPORTED_SHAPE).
+ * Errors as for rmsq_fused_add_rmsnorm_quant (no output may overlap an input
+ * or another output).  Asynchronous on `stream`; the caller owns all memory.
+ */
+int rmsq_silu_mul_quant(const void *gate_up, int quant_mode, const float *scale_in, void *out_q,
+                        void *out_scales, int64_t n_tokens, int64_t d, int dtype, void *stream);
+
 /*
  * rmsq_set_pipeline_config — process-wide tuning of the PIPELINED variant:
  * chunks_per_thread (16-byte chunks of a row per thread: 1, 2 or 4), stages
@@ -268,6 +300,17 @@ int rmsq_query_sizes(int quant_mode, int64_t n_tokens, int64_t hidden, size_t *q
  * in: device fp32[n]; out: device u8[n]; no alignment requirement.
  */
 int rmsq_debug_convert(int kind, const float *in, uint8_t *out, int64_t n, void *stream);
+
+/*
+ * rmsq_debug_activation — the library's own e^x and SiLU steps (those of
+ * rmsq_silu_mul_quant) on device arrays, so that tests can compare them with
+ * a reference element by element.  kind 0: out[i] = e^in[i]; kind 1:
+ * out[i] = silu(in[i]); kind 2: out[i] = silu(in[i]) * in2[i] (in2 is
+ * ignored otherwise and may be NULL).  Device fp32 arrays of n elements,
+ * 4-byte aligned; out must not overlap the inputs.
+ */
+int rmsq_debug_activation(int kind, const float *in, const float *in2, float *out, int64_t n,
+                          void *stream);
 
 /* Text for an rmsq_status (static storage, never NULL). */
 const char *rmsq_status_string(int status);

@@ -102,6 +102,14 @@ def _configure(L):
     L.oracle_fused_add_rmsnorm_nvfp4_dynamic.argtypes = [
         vp, vp, vp, f32, vp, vp, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int]
     L.oracle_fused_add_rmsnorm_nvfp4_dynamic.restype = ctypes.c_int
+    L.oracle_silu_mul_quant.argtypes = [vp, ctypes.c_int, f32, vp, vp, vp, i64, i64, ctypes.c_int,
+                                        ctypes.c_int]
+    L.oracle_silu_mul_quant.restype = ctypes.c_int
+    L.oracle_expf.argtypes, L.oracle_expf.restype = [f32], f32
+    L.oracle_silu.argtypes, L.oracle_silu.restype = [f32], f32
+    for name in ("oracle_expf_array", "oracle_silu_array"):
+        getattr(L, name).argtypes = [vp, vp, i64]
+        getattr(L, name).restype = None
     return L
 
 
@@ -217,6 +225,58 @@ def run_nvfp4_dynamic(x, residual, weight, *, eps: float, dtype: str = "bf16",
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return {"q": q, "scales": sc, "residual_out": ro, "global_scale": gs}
+
+
+def expf(v) -> np.ndarray:
+    """The oracle's e^x (Cody-Waite reduction, degree-7 Taylor polynomial) elementwise."""
+    v = _f32(v)
+    out = np.empty(v.shape, np.float32)
+    lib().oracle_expf_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def silu(v) -> np.ndarray:
+    """silu(g) = g / (1 + e^-g) elementwise, in the oracle's binary32 steps."""
+    v = _f32(v)
+    out = np.empty(v.shape, np.float32)
+    lib().oracle_silu_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def run_silu_mul(gate_up, *, mode: str, scale_in: float = 0.0, dtype: str = "bf16",
+                 want_y: bool = False, nthreads: int = 1) -> dict:
+    """SiLU+Mul + quantisation on host bit patterns: gate_up uint16 [n, 2d]
+    (gate in the first d columns, up in the next d).  Returns ``q``,
+    ``scales`` and, when ``want_y``, the fp32 activation ``y`` [n, d]."""
+    gu = np.ascontiguousarray(gate_up, np.uint16)
+    n, d2 = gu.shape
+    assert d2 % 2 == 0
+    d = d2 // 2
+    q = np.zeros((n, d // 2) if mode == "nvfp4" else (n, d), np.uint8)
+    ss = scale_shape(mode, n, d)
+    scales = None if ss is None else np.zeros(ss[0], ss[1])
+    y = np.zeros((n, d), np.float32) if want_y else None
+    rc = lib().oracle_silu_mul_quant(_ptr(gu), MODES[mode], ctypes.c_float(scale_in), _ptr(q), _ptr(scales),
+                                     _ptr(y), n, d, DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": scales, "residual_out": None, "y": y}
+
+
+def run_silu_mul_workload(wl, mode: str, *, scale_in: float | None = None, want_y: bool = False,
+                          nthreads: int = 1) -> dict:
+    """Run a SiLU+Mul workload (``rmsq_inputs.ActWorkload``).  For NVFP4
+    without an explicit scale_in, gs = 2688 / amax(all activations) from a
+    first pass, as for the norm op."""
+    if mode == "fp8_static" and scale_in is None:
+        scale_in = wl.static_scale
+    if mode == "nvfp4" and scale_in is None:
+        pre = run_silu_mul(wl.gate_up, mode="fp8_per_token", dtype=wl.dtype, want_y=True, nthreads=nthreads)
+        scale_in = nvfp4_global_scale(float(np.max(np.abs(pre["y"]))))
+    r = run_silu_mul(wl.gate_up, mode=mode, scale_in=scale_in or 0.0, dtype=wl.dtype, want_y=want_y,
+                     nthreads=nthreads)
+    r["scale_in"] = scale_in
+    return r
 
 
 def nvfp4_global_scale(y_amax: float) -> float:

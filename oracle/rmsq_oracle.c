@@ -38,6 +38,15 @@
  *  R7 E2M1 nibble order: element 2j in the low nibble of byte j.
  *  R8 column-major group scales use stride n_tokens.
  *  R14 dynamic NVFP4 global scale: gs = 1 when amax over the batch is 0.
+ *  R15 SiLU+Mul (vLLM docs, same page, section "SiLU+Mul + Quantization
+ *      (fuse_act_quant)": silu_and_mul on the gated up-projection, then the
+ *      quantisation, no full-precision activation tensor in between): each
+ *      row of the input holds the gate g in its first d elements and the up
+ *      projection u in the next d; a = silu(g) * u with
+ *      silu(g) = g / (1 + e^-g), kept in fp32 like y; then the same
+ *      quantisation as the norm op.
+ *  R16 e^x is oracle_expf below (the pages do not fix an exp routine; the GPU
+ *      evaluates the same steps).
  *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
  */
 #include <math.h>
@@ -173,6 +182,54 @@ float oracle_e2m1_decode(uint8_t c)
 }
 
 /* ------------------------------------------------------------------------ */
+/* e^x (reading R16).                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* W. J. Cody and W. Waite, "Software Manual for the Elementary Functions"
+ * (1980), exponential: write x = n ln2 + r with n the integer nearest to
+ * x log2(e), so that |r| <= ln2 / 2 (about 0.347); ln2 is split into a high
+ * part with 15 significant bits (n times it is exact for |n| < 512) and the
+ * rest, and r = (x - n ln2_hi) - n ln2_lo is formed with two fused
+ * multiply-adds; e^r is the Taylor polynomial sum r^k / k!, k = 0..7, in
+ * Horner form with one fused multiply-add per step (truncation error below
+ * r^8 / 8! < 2^-27 relative); e^x = e^r 2^n, the scaling split in two steps
+ * where 2^n alone is not a normal binary32.  Every step is one binary32
+ * operation (fmaf: one rounding of the exact a * b + c), rounded to nearest
+ * even, in the order written. */
+static float pow2i(int k) { return bits_to_float((uint32_t)(k + 127) << 23); }   /* -126 <= k <= 127 */
+
+float oracle_expf(float x)
+{
+    if (x != x) return x;
+    if (x > 89.0f) return INFINITY;      /* e^89 > FLT_MAX */
+    if (x < -104.0f) return 0.0f;        /* e^-104 < half the smallest subnormal */
+    const float log2e = 1.44269502162933349609375f;         /* RN(log2 e) */
+    const float ln2_hi = 0.693145751953125f;               /* 0x3f317200 */
+    const float ln2_lo = 1.428606765330187045e-06f;        /* RN(ln2 - ln2_hi) */
+    const float n = rintf(x * log2e);
+    const float r = fmaf(-n, ln2_lo, fmaf(-n, ln2_hi, x));
+    /* 1/k! rounded to binary32, k = 7 .. 0 */
+    float p = 1.98412701e-4f;                               /* 1/5040 */
+    p = fmaf(p, r, 1.38888892e-3f);                         /* 1/720 */
+    p = fmaf(p, r, 8.33333377e-3f);                         /* 1/120 */
+    p = fmaf(p, r, 4.16666679e-2f);                         /* 1/24 */
+    p = fmaf(p, r, 1.66666672e-1f);                         /* 1/6 */
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    const int k = (int)n;
+    if (k > 127) return (p * pow2i(127)) * pow2i(k - 127);
+    if (k < -126) return (p * pow2i(k + 64)) * pow2i(-64);
+    return p * pow2i(k);
+}
+
+/* silu(g) = g / (1 + e^-g) (reading R15). */
+float oracle_silu(float g)
+{
+    return g / (1.0f + oracle_expf(-g));
+}
+
+/* ------------------------------------------------------------------------ */
 /* Canonical pairwise sum (reading R3).                                     */
 /* ------------------------------------------------------------------------ */
 
@@ -215,6 +272,7 @@ typedef struct {
     float *y_out;            /* optional fp32 copy of y [n, H] for diagnostics */
     int64_t n, H;
     int dtype;
+    int silu_mul;            /* 1: the SiLU+Mul op, x = [n, 2H] gate | up (R15) */
 } OracleArgs;
 
 typedef struct {
@@ -237,6 +295,53 @@ static int group_size(int mode)
     case OR_FP8_G128_ROW: case OR_FP8_G128_COL: return 128;
     case OR_FP8_G64_ROW: case OR_FP8_G64_COL: return 64;
     default: return 0;
+    }
+}
+
+/* Step 5 of the op: quantisation of the fp32 row y (R4-R8). */
+static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
+{
+    const int64_t H = a->H;
+    uint8_t *q = a->out_q;
+    if (a->mode == OR_FP8_STATIC) {
+        float sc = a->scale_in;
+        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(y[i] / sc);
+    } else if (a->mode == OR_FP8_PER_TOKEN) {
+        float amax = 0.0f;
+        for (int64_t i = 0; i < H; ++i) amax = fmaxf(amax, fabsf(y[i]));
+        float sc = fmaxf(amax / 448.0f, 1e-12f);
+        ((float *)a->out_scales)[t] = sc;
+        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(y[i] / sc);
+    } else if (a->mode == OR_NVFP4) {
+        float gs = a->scale_in;
+        uint8_t *bs = (uint8_t *)a->out_scales;
+        for (int64_t b = 0; b < H / 16; ++b) {
+            const float *yb = y + 16 * b;
+            float amax = 0.0f;
+            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(yb[k]));
+            uint8_t sb = oracle_e4m3_encode((amax / 6.0f) * gs);
+            bs[t * (H / 16) + b] = sb;
+            float d = oracle_e4m3_decode(sb);
+            float r = (d == 0.0f) ? 0.0f : gs / d;
+            for (int k = 0; k < 16; k += 2) {
+                uint8_t lo = oracle_e2m1_encode(yb[k] * r);
+                uint8_t hi = oracle_e2m1_encode(yb[k + 1] * r);
+                q[t * (H / 2) + 8 * b + k / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
+    } else {
+        int G = group_size(a->mode);
+        int col = (a->mode == OR_FP8_G128_COL || a->mode == OR_FP8_G64_COL);
+        float *sc_out = (float *)a->out_scales;
+        for (int64_t g = 0; g < H / G; ++g) {
+            const float *yg = y + G * g;
+            float amax = 0.0f;
+            for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));
+            float sc = fmaxf(amax / 448.0f, 1e-12f);
+            if (col) sc_out[g * a->n + t] = sc;
+            else sc_out[t * (H / G) + g] = sc;
+            for (int k = 0; k < G; ++k) q[t * H + G * g + k] = oracle_e4m3_encode(yg[k] / sc);
+        }
     }
 }
 
@@ -272,47 +377,19 @@ static void oracle_row(const OracleArgs *a, int64_t t, RowScratch *s)
     if (a->y_out) memcpy(a->y_out + t * H, s->y, (size_t)H * sizeof(float));
 
     /* Step 5: quantisation. */
-    uint8_t *q = a->out_q;
-    if (a->mode == OR_FP8_STATIC) {
-        float sc = a->scale_in;
-        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(s->y[i] / sc);
-    } else if (a->mode == OR_FP8_PER_TOKEN) {
-        float amax = 0.0f;
-        for (int64_t i = 0; i < H; ++i) amax = fmaxf(amax, fabsf(s->y[i]));
-        float sc = fmaxf(amax / 448.0f, 1e-12f);
-        ((float *)a->out_scales)[t] = sc;
-        for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(s->y[i] / sc);
-    } else if (a->mode == OR_NVFP4) {
-        float gs = a->scale_in;
-        uint8_t *bs = (uint8_t *)a->out_scales;
-        for (int64_t b = 0; b < H / 16; ++b) {
-            const float *yb = s->y + 16 * b;
-            float amax = 0.0f;
-            for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(yb[k]));
-            uint8_t sb = oracle_e4m3_encode((amax / 6.0f) * gs);
-            bs[t * (H / 16) + b] = sb;
-            float d = oracle_e4m3_decode(sb);
-            float r = (d == 0.0f) ? 0.0f : gs / d;
-            for (int k = 0; k < 16; k += 2) {
-                uint8_t lo = oracle_e2m1_encode(yb[k] * r);
-                uint8_t hi = oracle_e2m1_encode(yb[k + 1] * r);
-                q[t * (H / 2) + 8 * b + k / 2] = (uint8_t)(lo | (hi << 4));
-            }
-        }
-    } else {
-        int G = group_size(a->mode);
-        int col = (a->mode == OR_FP8_G128_COL || a->mode == OR_FP8_G64_COL);
-        float *sc_out = (float *)a->out_scales;
-        for (int64_t g = 0; g < H / G; ++g) {
-            const float *yg = s->y + G * g;
-            float amax = 0.0f;
-            for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));
-            float sc = fmaxf(amax / 448.0f, 1e-12f);
-            if (col) sc_out[g * a->n + t] = sc;
-            else sc_out[t * (H / G) + g] = sc;
-            for (int k = 0; k < G; ++k) q[t * H + G * g + k] = oracle_e4m3_encode(yg[k] / sc);
-        }
-    }
+    quantize_row(a, t, s->y);
+}
+
+/* SiLU+Mul, one row (R15): a = silu(g) * u in fp32, then step 5 of the norm
+ * op on a. */
+static void oracle_act_row(const OracleArgs *a, int64_t t, RowScratch *s)
+{
+    const int64_t d = a->H;
+    const uint16_t *g = a->x + t * 2 * d, *u = g + d;
+    for (int64_t i = 0; i < d; ++i)
+        s->y[i] = oracle_silu(widen(a->dtype, g[i])) * widen(a->dtype, u[i]);
+    if (a->y_out) memcpy(a->y_out + t * d, s->y, (size_t)d * sizeof(float));
+    quantize_row(a, t, s->y);
 }
 
 typedef struct {
@@ -333,14 +410,18 @@ static void *run_span(void *p)
     s.buf = (float *)malloc((size_t)P * sizeof(float));
     sp->ok = s.h && s.sq && s.y && s.buf;
     if (sp->ok)
-        for (int64_t t = sp->r0; t < sp->r1; ++t) oracle_row(sp->a, t, &s);
+        for (int64_t t = sp->r0; t < sp->r1; ++t) {
+            if (sp->a->silu_mul) oracle_act_row(sp->a, t, &s);
+            else oracle_row(sp->a, t, &s);
+        }
     free(s.h); free(s.sq); free(s.y); free(s.buf);
     return NULL;
 }
 
-/* Whole tensor.  Rows are independent, so splitting them over threads gives
- * bit-identical results for any thread count.  Returns 0 on success,
- * -1 on a bad argument, -2 on an allocation or thread failure. */
+static int run_rows(const OracleArgs *ap, int nthreads);
+
+/* Whole tensor.  Returns 0 on success, -1 on a bad argument, -2 on an
+ * allocation or thread failure. */
 int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
                                    const uint16_t *weight, float eps, int mode, float scale_in,
                                    uint8_t *out_q, void *out_scales, uint16_t *residual_out,
@@ -352,7 +433,16 @@ int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
     if (mode == OR_NVFP4 && H % 16) return -1;
     if (group_size(mode) && H % group_size(mode)) return -1;
     OracleArgs a = {x, residual, weight, eps, mode, scale_in, out_q, out_scales,
-                    residual_out, y_out, n, H, dtype};
+                    residual_out, y_out, n, H, dtype, 0};
+    return run_rows(&a, nthreads);
+}
+
+/* Rows are independent, so splitting them over threads gives bit-identical
+ * results for any thread count. */
+static int run_rows(const OracleArgs *ap, int nthreads)
+{
+    const OracleArgs a = *ap;
+    const int64_t n = a.n;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > n) nthreads = (int)(n > 0 ? n : 1);
     Span *spans = (Span *)calloc((size_t)nthreads, sizeof(Span));
@@ -378,6 +468,32 @@ int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
     free(spans);
     free(th);
     return rc;
+}
+
+/* SiLU+Mul + quantisation (R15): gate_up [n, 2d] (gate | up per row), the
+ * quantisation of `mode` on a = silu(gate) * up; y_out (optional) receives a.
+ * Returns 0, or -1 / -2 like oracle_fused_add_rmsnorm_quant. */
+int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uint8_t *out_q,
+                          void *out_scales, float *y_out, int64_t n, int64_t d, int dtype, int nthreads)
+{
+    if (n < 0 || d <= 0 || mode < 0 || mode > 6 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    if (!gate_up || !out_q || (mode != OR_FP8_STATIC && !out_scales)) return -1;
+    if (mode == OR_NVFP4 && d % 16) return -1;
+    if (group_size(mode) && d % group_size(mode)) return -1;
+    OracleArgs a = {gate_up, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
+                    NULL, y_out, n, d, dtype, 1};
+    return run_rows(&a, nthreads);
+}
+
+/* Array form of oracle_expf, for the accuracy checks. */
+void oracle_expf_array(const float *v, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_expf(v[i]);
+}
+
+void oracle_silu_array(const float *v, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_silu(v[i]);
 }
 
 /* NVFP4 with the global scale taken from the data: gs = 448 * 6 / amax over

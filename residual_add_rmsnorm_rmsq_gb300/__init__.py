@@ -38,9 +38,9 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
-           "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc",
+           "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
-           "rmsq_query_sizes", "rmsq_debug_convert",
+           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
 
@@ -78,6 +78,8 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm_nvfp4_dynamic.restype = ci
         L.rmsq_nvfp4_dynamic_workspace_bytes.argtypes = [i64]
         L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
+        L.rmsq_silu_mul_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
+        L.rmsq_silu_mul_quant.restype = ci
         L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci, ci]
         L.rmsq_set_pipeline_config.restype = ci
         L.rmsq_set_programmatic_launch.argtypes = [ci]
@@ -89,6 +91,8 @@ def load(path: str | None = None):
         L.rmsq_query_sizes.restype = ci
         L.rmsq_debug_convert.argtypes = [ci, vp, vp, i64, vp]
         L.rmsq_debug_convert.restype = ci
+        L.rmsq_debug_activation.argtypes = [ci, vp, vp, vp, i64, vp]
+        L.rmsq_debug_activation.restype = ci
         L.rmsq_status_string.argtypes = [ci]
         L.rmsq_status_string.restype = ctypes.c_char_p
         L.rmsq_last_cuda_error.argtypes = []
@@ -175,6 +179,32 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     return out_q, out_scales, residual_out
 
 
+def silu_mul_quant(gate_up: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *,
+                   out_q: torch.Tensor | None = None, out_scales: torch.Tensor | None = None, stream=None):
+    """rmsq_silu_mul_quant on torch CUDA tensors: gate_up [n, 2d] (gate | up),
+    scale_in a one-element fp32 device tensor (FP8 static scale / NVFP4 global
+    scale).  Missing outputs are allocated.  Returns (q, scales)."""
+    L = load()
+    n, d2 = gate_up.shape
+    if gate_up.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {gate_up.dtype}")
+    if d2 % 2:
+        raise ValueError("gate_up must have an even number of columns (gate | up)")
+    d = d2 // 2
+    for t in (gate_up, out_q, out_scales, scale_in):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    if out_q is None:
+        out_q = torch.empty(n, d // 2 if mode == "nvfp4" else d, dtype=torch.uint8, device=gate_up.device)
+    if out_scales is None:
+        out_scales = scales_like(mode, n, d, gate_up.device)
+    st = L.rmsq_silu_mul_quant(_p(gate_up), MODES[mode], _p(scale_in), _p(out_q), _p(out_scales), n, d,
+                               DTYPES[gate_up.dtype], _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_silu_mul_quant")
+    return out_q, out_scales
+
+
 def nvfp4_dynamic_workspace_bytes(n_tokens: int) -> int:
     return load().rmsq_nvfp4_dynamic_workspace_bytes(n_tokens)
 
@@ -241,6 +271,20 @@ def take_fault_flags() -> int:
     if st:
         raise RmsqError(st, "rmsq_take_fault_flags")
     return f.value
+
+
+def debug_activation(kind: str, values: torch.Tensor, up: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The library's e^x ("exp"), silu ("silu") or silu(g) * u ("silu_mul") on
+    fp32 CUDA tensors, elementwise."""
+    L = load()
+    v = values.contiguous().float()
+    u = None if up is None else up.contiguous().float()
+    out = torch.empty(v.shape, dtype=torch.float32, device=v.device)
+    st = L.rmsq_debug_activation({"exp": 0, "silu": 1, "silu_mul": 2}[kind], _p(v), _p(u), _p(out), v.numel(),
+                                 _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_debug_activation")
+    return out
 
 
 def debug_convert(kind: str, values: torch.Tensor, stream=None) -> torch.Tensor:

@@ -1,0 +1,175 @@
+// SiLU+Mul + quantisation: the activation of a gated MLP fused with the
+// quantisation of its result (vLLM docs "Fusion torch.compile passes",
+// section "SiLU+Mul + Quantization (fuse_act_quant)": silu_and_mul on the
+// gated up-projection and the following quantisation in one kernel, without
+// the full-precision activation tensor in between).
+//
+// Each row of the input holds the gate g in its first d elements and the up
+// projection u in the next d; a = silu(g) * u in fp32 with
+// silu(g) = g / (1 + e^-g), then exactly the quantisation epilogue of the
+// norm kernels (quantize_y) on a.  One CTA per row, thread t on the chunks
+// t*J .. t*J+J-1 of the row, as in the direct norm kernel.
+//
+// e^x is evaluated by W. J. Cody and W. Waite's method ("Software Manual for
+// the Elementary Functions", 1980): x = n ln2 + r with n = rint(x log2 e) and
+// ln2 split in a high part of 15 significant bits (n ln2_hi is exact) and the
+// rest, r formed by two fused multiply-adds; e^r by the degree-7 Taylor
+// polynomial in Horner form, one fused multiply-add per step; then the
+// scaling by 2^n in two power-of-two factors (the second is 1 unless 2^n is
+// not a normal binary32).  Every step is one correctly rounded binary32
+// operation in a fixed order, done in packed pairs where two elements take
+// the same step.
+#pragma once
+
+#include "rmsq_dispatch.cuh"
+
+namespace rmsq {
+
+__device__ __forceinline__ float pow2_bits(int k) { return __int_as_float((k + 127) << 23); }
+
+// e^x for two elements.
+__device__ __forceinline__ float2 exp_cw2(float2 x) {
+    const float hi_lim = 89.0f, lo_lim = -104.0f;    // e^89 > FLT_MAX; e^-104 < half the least subnormal
+    const float2 xc = make_float2(fminf(fmaxf(x.x, lo_lim), hi_lim), fminf(fmaxf(x.y, lo_lim), hi_lim));
+    const float log2e = 1.44269502162933349609375f;  // RN(log2 e)
+    const float ln2_hi = 0.693145751953125f;         // 0x3f317200
+    const float ln2_lo = 1.428606765330187045e-06f;  // RN(ln2 - ln2_hi)
+    const float2 t = mul2_rn(xc, make_float2(log2e, log2e));
+    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 nn = make_float2(-n.x, -n.y);
+    const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), xc));
+    // 1/k!, k = 7 .. 0, rounded to binary32
+    float2 p = make_float2(1.98412701e-4f, 1.98412701e-4f);
+    p = fma2_rn(p, r, make_float2(1.38888892e-3f, 1.38888892e-3f));
+    p = fma2_rn(p, r, make_float2(8.33333377e-3f, 8.33333377e-3f));
+    p = fma2_rn(p, r, make_float2(4.16666679e-2f, 4.16666679e-2f));
+    p = fma2_rn(p, r, make_float2(1.66666672e-1f, 1.66666672e-1f));
+    p = fma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    // 2^k = 2^ka * 2^kb with both factors normal: ka = min(k, 127), or k + 64
+    // below -126; kb = k - ka (0 unless 2^k alone is out of the normal range).
+    const int k0 = __float2int_rn(n.x), k1 = __float2int_rn(n.y);
+    const int a0 = k0 < -126 ? k0 + 64 : min(k0, 127), a1 = k1 < -126 ? k1 + 64 : min(k1, 127);
+    float2 e = mul2_rn(mul2_rn(p, make_float2(pow2_bits(a0), pow2_bits(a1))),
+                       make_float2(pow2_bits(k0 - a0), pow2_bits(k1 - a1)));
+    const float inf = __int_as_float(0x7f800000);
+    e.x = x.x != x.x ? x.x : x.x > hi_lim ? inf : x.x < lo_lim ? 0.0f : e.x;
+    e.y = x.y != x.y ? x.y : x.y > hi_lim ? inf : x.y < lo_lim ? 0.0f : e.y;
+    return e;
+}
+
+// a = silu(g) * u = (g / (1 + e^-g)) * u for two elements.
+__device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
+    const float2 e = exp_cw2(make_float2(-g.x, -g.y));
+    const float2 den = add2_rn(make_float2(1.0f, 1.0f), e);
+    const float2 s = make_float2(__fdiv_rn(g.x, den.x), __fdiv_rn(g.y, den.y));
+    return mul2_rn(s, u);
+}
+
+// Threads per row of the activation kernel: chunks t*J .. t*J+J-1 per thread.
+constexpr int kActMaxThreads = 512;
+
+template <class E, int MODE, int J>
+__global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs a) {
+    __shared__ float s_max[32];
+    __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
+    const int tid = threadIdx.x, nwarps = blockDim.x >> 5;
+    const int row = blockIdx.x;
+    const int c0 = tid * J;
+    allow_dependents();
+    grid_dependency_wait();
+
+    // a.x: the [n, 2d] input; gate chunks of the row, then up chunks
+    const uint4* gp = a.x + (int64_t)row * 2 * a.chunks;
+    const uint4* up = gp + a.chunks;
+    uint4 gv[J], uv[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) gv[j] = uv[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (J >= 2 && a.pair) {   // chunks even: a chunk pair is in the row or wholly past it
+#pragma unroll
+        for (int j = 0; j + 1 < J; j += 2)
+            if (c0 + j < a.chunks) {
+                ld_act_pair(gp + c0 + j, gv[j], gv[j + 1]);
+                ld_act_pair(up + c0 + j, uv[j], uv[j + 1]);
+            }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (c0 + j < a.chunks) {
+                gv[j] = ld_act(gp + c0 + j);
+                uv[j] = ld_act(up + c0 + j);
+            }
+    }
+    const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
+    if constexpr (MODE == kNvfp4) {
+        fill_nvfp4_rtab(s_rtab, sin);
+        __syncthreads();
+    }
+
+    float y[J][8];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+        const uint32_t u[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 v = silu_mul2(make_float2(E::lo(g[k]), E::hi(g[k])), make_float2(E::lo(u[k]), E::hi(u[k])));
+            y[j][2 * k] = v.x;
+            y[j][2 * k + 1] = v.y;
+        }
+    }
+    quantize_y<MODE, J>(a, row, y, sin, s_rtab, s_max, tid, nwarps);
+}
+
+template <class E, int MODE>
+const void* pick_act_j(int J) {
+    switch (J) {
+    case 1: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 1>);
+    case 2: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 2>);
+    case 4: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 4>);
+    default: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 8>);
+    }
+}
+
+template <class E>
+const void* pick_act(int mode, int J) {
+    switch (mode) {
+    case kFp8Static: return pick_act_j<E, kFp8Static>(J);
+    case kFp8PerToken: return pick_act_j<E, kFp8PerToken>(J);
+    case kFp8G128Row: return pick_act_j<E, kFp8G128Row>(J);
+    case kFp8G128Col: return pick_act_j<E, kFp8G128Col>(J);
+    case kFp8G64Row: return pick_act_j<E, kFp8G64Row>(J);
+    case kFp8G64Col: return pick_act_j<E, kFp8G64Col>(J);
+    case kNvfp4: return pick_act_j<E, kNvfp4>(J);
+    default: return nullptr;
+    }
+}
+
+// One launch: la.x = gate_up [n, 2d], la.hidden = d.
+template <class E>
+cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
+    RowArgs a;
+    a.x = static_cast<const uint4*>(la.x);
+    a.res = nullptr;
+    a.w = nullptr;
+    a.res_out = nullptr;
+    a.q = static_cast<uint8_t*>(la.q);
+    a.scales = la.scales;
+    a.scale_in = la.scale_in;
+    a.eps = 0.0f;
+    a.n = la.n;
+    a.hidden = la.hidden;
+    a.chunks = la.hidden / 8;
+    a.inv_hidden_pow2 = 0.0f;
+    a.pair = a.chunks % 2 == 0 && reinterpret_cast<uintptr_t>(la.x) % 32 == 0 &&
+             reinterpret_cast<uintptr_t>(la.q) % 16 == 0;
+    const int J = a.chunks <= 512 ? 1 : a.chunks <= 1024 ? 2 : a.chunks <= 2048 ? 4 : 8;
+    const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
+    const void* fn = pick_act<E>(la.mode, J);
+    if (!fn) return cudaErrorInvalidValue;
+    void* params[] = {&a};
+    return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+}
+
+}  // namespace rmsq

@@ -198,6 +198,55 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     return RMSQ_OK;
 }
 
+int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_in, void* out_q,
+                        void* out_scales, int64_t n_tokens, int64_t d, int dtype, void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (quant_mode < RMSQ_FP8_STATIC || quant_mode > RMSQ_NVFP4) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens < 0 || d <= 0) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens > INT32_MAX || d > RMSQ_ACT_MAX_D) return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    int st = check_shape(quant_mode, n_tokens, d <= RMSQ_MAX_HIDDEN ? d : 8);
+    if (st != RMSQ_OK) return st;
+    if (d % 8 != 0 || (quant_mode == RMSQ_NVFP4 && d % 16 != 0) ||
+        (group_of(quant_mode) && d % group_of(quant_mode) != 0))
+        return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    if (n_tokens == 0) return RMSQ_OK;
+
+    const bool needs_scale_in = quant_mode == RMSQ_FP8_STATIC || quant_mode == RMSQ_NVFP4;
+    const bool has_scales = quant_mode != RMSQ_FP8_STATIC;
+    if (!gate_up || !out_q) return RMSQ_ERR_INVALID_ARG;
+    if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
+    if (has_scales && !out_scales) return RMSQ_ERR_INVALID_ARG;
+    if (!needs_scale_in) scale_in = nullptr;
+    if (!has_scales) out_scales = nullptr;
+    if (!aligned(gate_up, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (quant_mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+
+    size_t q_bytes = 0, sc_bytes = 0;
+    sizes_of(quant_mode, n_tokens, d, &q_bytes, &sc_bytes);
+    const Span GU = span(gate_up, static_cast<size_t>(n_tokens * d) * 4), Q = span(out_q, q_bytes),
+               SC = span(out_scales, sc_bytes), SI = span(scale_in, 4);
+    const Span outs[2] = {Q, SC};
+    for (const Span& o : outs)
+        if (overlaps(o, GU) || overlaps(o, SI)) return RMSQ_ERR_ALIAS;
+    if (overlaps(Q, SC)) return RMSQ_ERR_ALIAS;
+
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+
+    rmsq::LaunchArgs la = {};
+    la.x = gate_up;
+    la.q = out_q;
+    la.scales = out_scales;
+    la.scale_in = scale_in;
+    la.mode = quant_mode;
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(d);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::launch_act_bf16(la, s) : rmsq::launch_act_fp16(la, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return RMSQ_OK;
+}
+
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens) {
     return n_tokens < 0 ? 0 : rmsq::nvfp4_dynamic_workspace_bytes(n_tokens);
 }
@@ -305,6 +354,21 @@ int rmsq_debug_convert(int kind, const float* in, uint8_t* out, int64_t n, void*
     const int st = check_device();
     if (st != RMSQ_OK) return st;
     const cudaError_t e = rmsq::launch_convert(kind, in, out, n, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
+int rmsq_debug_activation(int kind, const float* in, const float* in2, float* out, int64_t n, void* stream) {
+    if (kind < 0 || kind > 2 || n < 0) return RMSQ_ERR_INVALID_ARG;
+    if (n == 0) return RMSQ_OK;
+    if (!in || !out || (kind == 2 && !in2)) return RMSQ_ERR_INVALID_ARG;
+    if (kind != 2) in2 = nullptr;
+    if (!aligned(in, 4) || !aligned(in2, 4) || !aligned(out, 4)) return RMSQ_ERR_ALIGNMENT;
+    const Span O = span(out, static_cast<size_t>(n) * 4);
+    if (overlaps(O, span(in, static_cast<size_t>(n) * 4)) || overlaps(O, span(in2, static_cast<size_t>(n) * 4)))
+        return RMSQ_ERR_ALIAS;
+    const int st = check_device();
+    if (st != RMSQ_OK) return st;
+    const cudaError_t e = rmsq::launch_debug_activation(kind, in, in2, out, n, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
 }
 

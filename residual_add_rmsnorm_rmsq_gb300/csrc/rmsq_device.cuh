@@ -170,6 +170,21 @@ __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
 #endif
 }
 
+// a * b + c with one rounding (fused multiply-add) for two elements.  ptxas
+// may also fuse a packed multiply feeding a packed add on its own (it did so
+// for the Horner steps of an e^x evaluation), so every place whose result
+// would change under such fusion states the fused form explicitly; the
+// packed multiply-adds left elsewhere multiply exact squares or scale by
+// powers of two, where fused and separate roundings agree.
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // ---------------------------------------------------------------------------
 // Conversions.
 // ---------------------------------------------------------------------------

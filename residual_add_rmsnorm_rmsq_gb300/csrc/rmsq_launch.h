@@ -49,6 +49,12 @@ cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);
 // batch amax word and the per-row inv_rms.
 cudaError_t launch_nvfp4_dynamic_bf16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
 cudaError_t launch_nvfp4_dynamic_fp16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
+// The activation's e^x / silu / silu * u, elementwise (kind 0 / 1 / 2).
+cudaError_t launch_debug_activation(int kind, const float* in, const float* in2, float* out, int64_t n,
+                                    cudaStream_t stream);
+// SiLU+Mul + quantisation: a.x = gate_up [n, 2d], a.hidden = d.
+cudaError_t launch_act_bf16(const LaunchArgs& a, cudaStream_t stream);
+cudaError_t launch_act_fp16(const LaunchArgs& a, cudaStream_t stream);
 // Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
 inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
     const size_t raw = 256 + 4 * static_cast<size_t>(n);

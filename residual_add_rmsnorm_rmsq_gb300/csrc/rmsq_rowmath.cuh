@@ -225,30 +225,21 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
     store_fp8_codes<J>(a, row, y, s, tid * J);
 }
 
-// y = (h * inv) * w, then the quantisation of `MODE` and all its stores.
-// `sin` is the static scale (FP8 static) or the global scale (NVFP4);
-// `rtab` the NVFP4 table of gs / decode(code) (fill_nvfp4_rtab), else unused.
-// FP8 per-token does a CTA-wide amax through `s_max` (32 floats) and one
-// __syncthreads; every thread of the CTA must call this.
-template <class E, int MODE, int J>
-__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
-                                             const float (&wv)[J][8], float inv, float sin,
-                                             const float* rtab, float* s_max, int tid, int nwarps,
-                                             float& run_max) {
+// The quantisation of `MODE` of the fp32 values y of the thread's chunks
+// (chunks tid*J .. tid*J+J-1 of `row`) and all its stores.  `sin` is the
+// static scale (FP8 static) or the global scale (NVFP4); `rtab` the NVFP4
+// table of gs / decode(code) (fill_nvfp4_rtab), else unused.  FP8 per-token
+// does a CTA-wide amax through `s_max` (32 floats) and one __syncthreads;
+// every thread of the CTA must call this.
+template <int MODE, int J>
+__device__ __forceinline__ void quantize_y(const RowArgs& a, int row, const float (&y)[J][8], float sin,
+                                           const float* rtab, float* s_max, int tid, int nwarps) {
     const int lane = tid & 31, warp = tid >> 5;
     const int c0 = tid * J;
-    float y[J][8];
-    compute_y<E, J>(hw, wv, inv, y);
-
     if constexpr (MODE == kFp8PerToken) {
         per_token_warp_amax<J>(y, s_max, lane, warp);
         __syncthreads();
         per_token_finish<J>(a, row, y, s_max, tid, nwarps);
-    } else if constexpr (MODE == kNormAmax) {
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            run_max = max_abs8(run_max, y[j]);
-        if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
     } else if constexpr (MODE == kNvfp4) {
         // 16-element blocks = chunk pairs (2m, 2m+1): a lane pair when J == 1,
         // inside the thread otherwise.
@@ -317,8 +308,26 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
                 else sc[(int64_t)row * (a.hidden / G) + g] = s;
             }
         }
-        (void)run_max;
         store_fp8_codes<J>(a, row, y, s, c0);
+    }
+}
+
+// y = (h * inv) * w, then the quantisation of `MODE` (quantize_y), or for
+// kNormAmax the row's inv_rms into the workspace and the running amax.
+template <class E, int MODE, int J>
+__device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const uint32_t (&hw)[J][4],
+                                             const float (&wv)[J][8], float inv, float sin,
+                                             const float* rtab, float* s_max, int tid, int nwarps,
+                                             float& run_max) {
+    float y[J][8];
+    compute_y<E, J>(hw, wv, inv, y);
+    if constexpr (MODE == kNormAmax) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) run_max = max_abs8(run_max, y[j]);
+        if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
+    } else {
+        (void)run_max;
+        quantize_y<MODE, J>(a, row, y, sin, rtab, s_max, tid, nwarps);
     }
 }
 

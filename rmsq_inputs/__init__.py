@@ -36,6 +36,7 @@ _CHUNK = 1 << 22
 
 # stream ids: one independent stream per tensor / purpose
 STREAM_X, STREAM_RES, STREAM_W, STREAM_OUTLIER, STREAM_AUX = 1, 2, 3, 4, 5
+STREAM_GATE, STREAM_UP = 6, 7
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -198,3 +199,43 @@ def decode(n_tokens: int = 1, residual: bool = True, seed: int = 0) -> Workload:
 
 QWEN_TOKENS = (1, 16, 256, 4096, 16384)
 DECODE_TOKENS = tuple(2 ** i for i in range(9))   # 1 .. 256
+
+
+# ----------------------------------------------------------------------------
+# SiLU+Mul + quantisation (the activation of a gated MLP).
+# ----------------------------------------------------------------------------
+
+@dataclass
+class ActWorkload:
+    """Bit patterns of one gated-MLP activation input: gate_up [n, 2d] holds
+    the gate pre-activation in columns [0, d) and the up projection in
+    [d, 2d) of every row."""
+    name: str
+    n_tokens: int
+    d: int
+    dtype: str
+    gate_up: np.ndarray          # uint16 [n, 2d]
+    static_scale: float | None = None
+
+
+def make_act_workload(name: str, n_tokens: int, d: int, *, dtype: str = "bf16",
+                      gate_sigma: float = 2.0, up_sigma: float = 1.0,
+                      gate_range: tuple | None = None, static_scale: float | None = 0.05,
+                      seed: int = 0) -> ActWorkload:
+    """gate ~ gate_sigma * N(0,1) (or uniform on gate_range), up ~ up_sigma * N(0,1)."""
+    n, d = int(n_tokens), int(d)
+    if gate_range is None:
+        g = normal(seed, STREAM_GATE, n * d) * gate_sigma
+    else:
+        lo, hi = gate_range
+        g = lo + (hi - lo) * uniform(seed, STREAM_GATE, n * d)
+    u = normal(seed, STREAM_UP, n * d) * up_sigma
+    gu = np.empty((n, 2 * d), np.uint16)
+    gu[:, :d] = to_bits(g, dtype).reshape(n, d)
+    gu[:, d:] = to_bits(u, dtype).reshape(n, d)
+    return ActWorkload(name, n, d, dtype, gu, static_scale)
+
+
+def llama_mlp(n_tokens: int = 4096, seed: int = 0) -> ActWorkload:
+    """Llama-8B-shaped MLP activation: d = 14336 (gate_up [n, 28672]) bf16."""
+    return make_act_workload(f"llama_mlp_{n_tokens}x14336", n_tokens, 14336, seed=seed)
