@@ -21,7 +21,7 @@ MUTANTS = [
     ("norm_of_unrounded_sum", "s->h[i] = widen(a->dtype, hb);", "s->h[i] = sum;"),
     ("residual_subtracted", "widen(a->dtype, xr[i]) + widen(a->dtype, a->residual[t * H + i])",
      "widen(a->dtype, xr[i]) - widen(a->dtype, a->residual[t * H + i])"),
-    ("times_scale", "oracle_e4m3_encode(s->y[i] / sc)", "oracle_e4m3_encode(s->y[i] * sc)"),
+    ("times_scale", "oracle_e4m3_encode(y[i] / sc)", "oracle_e4m3_encode(y[i] * sc)"),
     ("scale_over_447", "amax / 448.0f", "amax / 447.0f"),
     ("col_stored_row_major", "if (col) sc_out[g * a->n + t] = sc;", "if (col) sc_out[t * (H / G) + g] = sc;"),
     ("group_of_first_half", "for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));",
@@ -38,6 +38,14 @@ MUTANTS = [
     ("e2m1_sign_dropped", "uint8_t sign = signbit(v) ? 0x8 : 0x0;", "uint8_t sign = 0;"),
     ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;", ""),
     ("fp16_subnormal_step", "float k = rintf(ldexpf(a, 24));", "float k = rintf(ldexpf(a, 23));"),
+    # SiLU+Mul (pinned by test_oracle_act.py)
+    ("exp_term_dropped", "    p = fmaf(p, r, 4.16666679e-2f);                         /* 1/24 */\n", ""),
+    ("exp_ln2_lo_dropped", "fmaf(-n, ln2_lo, fmaf(-n, ln2_hi, x))", "fmaf(-n, ln2_hi, x)"),
+    ("exp_no_subnormal_step", "if (k < -126) return (p * pow2i(k + 64)) * pow2i(-64);",
+     "if (k < -126) return 0.0f;"),
+    ("silu_sign_slip", "return g / (1.0f + oracle_expf(-g));", "return g / (1.0f + oracle_expf(g));"),
+    ("gate_up_swapped", "const uint16_t *g = a->x + t * 2 * d, *u = g + d;",
+     "const uint16_t *u = a->x + t * 2 * d, *g = u + d;"),
 ]
 
 
@@ -59,7 +67,8 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
     env = dict(os.environ, ORACLE_LIB=str(so_path))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_op.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_op.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_act.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout, r.stdout[-2000:]
