@@ -306,7 +306,8 @@ int rmsq_debug_convert(int kind, const float *in, uint8_t *out, int64_t n, void 
  * rmsq_silu_mul_quant) on device arrays, so that tests can compare them with
  * a reference element by element.  kind 0: out[i] = e^in[i]; kind 1:
  * out[i] = silu(in[i]); kind 2: out[i] = silu(in[i]) * in2[i] (in2 is
- * ignored otherwise and may be NULL).  Device fp32 arrays of n elements,
+ * ignored otherwise and may be NULL); kind 3: e^in[i] by the shorter steps
+ * the kernel takes when |in[i]| <= 87 (defined only there).  Device fp32 arrays of n elements,
  * 4-byte aligned; out must not overlap the inputs.
  */
 int rmsq_debug_activation(int kind, const float *in, const float *in2, float *out, int64_t n,

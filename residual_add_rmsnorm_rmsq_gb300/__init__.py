@@ -274,13 +274,13 @@ def take_fault_flags() -> int:
 
 
 def debug_activation(kind: str, values: torch.Tensor, up: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """The library's e^x ("exp"), silu ("silu") or silu(g) * u ("silu_mul") on
-    fp32 CUDA tensors, elementwise."""
+    """The library's e^x ("exp"; "exp_mid": the steps used for |x| <= 87),
+    silu ("silu") or silu(g) * u ("silu_mul") on fp32 CUDA tensors, elementwise."""
     L = load()
     v = values.contiguous().float()
     u = None if up is None else up.contiguous().float()
     out = torch.empty(v.shape, dtype=torch.float32, device=v.device)
-    st = L.rmsq_debug_activation({"exp": 0, "silu": 1, "silu_mul": 2}[kind], _p(v), _p(u), _p(out), v.numel(),
+    st = L.rmsq_debug_activation({"exp": 0, "silu": 1, "silu_mul": 2, "exp_mid": 3}[kind], _p(v), _p(u), _p(out), v.numel(),
                                  _stream(stream))
     if st:
         raise RmsqError(st, "rmsq_debug_activation")

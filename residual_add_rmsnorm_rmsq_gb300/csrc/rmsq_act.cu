@@ -15,6 +15,8 @@ __global__ void debug_activation_kernel(int kind, const float* in, const float* 
         float2 r;
         if (kind == 0) {
             r = exp_cw2(x);
+        } else if (kind == 3) {
+            r = exp_cw2_mid(x);
         } else {
             const float2 u = kind == 2 ? make_float2(in2[i], two ? in2[i + 1] : 0.0f) : make_float2(1.0f, 1.0f);
             r = kind == 2 ? silu_mul2(x, u) : silu_mul2(x, make_float2(1.0f, 1.0f));

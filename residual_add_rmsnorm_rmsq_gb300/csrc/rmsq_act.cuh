@@ -59,12 +59,50 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
     return e;
 }
 
-// a = silu(g) * u = (g / (1 + e^-g)) * u for two elements.
+// e^x for two elements with |x| <= 87: the same steps as exp_cw2, where
+// nothing is clamped, 2^n is a normal binary32 (|n| <= 126) and no special
+// value arises, so the result is identical with a single scaling factor.
+__device__ __forceinline__ float2 exp_cw2_mid(float2 x) {
+    const float log2e = 1.44269502162933349609375f, ln2_hi = 0.693145751953125f, ln2_lo = 1.428606765330187045e-06f;
+    const float2 t = mul2_rn(x, make_float2(log2e, log2e));
+    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 nn = make_float2(-n.x, -n.y);
+    const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), x));
+    float2 p = make_float2(1.98412701e-4f, 1.98412701e-4f);
+    p = fma2_rn(p, r, make_float2(1.38888892e-3f, 1.38888892e-3f));
+    p = fma2_rn(p, r, make_float2(8.33333377e-3f, 8.33333377e-3f));
+    p = fma2_rn(p, r, make_float2(4.16666679e-2f, 4.16666679e-2f));
+    p = fma2_rn(p, r, make_float2(1.66666672e-1f, 1.66666672e-1f));
+    p = fma2_rn(p, r, make_float2(0.5f, 0.5f));
+    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    return mul2_rn(p, make_float2(pow2_bits(__float2int_rn(n.x)), pow2_bits(__float2int_rn(n.y))));
+}
+
+// a = silu(g) * u = (g / (1 + e^-g)) * u for two elements; MID: both |g| <= 87,
+// where exp_cw2_mid(-g) equals exp_cw2(-g).
+template <bool MID = false>
 __device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
-    const float2 e = exp_cw2(make_float2(-g.x, -g.y));
+    const float2 e = MID ? exp_cw2_mid(make_float2(-g.x, -g.y)) : exp_cw2(make_float2(-g.x, -g.y));
     const float2 den = add2_rn(make_float2(1.0f, 1.0f), e);
     const float2 s = make_float2(__fdiv_rn(g.x, den.x), __fdiv_rn(g.y, den.y));
     return mul2_rn(s, u);
+}
+
+// a for the thread's J chunks of gate and up.
+template <class E, int J, bool MID>
+__device__ __forceinline__ void act_chunks(const uint4 (&gv)[J], const uint4 (&uv)[J], float (&y)[J][8]) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+        const uint32_t u[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 v = silu_mul2<MID>(make_float2(E::lo(g[k]), E::hi(g[k])), make_float2(E::lo(u[k]), E::hi(u[k])));
+            y[j][2 * k] = v.x;
+            y[j][2 * k + 1] = v.y;
+        }
+    }
 }
 
 // Threads per row of the activation kernel: chunks t*J .. t*J+J-1 per thread.
@@ -107,18 +145,21 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
         __syncthreads();
     }
 
-    float y[J][8];
+    // The usual case (every gate of the thread within +-87, tested on the bit
+    // patterns: a NaN or infinity fails it) takes the shorter e^x steps, with
+    // identical results.
+    uint32_t in_range = 0xffffffffu;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-        const uint32_t u[4] = {uv[j].x, uv[j].y, uv[j].z, uv[j].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float2 v = silu_mul2(make_float2(E::lo(g[k]), E::hi(g[k])), make_float2(E::lo(u[k]), E::hi(u[k])));
-            y[j][2 * k] = v.x;
-            y[j][2 * k + 1] = v.y;
-        }
+        for (int k = 0; k < 4; ++k) in_range &= __vcmpleu2(g[k] & 0x7fff7fffu, E::kBits87 * 0x10001u);
     }
+    float y[J][8];
+    if (in_range == 0xffffffffu)
+        act_chunks<E, J, true>(gv, uv, y);
+    else
+        act_chunks<E, J, false>(gv, uv, y);
     quantize_y<MODE, J>(a, row, y, sin, s_rtab, s_max, tid, nwarps);
 }
 

@@ -358,7 +358,7 @@ int rmsq_debug_convert(int kind, const float* in, uint8_t* out, int64_t n, void*
 }
 
 int rmsq_debug_activation(int kind, const float* in, const float* in2, float* out, int64_t n, void* stream) {
-    if (kind < 0 || kind > 2 || n < 0) return RMSQ_ERR_INVALID_ARG;
+    if (kind < 0 || kind > 3 || n < 0) return RMSQ_ERR_INVALID_ARG;
     if (n == 0) return RMSQ_OK;
     if (!in || !out || (kind == 2 && !in2)) return RMSQ_ERR_INVALID_ARG;
     if (kind != 2) in2 = nullptr;

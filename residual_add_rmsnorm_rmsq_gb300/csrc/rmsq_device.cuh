@@ -23,6 +23,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // apart, and then the smaller one is below half an ulp of T, so neither
 // rounding path can land on a tie of T and both give the larger operand.
 struct Bf16T {
+    static constexpr uint32_t kBits87 = 0x42aeu;    // 87.0 (magnitudes order like their bit patterns)
     static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
     static __device__ __forceinline__ float hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
     static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
@@ -38,6 +39,7 @@ struct Bf16T {
 };
 
 struct Fp16T {
+    static constexpr uint32_t kBits87 = 0x5570u;    // 87.0
     static __device__ __forceinline__ float lo(uint32_t w) {
         float f;
         asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(f) : "r"(w));
