@@ -105,16 +105,18 @@ __device__ __forceinline__ void act_chunks(const uint4 (&gv)[J], const uint4 (&u
     }
 }
 
-// Threads per row of the activation kernel: chunks t*J .. t*J+J-1 per thread.
+// Threads per CTA of the activation kernel.  A CTA covers a segment of
+// `seg` chunks of one row (the whole row for FP8 per-token, whose scale needs
+// the row's amax), thread t the chunks base + t*J .. base + t*J+J-1.
 constexpr int kActMaxThreads = 512;
 
 template <class E, int MODE, int J>
-__global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs a, const int segs, const int seg) {
     __shared__ float s_max[32];
     __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
     const int tid = threadIdx.x, nwarps = blockDim.x >> 5;
-    const int row = blockIdx.x;
-    const int c0 = tid * J;
+    const int row = blockIdx.x / segs;
+    const int c0 = (blockIdx.x - row * segs) * seg + tid * J;
     allow_dependents();
     grid_dependency_wait();
 
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
         act_chunks<E, J, true>(gv, uv, y);
     else
         act_chunks<E, J, false>(gv, uv, y);
-    quantize_y<MODE, J>(a, row, y, sin, s_rtab, s_max, tid, nwarps);
+    quantize_y<MODE, J>(a, row, y, sin, s_rtab, s_max, tid, nwarps, c0);
 }
 
 template <class E, int MODE>
@@ -187,6 +189,21 @@ const void* pick_act(int mode, int J) {
     }
 }
 
+// Segment shape for the modes without a row-wide scale (compile-time tuning;
+// results do not depend on it): kActSegThreads threads of kActSegJ chunks.
+// Small segments (many small CTAs per SM) hide the load latency of this
+// arithmetic-heavy kernel best (measured on GB300: 64 x 4 beat 128 x 2,
+// 256 x 2, 128 x 1 and 256 x 4 on 4096 x 14336).
+#ifndef RMSQ_ACT_SEG_THREADS
+#define RMSQ_ACT_SEG_THREADS 64
+#endif
+#ifndef RMSQ_ACT_SEG_J
+#define RMSQ_ACT_SEG_J 4
+#endif
+constexpr int kActSegThreads = RMSQ_ACT_SEG_THREADS;
+constexpr int kActSegJ = RMSQ_ACT_SEG_J;
+static_assert(kActSegThreads * kActSegJ % 16 == 0, "segments hold whole groups of 128");
+
 // One launch: la.x = gate_up [n, 2d], la.hidden = d.
 template <class E>
 cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
@@ -205,12 +222,27 @@ cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
     a.inv_hidden_pow2 = 0.0f;
     a.pair = a.chunks % 2 == 0 && reinterpret_cast<uintptr_t>(la.x) % 32 == 0 &&
              reinterpret_cast<uintptr_t>(la.q) % 16 == 0;
-    const int J = a.chunks <= 512 ? 1 : a.chunks <= 1024 ? 2 : a.chunks <= 2048 ? 4 : 8;
-    const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
+    int J, threads, seg;
+    if (la.mode == kFp8PerToken) {   // one CTA per row
+        J = a.chunks <= 512 ? 1 : a.chunks <= 1024 ? 2 : a.chunks <= 2048 ? 4 : 8;
+        threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
+        seg = a.chunks;
+    } else {
+        // Equal segments of at most kActSegThreads * kActSegJ chunks, a
+        // multiple of 16 chunks each (so that no group of 128 and no NVFP4
+        // block straddles two).
+        J = kActSegJ;
+        const int most = kActSegThreads * kActSegJ;
+        const int count = (a.chunks + most - 1) / most;
+        seg = ((a.chunks + count - 1) / count + 15) / 16 * 16;
+        threads = ((seg + J - 1) / J + 31) / 32 * 32;
+    }
+    const int segs = (a.chunks + seg - 1) / seg;
     const void* fn = pick_act<E>(la.mode, J);
     if (!fn) return cudaErrorInvalidValue;
-    void* params[] = {&a};
-    return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+    int segs_arg = segs, seg_arg = seg;
+    void* params[] = {&a, &segs_arg, &seg_arg};
+    return launch_kernel(fn, dim3((unsigned)((int64_t)a.n * segs)), dim3(threads), params, 0, stream);
 }
 
 }  // namespace rmsq

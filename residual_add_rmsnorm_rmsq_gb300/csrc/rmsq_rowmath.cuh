@@ -226,16 +226,16 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
 }
 
 // The quantisation of `MODE` of the fp32 values y of the thread's chunks
-// (chunks tid*J .. tid*J+J-1 of `row`) and all its stores.  `sin` is the
-// static scale (FP8 static) or the global scale (NVFP4); `rtab` the NVFP4
-// table of gs / decode(code) (fill_nvfp4_rtab), else unused.  FP8 per-token
-// does a CTA-wide amax through `s_max` (32 floats) and one __syncthreads;
+// (chunks c0 .. c0+J-1 of `row`; c0 = tid*J unless the CTA covers a segment
+// of the row) and all its stores.  `sin` is the static scale (FP8 static) or
+// the global scale (NVFP4); `rtab` the NVFP4 table of gs / decode(code)
+// (fill_nvfp4_rtab), else unused.  FP8 per-token does a CTA-wide amax through
+// `s_max` (32 floats) and one __syncthreads, over the whole row (c0 = tid*J);
 // every thread of the CTA must call this.
 template <int MODE, int J>
 __device__ __forceinline__ void quantize_y(const RowArgs& a, int row, const float (&y)[J][8], float sin,
-                                           const float* rtab, float* s_max, int tid, int nwarps) {
+                                           const float* rtab, float* s_max, int tid, int nwarps, int c0) {
     const int lane = tid & 31, warp = tid >> 5;
-    const int c0 = tid * J;
     if constexpr (MODE == kFp8PerToken) {
         per_token_warp_amax<J>(y, s_max, lane, warp);
         __syncthreads();
@@ -327,7 +327,7 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
         if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
     } else {
         (void)run_max;
-        quantize_y<MODE, J>(a, row, y, sin, rtab, s_max, tid, nwarps);
+        quantize_y<MODE, J>(a, row, y, sin, rtab, s_max, tid, nwarps, tid * J);
     }
 }
 
