@@ -98,6 +98,26 @@ typedef enum {
 } rmsq_quant_mode;
 
 /*
+ * Scale options, OR-ed into a quant_mode argument (blog "[vLLM] Compilation
+ * Fusion Passes", section "Why this design", item 3: E8M0 scales,
+ * column-major scales and TMA alignment registered as combinable options).
+ *  RMSQ_QUANT_E8M0         the dynamic scale (per-token and group modes only)
+ *                          is rounded up to a power of two,
+ *                          s = 2^ceil(log2 max(amax / 448, 1e-12)); it is
+ *                          still stored as fp32 (its E8M0 byte is the
+ *                          exponent field, bits 30..23), q = e4m3(y / s).
+ *  RMSQ_QUANT_TMA_ALIGNED  column-major group scales (_COL modes only) use a
+ *                          stride of n_tokens rounded up to a multiple of 4
+ *                          (16 bytes) between groups: [hidden/G, round4(n)];
+ *                          the padding entries are not written.
+ * Any other bit, or an option with a mode it does not apply to, is
+ * RMSQ_ERR_INVALID_ARG.
+ */
+#define RMSQ_QUANT_MODE_MASK 0x0f
+#define RMSQ_QUANT_E8M0 0x10
+#define RMSQ_QUANT_TMA_ALIGNED 0x20
+
+/*
  * rmsq_fused_add_rmsnorm_quant — one launch of the fused op over n_tokens rows.
  *
  *  x            device, T[n_tokens, hidden], row-major, 16-byte aligned.

@@ -29,6 +29,20 @@ MODES = {
     "nvfp4": 6,
 }
 DTYPES = {"bf16": 0, "fp16": 1}
+# Scale options, appended to a mode name with "+": "e8m0" (dynamic scales
+# rounded up to a power of two) and "tma" (column-major scales with the
+# stride padded to a multiple of 4).
+OPTIONS = {"e8m0": 0x10, "tma": 0x20}
+
+
+def mode_code(mode: str) -> int:
+    """The oracle's integer for a mode name with optional "+e8m0" / "+tma"."""
+    base, *opts = mode.split("+")
+    return MODES[base] | sum(OPTIONS[o] for o in opts)
+
+
+def base_mode(mode: str) -> str:
+    return mode.split("+")[0]
 GROUP = {"fp8_group128_row": 128, "fp8_group128_col": 128,
          "fp8_group64_row": 64, "fp8_group64_col": 64}
 
@@ -167,16 +181,18 @@ def tree_sum(v) -> float:
 
 
 def scale_shape(mode: str, n: int, H: int):
-    """Shape and dtype of the scale output of ``mode`` for an [n, H] input."""
-    if mode == "fp8_static":
+    """Shape and dtype of the scale output of ``mode`` for an [n, H] input
+    (column-major with "+tma": [H/G, n rounded up to 4])."""
+    base = base_mode(mode)
+    if base == "fp8_static":
         return None
-    if mode == "fp8_per_token":
+    if base == "fp8_per_token":
         return (n,), np.float32
-    if mode == "nvfp4":
+    if base == "nvfp4":
         return (n, H // 16), np.uint8
-    G = GROUP[mode]
-    if mode.endswith("_col"):
-        return (H // G, n), np.float32
+    G = GROUP[base]
+    if base.endswith("_col"):
+        return (H // G, (n + 3) // 4 * 4 if "+tma" in mode else n), np.float32
     return (n, H // G), np.float32
 
 
@@ -199,7 +215,7 @@ def run(x, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
     res_out = None if res is None else np.zeros((n, H), np.uint16)
     y = np.zeros((n, H), np.float32) if want_y else None
     rc = lib().oracle_fused_add_rmsnorm_quant(
-        _ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), MODES[mode],
+        _ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), mode_code(mode),
         ctypes.c_float(scale_in), _ptr(q), _ptr(scales), _ptr(res_out), _ptr(y),
         n, H, DTYPES[dtype], int(nthreads))
     if rc != 0:
@@ -256,7 +272,7 @@ def run_silu_mul(gate_up, *, mode: str, scale_in: float = 0.0, dtype: str = "bf1
     ss = scale_shape(mode, n, d)
     scales = None if ss is None else np.zeros(ss[0], ss[1])
     y = np.zeros((n, d), np.float32) if want_y else None
-    rc = lib().oracle_silu_mul_quant(_ptr(gu), MODES[mode], ctypes.c_float(scale_in), _ptr(q), _ptr(scales),
+    rc = lib().oracle_silu_mul_quant(_ptr(gu), mode_code(mode), ctypes.c_float(scale_in), _ptr(q), _ptr(scales),
                                      _ptr(y), n, d, DTYPES[dtype], int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")

@@ -47,6 +47,14 @@
  *      quantisation as the norm op.
  *  R16 e^x is oracle_expf below (the pages do not fix an exp routine; the GPU
  *      evaluates the same steps).
+ *  R17 E8M0 scale option (blog, "Why this design", item 3: E8M0 scales,
+ *      column-major scales and TMA alignment registered as combinable
+ *      options): a dynamic (per-token or group) scale is rounded up to the
+ *      next power of two, s = 2^ceil(log2 s), still stored as fp32 (its E8M0
+ *      byte is the exponent field); q = e4m3(y / s) as before.
+ *  R18 TMA-aligned option for column-major group scales: the stride between
+ *      the scale columns of consecutive groups is n_tokens rounded up to a
+ *      multiple of 4 (16 bytes); the padding entries are not written.
  *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
  */
 #include <math.h>
@@ -56,6 +64,8 @@
 #include <string.h>
 
 enum { OR_BF16 = 0, OR_FP16 = 1 };
+/* Option bits of the mode argument (R17, R18). */
+enum { OR_OPT_E8M0 = 0x10, OR_OPT_TMA = 0x20 };
 enum {
     OR_FP8_STATIC = 0,
     OR_FP8_PER_TOKEN = 1,
@@ -264,7 +274,7 @@ float oracle_tree_sum(const float *v, int64_t n)
 typedef struct {
     const uint16_t *x, *residual, *weight;
     float eps;
-    int mode;
+    int mode;                /* base mode, without option bits */
     float scale_in;          /* FP8 static: s;  NVFP4: global scale gs */
     uint8_t *out_q;
     void *out_scales;
@@ -273,7 +283,33 @@ typedef struct {
     int64_t n, H;
     int dtype;
     int silu_mul;            /* 1: the SiLU+Mul op, x = [n, 2H] gate | up (R15) */
+    int e8m0;                /* R17 */
+    int64_t col_stride;      /* column-major scale stride: n, or n rounded up to 4 (R18) */
 } OracleArgs;
+
+/* The smallest power of two >= x, for a positive normal x: x = f 2^k with
+ * f in [0.5, 1); 2^(k-1) when f = 0.5, else 2^k (exact). */
+static float pow2_ceil(float x)
+{
+    int k;
+    const float f = frexpf(x, &k);
+    return f == 0.5f ? x : ldexpf(1.0f, k);
+}
+
+/* Mode argument -> base mode and options; -1 for an invalid combination. */
+static int split_mode(int mode, int64_t n, int *base, int *e8m0, int64_t *col_stride)
+{
+    *base = mode & 0xf;
+    const int opts = mode & ~0xf;
+    if (*base < 0 || *base > 6 || (opts & ~(OR_OPT_E8M0 | OR_OPT_TMA))) return -1;
+    const int dynamic = *base >= OR_FP8_PER_TOKEN && *base <= OR_FP8_G64_COL;
+    const int col = *base == OR_FP8_G128_COL || *base == OR_FP8_G64_COL;
+    if ((opts & OR_OPT_E8M0) && !dynamic) return -1;
+    if ((opts & OR_OPT_TMA) && !col) return -1;
+    *e8m0 = (opts & OR_OPT_E8M0) != 0;
+    *col_stride = (opts & OR_OPT_TMA) ? (n + 3) / 4 * 4 : n;
+    return 0;
+}
 
 typedef struct {
     float *h, *sq, *y, *buf;
@@ -310,6 +346,7 @@ static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
         float amax = 0.0f;
         for (int64_t i = 0; i < H; ++i) amax = fmaxf(amax, fabsf(y[i]));
         float sc = fmaxf(amax / 448.0f, 1e-12f);
+        if (a->e8m0) sc = pow2_ceil(sc);
         ((float *)a->out_scales)[t] = sc;
         for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(y[i] / sc);
     } else if (a->mode == OR_NVFP4) {
@@ -338,7 +375,8 @@ static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
             float amax = 0.0f;
             for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));
             float sc = fmaxf(amax / 448.0f, 1e-12f);
-            if (col) sc_out[g * a->n + t] = sc;
+            if (a->e8m0) sc = pow2_ceil(sc);
+            if (col) sc_out[g * a->col_stride + t] = sc;
             else sc_out[t * (H / G) + g] = sc;
             for (int k = 0; k < G; ++k) q[t * H + G * g + k] = oracle_e4m3_encode(yg[k] / sc);
         }
@@ -427,13 +465,16 @@ int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
                                    uint8_t *out_q, void *out_scales, uint16_t *residual_out,
                                    float *y_out, int64_t n, int64_t H, int dtype, int nthreads)
 {
-    if (n < 0 || H <= 0 || mode < 0 || mode > 6 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    int e8m0;
+    int64_t col_stride;
+    if (n < 0 || split_mode(mode, n, &mode, &e8m0, &col_stride)) return -1;
+    if (H <= 0 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
     if (!x || !weight || !out_q || (residual && !residual_out)) return -1;
     if (mode != OR_FP8_STATIC && !out_scales) return -1;
     if (mode == OR_NVFP4 && H % 16) return -1;
     if (group_size(mode) && H % group_size(mode)) return -1;
     OracleArgs a = {x, residual, weight, eps, mode, scale_in, out_q, out_scales,
-                    residual_out, y_out, n, H, dtype, 0};
+                    residual_out, y_out, n, H, dtype, 0, e8m0, col_stride};
     return run_rows(&a, nthreads);
 }
 
@@ -476,12 +517,15 @@ static int run_rows(const OracleArgs *ap, int nthreads)
 int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uint8_t *out_q,
                           void *out_scales, float *y_out, int64_t n, int64_t d, int dtype, int nthreads)
 {
-    if (n < 0 || d <= 0 || mode < 0 || mode > 6 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    int e8m0;
+    int64_t col_stride;
+    if (n < 0 || split_mode(mode, n, &mode, &e8m0, &col_stride)) return -1;
+    if (d <= 0 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
     if (!gate_up || !out_q || (mode != OR_FP8_STATIC && !out_scales)) return -1;
     if (mode == OR_NVFP4 && d % 16) return -1;
     if (group_size(mode) && d % group_size(mode)) return -1;
     OracleArgs a = {gate_up, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
-                    NULL, y_out, n, d, dtype, 1};
+                    NULL, y_out, n, d, dtype, 1, e8m0, col_stride};
     return run_rows(&a, nthreads);
 }
 

@@ -30,6 +30,17 @@ MODES = {
     "fp8_group64_col": 5,
     "nvfp4": 6,
 }
+# Scale options (RMSQ_QUANT_E8M0, RMSQ_QUANT_TMA_ALIGNED), appended to a mode
+# name with "+": e.g. "fp8_group128_col+e8m0+tma".
+OPTIONS = {"e8m0": 0x10, "tma": 0x20}
+
+
+def mode_code(mode: str) -> int:
+    """The C quant_mode argument for a mode name with optional "+e8m0" / "+tma"."""
+    base, *opts = mode.split("+")
+    return MODES[base] | sum(OPTIONS[o] for o in opts)
+
+
 # rmsq_dtype
 DTYPES = {torch.bfloat16: 0, torch.float16: 1}
 MAX_HIDDEN = 16384
@@ -113,7 +124,7 @@ def version() -> int:
 
 def query_sizes(mode: str, n_tokens: int, hidden: int) -> tuple[int, int]:
     q, s = ctypes.c_size_t(), ctypes.c_size_t()
-    st = load().rmsq_query_sizes(MODES[mode], n_tokens, hidden, ctypes.byref(q), ctypes.byref(s))
+    st = load().rmsq_query_sizes(mode_code(mode), n_tokens, hidden, ctypes.byref(q), ctypes.byref(s))
     if st:
         raise RmsqError(st, "rmsq_query_sizes")
     return q.value, s.value
@@ -130,15 +141,18 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 def scales_like(mode: str, n_tokens: int, hidden: int, device) -> torch.Tensor | None:
-    """An output tensor of the right shape and dtype for the scales of ``mode``."""
-    if mode == "fp8_static":
+    """An output tensor of the right shape and dtype for the scales of ``mode``
+    (column-major with "+tma": [hidden/G, n_tokens rounded up to 4])."""
+    base = mode.split("+")[0]
+    if base == "fp8_static":
         return None
-    if mode == "fp8_per_token":
+    if base == "fp8_per_token":
         return torch.empty(n_tokens, dtype=torch.float32, device=device)
-    if mode == "nvfp4":
+    if base == "nvfp4":
         return torch.empty(n_tokens, hidden // 16, dtype=torch.uint8, device=device)
-    G = 128 if "128" in mode else 64
-    shape = (hidden // G, n_tokens) if mode.endswith("_col") else (n_tokens, hidden // G)
+    G = 128 if "128" in base else 64
+    cols = (n_tokens + 3) // 4 * 4 if "+tma" in mode else n_tokens
+    shape = (hidden // G, cols) if base.endswith("_col") else (n_tokens, hidden // G)
     return torch.empty(shape, dtype=torch.float32, device=device)
 
 
@@ -171,7 +185,7 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     if residual is not None and residual_out is None:
         residual_out = torch.empty_like(residual)
     st = L.rmsq_fused_add_rmsnorm_quant_ex(_p(x), _p(residual), _p(weight), ctypes.c_float(eps),
-                                           MODES[mode], _p(scale_in), _p(out_q), _p(out_scales),
+                                           mode_code(mode), _p(scale_in), _p(out_q), _p(out_scales),
                                            _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream),
                                            VARIANTS[variant])
     if st:
@@ -198,7 +212,7 @@ def silu_mul_quant(gate_up: torch.Tensor, mode: str, scale_in: torch.Tensor | No
         out_q = torch.empty(n, d // 2 if mode == "nvfp4" else d, dtype=torch.uint8, device=gate_up.device)
     if out_scales is None:
         out_scales = scales_like(mode, n, d, gate_up.device)
-    st = L.rmsq_silu_mul_quant(_p(gate_up), MODES[mode], _p(scale_in), _p(out_q), _p(out_scales), n, d,
+    st = L.rmsq_silu_mul_quant(_p(gate_up), mode_code(mode), _p(scale_in), _p(out_q), _p(out_scales), n, d,
                                DTYPES[gate_up.dtype], _stream(stream))
     if st:
         raise RmsqError(st, "rmsq_silu_mul_quant")

@@ -222,6 +222,8 @@ cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
     a.inv_hidden_pow2 = 0.0f;
     a.pair = a.chunks % 2 == 0 && reinterpret_cast<uintptr_t>(la.x) % 32 == 0 &&
              reinterpret_cast<uintptr_t>(la.q) % 16 == 0;
+    a.e8m0 = la.e8m0;
+    a.col_stride = la.col_stride;
     int J, threads, seg;
     if (la.mode == kFp8PerToken) {   // one CTA per row
         J = a.chunks <= 512 ? 1 : a.chunks <= 1024 ? 2 : a.chunks <= 2048 ? 4 : 8;

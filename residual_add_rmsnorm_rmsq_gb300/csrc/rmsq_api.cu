@@ -61,7 +61,23 @@ int group_of(int mode) {
     }
 }
 
-int check_shape(int mode, int64_t n, int64_t hidden) {
+// Option bits of a quant_mode argument: only with a dynamic FP8 scale
+// (E8M0) or with column-major group scales (TMA-aligned stride).
+bool options_valid(int quant_mode) {
+    const int base = quant_mode & RMSQ_QUANT_MODE_MASK, opts = quant_mode & ~RMSQ_QUANT_MODE_MASK;
+    if (opts & ~(RMSQ_QUANT_E8M0 | RMSQ_QUANT_TMA_ALIGNED)) return false;
+    const bool dynamic = base >= RMSQ_FP8_PER_TOKEN && base <= RMSQ_FP8_GROUP64_COL;
+    const bool col = base == RMSQ_FP8_GROUP128_COL || base == RMSQ_FP8_GROUP64_COL;
+    return !((opts & RMSQ_QUANT_E8M0) && !dynamic) && !((opts & RMSQ_QUANT_TMA_ALIGNED) && !col);
+}
+
+int64_t col_stride_of(int quant_mode, int64_t n) {
+    return (quant_mode & RMSQ_QUANT_TMA_ALIGNED) ? (n + 3) / 4 * 4 : n;
+}
+
+int check_shape(int quant_mode, int64_t n, int64_t hidden) {
+    if (quant_mode < 0 || !options_valid(quant_mode)) return RMSQ_ERR_INVALID_ARG;
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
     if (mode < RMSQ_FP8_STATIC || mode > RMSQ_NVFP4) return RMSQ_ERR_INVALID_ARG;
     if (n < 0 || hidden <= 0) return RMSQ_ERR_INVALID_ARG;
     if (n > INT32_MAX || hidden > RMSQ_MAX_HIDDEN || hidden % 8 != 0) return RMSQ_ERR_UNSUPPORTED_SHAPE;
@@ -71,12 +87,17 @@ int check_shape(int mode, int64_t n, int64_t hidden) {
     return RMSQ_OK;
 }
 
-void sizes_of(int mode, int64_t n, int64_t hidden, size_t* q, size_t* sc) {
+void sizes_of(int quant_mode, int64_t n, int64_t hidden, size_t* q, size_t* sc) {
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
     *q = static_cast<size_t>(mode == RMSQ_NVFP4 ? n * (hidden / 2) : n * hidden);
     switch (mode) {
     case RMSQ_FP8_STATIC: *sc = 0; break;
     case RMSQ_FP8_PER_TOKEN: *sc = static_cast<size_t>(n) * 4; break;
     case RMSQ_NVFP4: *sc = static_cast<size_t>(n * (hidden / 16)); break;
+    case RMSQ_FP8_GROUP128_COL:
+    case RMSQ_FP8_GROUP64_COL:
+        *sc = static_cast<size_t>(col_stride_of(quant_mode, n) * (hidden / group_of(mode))) * 4;
+        break;
     default: *sc = static_cast<size_t>(n * (hidden / group_of(mode))) * 4; break;
     }
 }
@@ -142,9 +163,10 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     if (st != RMSQ_OK) return st;
     if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
     if (n_tokens == 0) return RMSQ_OK;
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
 
-    const bool needs_scale_in = quant_mode == RMSQ_FP8_STATIC || quant_mode == RMSQ_NVFP4;
-    const bool has_scales = quant_mode != RMSQ_FP8_STATIC;
+    const bool needs_scale_in = mode == RMSQ_FP8_STATIC || mode == RMSQ_NVFP4;
+    const bool has_scales = mode != RMSQ_FP8_STATIC;
     if (!x || !weight || !out_q) return RMSQ_ERR_INVALID_ARG;
     if ((residual == nullptr) != (residual_out == nullptr)) return RMSQ_ERR_INVALID_ARG;
     if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
@@ -155,7 +177,7 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16) ||
         !aligned(residual_out, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4))
         return RMSQ_ERR_ALIGNMENT;
-    if (quant_mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
 
     size_t q_bytes = 0, sc_bytes = 0;
     sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
@@ -178,7 +200,7 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     st = check_device();
     if (st != RMSQ_OK) return st;
 
-    rmsq::LaunchArgs la;
+    rmsq::LaunchArgs la = {};
     la.x = x;
     la.res = residual;
     la.w = weight;
@@ -187,7 +209,9 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     la.scales = out_scales;
     la.scale_in = scale_in;
     la.eps = eps;
-    la.mode = quant_mode;
+    la.mode = mode;
+    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(hidden);
     la.variant = variant == RMSQ_VARIANT_DIRECT ? rmsq::kVariantDirect
@@ -201,25 +225,26 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
 int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_in, void* out_q,
                         void* out_scales, int64_t n_tokens, int64_t d, int dtype, void* stream) {
     if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
-    if (quant_mode < RMSQ_FP8_STATIC || quant_mode > RMSQ_NVFP4) return RMSQ_ERR_INVALID_ARG;
+    if (quant_mode < 0 || !options_valid(quant_mode)) return RMSQ_ERR_INVALID_ARG;
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
+    if (mode < RMSQ_FP8_STATIC || mode > RMSQ_NVFP4) return RMSQ_ERR_INVALID_ARG;
     if (n_tokens < 0 || d <= 0) return RMSQ_ERR_INVALID_ARG;
     if (n_tokens > INT32_MAX || d > RMSQ_ACT_MAX_D) return RMSQ_ERR_UNSUPPORTED_SHAPE;
     int st = check_shape(quant_mode, n_tokens, d <= RMSQ_MAX_HIDDEN ? d : 8);
     if (st != RMSQ_OK) return st;
-    if (d % 8 != 0 || (quant_mode == RMSQ_NVFP4 && d % 16 != 0) ||
-        (group_of(quant_mode) && d % group_of(quant_mode) != 0))
+    if (d % 8 != 0 || (mode == RMSQ_NVFP4 && d % 16 != 0) || (group_of(mode) && d % group_of(mode) != 0))
         return RMSQ_ERR_UNSUPPORTED_SHAPE;
     if (n_tokens == 0) return RMSQ_OK;
 
-    const bool needs_scale_in = quant_mode == RMSQ_FP8_STATIC || quant_mode == RMSQ_NVFP4;
-    const bool has_scales = quant_mode != RMSQ_FP8_STATIC;
+    const bool needs_scale_in = mode == RMSQ_FP8_STATIC || mode == RMSQ_NVFP4;
+    const bool has_scales = mode != RMSQ_FP8_STATIC;
     if (!gate_up || !out_q) return RMSQ_ERR_INVALID_ARG;
     if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
     if (has_scales && !out_scales) return RMSQ_ERR_INVALID_ARG;
     if (!needs_scale_in) scale_in = nullptr;
     if (!has_scales) out_scales = nullptr;
     if (!aligned(gate_up, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4)) return RMSQ_ERR_ALIGNMENT;
-    if (quant_mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
 
     size_t q_bytes = 0, sc_bytes = 0;
     sizes_of(quant_mode, n_tokens, d, &q_bytes, &sc_bytes);
@@ -238,7 +263,9 @@ int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_
     la.q = out_q;
     la.scales = out_scales;
     la.scale_in = scale_in;
-    la.mode = quant_mode;
+    la.mode = mode;
+    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(d);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -293,7 +320,7 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic(const void* x, const void* residual, co
     st = check_device();
     if (st != RMSQ_OK) return st;
 
-    rmsq::LaunchArgs la;
+    rmsq::LaunchArgs la = {};
     la.x = x;
     la.res = residual;
     la.w = weight;

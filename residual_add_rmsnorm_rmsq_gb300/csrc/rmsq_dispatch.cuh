@@ -192,6 +192,8 @@ inline RowArgs make_row_args(const LaunchArgs& la) {
     auto on = [](const void* p, uintptr_t b) { return p == nullptr || reinterpret_cast<uintptr_t>(p) % b == 0; };
     a.pair = RMSQ_PAIR_ACCESS && a.chunks % 2 == 0 && on(la.x, 32) && on(la.res, 32) &&
              on(la.res_out, 32) && on(la.q, 16);
+    a.e8m0 = la.e8m0;
+    a.col_stride = la.col_stride;
     return a;
 }
 

@@ -19,6 +19,8 @@ struct LaunchArgs {
     int n;
     int hidden;
     int variant;            // kVariant*
+    bool e8m0;              // dynamic scales rounded up to a power of two
+    int col_stride;         // column-major scale stride (n, or n rounded up to 4)
 };
 
 constexpr int kVariantAuto = 0;

@@ -56,7 +56,16 @@ struct RowArgs {
     // loaded) as one access: set when `chunks` is even, x / residual /
     // residual_out start on 32 bytes and the codes on 16 bytes.
     bool pair;
+    bool e8m0;        // dynamic scales rounded up to a power of two
+    int col_stride;   // column-major scale stride: n, or n rounded up to 4
 };
+
+// The smallest power of two >= s for a positive normal s: s itself when its
+// fraction bits are zero, else the next binade's first value (exact).
+__device__ __forceinline__ float pow2_ceil(float s) {
+    const uint32_t u = __float_as_uint(s);
+    return (u & 0x007fffffu) == 0u ? s : __uint_as_float((u & 0x7f800000u) + 0x00800000u);
+}
 
 template <int MODE> struct ModeTraits {
     static constexpr int group = (MODE == kFp8G128Row || MODE == kFp8G128Col) ? 128
@@ -220,7 +229,8 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
                                                  const float* s_max, int tid, int nwarps) {
     const int lane = tid & 31;
     const float m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
-    const float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+    float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+    if (a.e8m0) s = pow2_ceil(s);
     if (tid == 0) static_cast<float*>(a.scales)[row] = s;
     store_fp8_codes<J>(a, row, y, s, tid * J);
 }
@@ -301,10 +311,11 @@ __device__ __forceinline__ void quantize_y(const RowArgs& a, int row, const floa
             for (int j = 0; j < J; ++j) m = max_abs8(m, y[j]);
             m = lanes_max<LANES>(m);
             s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+            if (a.e8m0) s = pow2_ceil(s);
             if (c0 < a.chunks && (c0 % (G / 8)) == 0) {
                 const int g = c0 / (G / 8);
                 float* sc = static_cast<float*>(a.scales);
-                if constexpr (ModeTraits<MODE>::col) sc[(int64_t)g * a.n + row] = s;
+                if constexpr (ModeTraits<MODE>::col) sc[(int64_t)g * a.col_stride + row] = s;
                 else sc[(int64_t)row * (a.hidden / G) + g] = s;
             }
         }

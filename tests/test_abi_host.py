@@ -51,6 +51,10 @@ def test_query_sizes(L):
     assert rq.query_sizes("nvfp4", 5, 2048) == (5 * 1024, 5 * 128)
     with pytest.raises(rq.RmsqError):
         rq.query_sizes("nvfp4", 5, 40)
+    # scale options: E8M0 keeps the sizes, TMA alignment pads the column stride to 4
+    assert rq.query_sizes("fp8_group64_col+e8m0", 3, 256) == (768, 48)
+    assert rq.query_sizes("fp8_group64_col+tma", 3, 256) == (768, 4 * 4 * 4)
+    assert rq.query_sizes("fp8_group128_col+e8m0+tma", 9, 256) == (9 * 256, 2 * 12 * 4)
 
 
 A, B, C, D, E, F = (0x10000000 * k for k in range(1, 7))   # far-apart fake addresses
@@ -82,6 +86,14 @@ def test_argument_errors(L):
     assert call(L, sc=0) == rq.ERR_INVALID_ARG           # dynamic mode needs out_scales
     assert call(L, mode=0) == rq.ERR_INVALID_ARG         # static needs scale_in
     assert call(L, mode=6, H=64) == rq.ERR_INVALID_ARG   # NVFP4 needs scale_in
+    # scale options only where they apply, no unknown bits
+    assert call(L, mode=0x10 | 0, s_in=A + 0x100) == rq.ERR_INVALID_ARG   # E8M0 with a static scale
+    assert call(L, mode=0x10 | 6, s_in=A + 0x100) == rq.ERR_INVALID_ARG   # E8M0 with NVFP4
+    assert call(L, mode=0x20 | 2) == rq.ERR_INVALID_ARG                   # TMA with row-major scales
+    assert call(L, mode=0x20 | 1) == rq.ERR_INVALID_ARG                   # TMA with per-token
+    assert call(L, mode=0x40 | 1) == rq.ERR_INVALID_ARG                   # unknown bit
+    assert call(L, mode=0x10 | 1) == rq.ERR_NO_DEVICE                     # valid: reaches the device check
+    assert call(L, mode=0x30 | 3, H=128) == rq.ERR_NO_DEVICE
 
 
 def test_shape_errors(L):
