@@ -23,7 +23,9 @@ MUTANTS = [
      "widen(a->dtype, xr[i]) - widen(a->dtype, a->residual[t * H + i])"),
     ("times_scale", "oracle_e4m3_encode(y[i] / sc)", "oracle_e4m3_encode(y[i] * sc)"),
     ("scale_over_447", "amax / 448.0f", "amax / 447.0f"),
-    ("col_stored_row_major", "if (col) sc_out[g * a->n + t] = sc;", "if (col) sc_out[t * (H / G) + g] = sc;"),
+    ("col_stored_row_major", "if (col) sc_out[g * a->col_stride + t] = sc;", "if (col) sc_out[t * (H / G) + g] = sc;"),
+    ("e8m0_rounds_down", "return f == 0.5f ? x : ldexpf(1.0f, k);", "return ldexpf(1.0f, k - 1);"),
+    ("tma_stride_not_padded", "*col_stride = (opts & OR_OPT_TMA) ? (n + 3) / 4 * 4 : n;", "*col_stride = n;"),
     ("group_of_first_half", "for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));",
      "for (int k = 0; k < G / 2; ++k) amax = fmaxf(amax, fabsf(yg[k]));"),
     ("nibbles_swapped", "(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
@@ -68,7 +70,8 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                         os.path.join(ROOT, "tests", "test_oracle_op.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_act.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_act.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_scale_options.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout, r.stdout[-2000:]
