@@ -308,6 +308,39 @@ class ActBuffers:
                                stream=stream)
 
 
+class UnfusedBuffers:
+    """Rotating buffer sets for the unfused two-op sequence (add + RMSNorm
+    writing y in the activation type, then the quantisation of y): one step
+    is both calls.  `bytes` counts what the two ops move, `fused_bytes` what
+    the fused op moves for the same result shape."""
+
+    def __init__(self, torch, rq, wl, mode, min_total_bytes):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        n, H = wl.n_tokens, wl.hidden
+        self.rq, self.wl, self.mode = rq, wl, mode
+        self.res = wl.residual is not None
+        self.fused_bytes = algorithmic_bytes(mode, n, H, 2, self.res)
+        self.bytes = self.fused_bytes + 2 * n * H * 2       # y written by the first op, read by the second
+        self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        x0 = torch.from_numpy(wl.x.view(np.int16)).view(tdt).cuda()
+        r0 = None if not self.res else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).cuda()
+        self.w = torch.from_numpy(wl.weight.view(np.int16)).view(tdt).cuda()
+        self.scale_in = gpu_scale_in(torch, rq, wl, mode, x0, r0, self.w)
+        self.x, self.r, self.ro, self.y, self.q, self.sc = [], [], [], [], [], []
+        for i in range(self.sets):
+            self.x.append(x0 if i == 0 else x0.clone())
+            self.r.append(None if r0 is None else (r0 if i == 0 else r0.clone()))
+            self.ro.append(None if r0 is None else torch.empty_like(r0))
+            self.y.append(torch.empty_like(x0))
+            self.q.append(torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device="cuda"))
+            self.sc.append(rq.scales_like(mode, n, H, "cuda"))
+
+    def launch(self, k, stream):
+        self.rq.fused_add_rmsnorm(self.x[k], self.r[k], self.w, self.wl.eps, y_out=self.y[k],
+                                  residual_out=self.ro[k], stream=stream)
+        self.rq.quant(self.y[k], self.mode, self.scale_in, out_q=self.q[k], out_scales=self.sc[k], stream=stream)
+
+
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
     """Mean device time per launch (ms) over exactly `steps` launches, CUDA
     events on `stream`.
@@ -559,8 +592,9 @@ def decode_sweep(torch, rq, stream, args):
 
 def sweep(torch, rq, stream, peak, args):
     """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of
-    peak), and SiLU+Mul + quantisation on a Llama-8B-shaped MLP activation
-    (4096 tokens, d = 14336)."""
+    peak), the unfused two-op sequence beside the fused op on two of them, and
+    SiLU+Mul + quantisation on a Llama-8B-shaped MLP activation (4096 tokens,
+    d = 14336)."""
     import rmsq_inputs as ri
     out = {}
     groups = [
@@ -571,6 +605,22 @@ def sweep(torch, rq, stream, peak, args):
         (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096", "qwen_nvfp4_dynamic_4096"]),
         (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384", "qwen_nvfp4_dynamic_16384"]),
     ]
+    # The unfused two-op sequence on the same workloads, for the fusion's
+    # saving at kernel level: time per step of both ops against the fused op.
+    for make, name, mode in ((lambda: ri.llama(4096, True), "llama_fp8_per_token", "fp8_per_token"),
+                             (lambda: ri.dsv3(8192), "dsv3_fp8_group128_row", "fp8_group128_row")):
+        wl = make()
+        fb = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
+        fused_ms = time_launches(torch, rq, wl, mode, fb, args.sweep_steps, 5, stream)
+        del fb
+        ub = UnfusedBuffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
+        ms = time_launches(torch, rq, wl, mode, ub, args.sweep_steps, 5, stream)
+        out[f"{name}_unfused"] = {"us": round(ms * 1e3, 3), "fused_us": round(fused_ms * 1e3, 3),
+                                  "fusion_speedup": round(ms / fused_ms, 3), "bytes": ub.bytes,
+                                  "fused_bytes": ub.fused_bytes,
+                                  "GB/s_moved": round(ub.bytes / (ms / 1e3) / 1e9, 1)}
+        del ub, wl
+        torch.cuda.empty_cache()
     act = ri.llama_mlp(4096)
     for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):
         name = f"llama_mlp_silu_mul_{mode}"

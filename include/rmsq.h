@@ -236,6 +236,30 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc(const void *x, const void *resi
                                                  int64_t hidden, int dtype, void *stream,
                                                  int variant);
 
+/*
+ * The unfused two-op sequence the fused op replaces (vLLM docs "Fusion
+ * torch.compile passes", fuse_norm_quant: fused_add_rms_norm / rms_norm
+ * followed by the quantisation op), for comparison and for callers that need
+ * the normalised activations themselves.
+ *
+ * rmsq_fused_add_rmsnorm — steps 1-4 of rmsq_fused_add_rmsnorm_quant (residual
+ * add and write-back, RMSNorm with the same canonical sum), then y rounded to
+ * the activation type (nearest even) into y_out: device [n_tokens, hidden],
+ * same type as x, 16-byte aligned, overlapping no input or residual_out.
+ * Arguments and errors otherwise as rmsq_fused_add_rmsnorm_quant.
+ *
+ * rmsq_quant — the quantisation step of rmsq_fused_add_rmsnorm_quant applied
+ * to a [n_tokens, hidden] tensor y of the activation type (widened exactly to
+ * fp32): every quant_mode and scale option, same outputs and layouts.
+ * Running the two in sequence gives the unfused result, which differs from
+ * the fused op's in that y is rounded to the activation type in between.
+ */
+int rmsq_fused_add_rmsnorm(const void *x, const void *residual, const void *weight, float eps,
+                           void *y_out, void *residual_out, int64_t n_tokens, int64_t hidden, int dtype,
+                           void *stream);
+int rmsq_quant(const void *y, int quant_mode, const float *scale_in, void *out_q, void *out_scales,
+               int64_t n_tokens, int64_t hidden, int dtype, void *stream);
+
 /* Largest d (activation width) of rmsq_silu_mul_quant. */
 #define RMSQ_ACT_MAX_D 32768
 

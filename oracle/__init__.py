@@ -119,6 +119,10 @@ def _configure(L):
     L.oracle_silu_mul_quant.argtypes = [vp, ctypes.c_int, f32, vp, vp, vp, i64, i64, ctypes.c_int,
                                         ctypes.c_int]
     L.oracle_silu_mul_quant.restype = ctypes.c_int
+    L.oracle_add_rmsnorm.argtypes = [vp, vp, vp, f32, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int]
+    L.oracle_add_rmsnorm.restype = ctypes.c_int
+    L.oracle_quant.argtypes = [vp, ctypes.c_int, f32, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int]
+    L.oracle_quant.restype = ctypes.c_int
     L.oracle_expf.argtypes, L.oracle_expf.restype = [f32], f32
     L.oracle_silu.argtypes, L.oracle_silu.restype = [f32], f32
     for name in ("oracle_expf_array", "oracle_silu_array"):
@@ -293,6 +297,36 @@ def run_silu_mul_workload(wl, mode: str, *, scale_in: float | None = None, want_
                      nthreads=nthreads)
     r["scale_in"] = scale_in
     return r
+
+
+def run_add_rmsnorm(x, residual, weight, *, eps: float, dtype: str = "bf16", nthreads: int = 1) -> dict:
+    """First op of the unfused sequence: ``y_t`` (y rounded to the activation
+    type, uint16 bit patterns [n, H]) and ``residual_out``."""
+    x = np.ascontiguousarray(x, np.uint16)
+    n, H = x.shape
+    weight = np.ascontiguousarray(weight, np.uint16)
+    res = None if residual is None else np.ascontiguousarray(residual, np.uint16)
+    y_t = np.zeros((n, H), np.uint16)
+    ro = None if res is None else np.zeros((n, H), np.uint16)
+    rc = lib().oracle_add_rmsnorm(_ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), _ptr(y_t), _ptr(ro),
+                                  n, H, DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"y_t": y_t, "residual_out": ro}
+
+
+def run_quant(y_t, *, mode: str, scale_in: float = 0.0, dtype: str = "bf16", nthreads: int = 1) -> dict:
+    """Second op of the unfused sequence: the quantisation of a T tensor."""
+    y_t = np.ascontiguousarray(y_t, np.uint16)
+    n, H = y_t.shape
+    q = np.zeros((n, H // 2) if base_mode(mode) == "nvfp4" else (n, H), np.uint8)
+    ss = scale_shape(mode, n, H)
+    scales = None if ss is None else np.zeros(ss[0], ss[1])
+    rc = lib().oracle_quant(_ptr(y_t), mode_code(mode), ctypes.c_float(scale_in), _ptr(q), _ptr(scales), n, H,
+                            DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": scales, "residual_out": None}
 
 
 def nvfp4_global_scale(y_amax: float) -> float:

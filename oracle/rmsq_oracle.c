@@ -55,6 +55,11 @@
  *  R18 TMA-aligned option for column-major group scales: the stride between
  *      the scale columns of consecutive groups is n_tokens rounded up to a
  *      multiple of 4 (16 bytes); the padding entries are not written.
+ *  R19 the unfused sequence the fusion replaces (vLLM docs, same page,
+ *      fuse_norm_quant: rms_norm / fused_add_rms_norm followed by quant_fp8):
+ *      the first op writes y rounded to the activation type T (nearest even)
+ *      and the updated residual; the second quantises that T tensor exactly
+ *      as step 5 quantises y.
  *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
  */
 #include <math.h>
@@ -282,7 +287,9 @@ typedef struct {
     float *y_out;            /* optional fp32 copy of y [n, H] for diagnostics */
     int64_t n, H;
     int dtype;
-    int silu_mul;            /* 1: the SiLU+Mul op, x = [n, 2H] gate | up (R15) */
+    int silu_mul;            /* 1: the SiLU+Mul op, x = [n, 2H] gate | up (R15);
+                                2: quantisation of x alone (R19) */
+    uint16_t *y_t_out;       /* R19: y rounded to T instead of step 5 */
     int e8m0;                /* R17 */
     int64_t col_stride;      /* column-major scale stride: n, or n rounded up to 4 (R18) */
 } OracleArgs;
@@ -413,8 +420,19 @@ static void oracle_row(const OracleArgs *a, int64_t t, RowScratch *s)
     for (int64_t i = 0; i < H; ++i)
         s->y[i] = (s->h[i] * inv) * widen(a->dtype, a->weight[i]);
     if (a->y_out) memcpy(a->y_out + t * H, s->y, (size_t)H * sizeof(float));
+    if (a->y_t_out) {   /* R19: the unfused first op ends here */
+        for (int64_t i = 0; i < H; ++i) a->y_t_out[t * H + i] = narrow(a->dtype, s->y[i]);
+        return;
+    }
 
     /* Step 5: quantisation. */
+    quantize_row(a, t, s->y);
+}
+
+/* R19, second op: step 5 on a T row. */
+static void oracle_quant_row(const OracleArgs *a, int64_t t, RowScratch *s)
+{
+    for (int64_t i = 0; i < a->H; ++i) s->y[i] = widen(a->dtype, a->x[t * a->H + i]);
     quantize_row(a, t, s->y);
 }
 
@@ -449,7 +467,8 @@ static void *run_span(void *p)
     sp->ok = s.h && s.sq && s.y && s.buf;
     if (sp->ok)
         for (int64_t t = sp->r0; t < sp->r1; ++t) {
-            if (sp->a->silu_mul) oracle_act_row(sp->a, t, &s);
+            if (sp->a->silu_mul == 2) oracle_quant_row(sp->a, t, &s);
+            else if (sp->a->silu_mul) oracle_act_row(sp->a, t, &s);
             else oracle_row(sp->a, t, &s);
         }
     free(s.h); free(s.sq); free(s.y); free(s.buf);
@@ -474,7 +493,7 @@ int oracle_fused_add_rmsnorm_quant(const uint16_t *x, const uint16_t *residual,
     if (mode == OR_NVFP4 && H % 16) return -1;
     if (group_size(mode) && H % group_size(mode)) return -1;
     OracleArgs a = {x, residual, weight, eps, mode, scale_in, out_q, out_scales,
-                    residual_out, y_out, n, H, dtype, 0, e8m0, col_stride};
+                    residual_out, y_out, n, H, dtype, 0, NULL, e8m0, col_stride};
     return run_rows(&a, nthreads);
 }
 
@@ -525,7 +544,35 @@ int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uin
     if (mode == OR_NVFP4 && d % 16) return -1;
     if (group_size(mode) && d % group_size(mode)) return -1;
     OracleArgs a = {gate_up, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
-                    NULL, y_out, n, d, dtype, 1, e8m0, col_stride};
+                    NULL, y_out, n, d, dtype, 1, NULL, e8m0, col_stride};
+    return run_rows(&a, nthreads);
+}
+
+/* R19: the two ops of the unfused sequence.  oracle_add_rmsnorm writes y
+ * rounded to T into y_t [n, H] (and residual_out); oracle_quant quantises a T
+ * tensor [n, H] by `mode`.  Returns like oracle_fused_add_rmsnorm_quant. */
+int oracle_add_rmsnorm(const uint16_t *x, const uint16_t *residual, const uint16_t *weight, float eps,
+                       uint16_t *y_t, uint16_t *residual_out, int64_t n, int64_t H, int dtype, int nthreads)
+{
+    if (n < 0 || H <= 0 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    if (!x || !weight || !y_t || (residual && !residual_out)) return -1;
+    OracleArgs a = {x, residual, weight, eps, OR_FP8_STATIC, 0.0f, NULL, NULL,
+                    residual_out, NULL, n, H, dtype, 0, y_t, 0, n};
+    return run_rows(&a, nthreads);
+}
+
+int oracle_quant(const uint16_t *y_t, int mode, float scale_in, uint8_t *out_q, void *out_scales,
+                 int64_t n, int64_t H, int dtype, int nthreads)
+{
+    int e8m0;
+    int64_t col_stride;
+    if (n < 0 || split_mode(mode, n, &mode, &e8m0, &col_stride)) return -1;
+    if (H <= 0 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    if (!y_t || !out_q || (mode != OR_FP8_STATIC && !out_scales)) return -1;
+    if (mode == OR_NVFP4 && H % 16) return -1;
+    if (group_size(mode) && H % group_size(mode)) return -1;
+    OracleArgs a = {y_t, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
+                    NULL, NULL, n, H, dtype, 2, NULL, e8m0, col_stride};
     return run_rows(&a, nthreads);
 }
 

@@ -50,6 +50,7 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
+           "rmsq_fused_add_rmsnorm", "rmsq_quant",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
            "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
@@ -89,6 +90,10 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm_nvfp4_dynamic.restype = ci
         L.rmsq_nvfp4_dynamic_workspace_bytes.argtypes = [i64]
         L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
+        L.rmsq_fused_add_rmsnorm.argtypes = [vp, vp, vp, f32, vp, vp, i64, i64, ci, vp]
+        L.rmsq_fused_add_rmsnorm.restype = ci
+        L.rmsq_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
+        L.rmsq_quant.restype = ci
         L.rmsq_silu_mul_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
         L.rmsq_silu_mul_quant.restype = ci
         L.rmsq_set_pipeline_config.argtypes = [ci, ci, ci, ci]
@@ -191,6 +196,44 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
+
+
+def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, weight: torch.Tensor, eps: float, *,
+                      y_out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None, stream=None):
+    """rmsq_fused_add_rmsnorm: the norm alone, y in the activation type.
+    Returns (y, residual_out)."""
+    L = load()
+    n, H = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {x.dtype}")
+    if y_out is None:
+        y_out = torch.empty_like(x)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(residual)
+    st = L.rmsq_fused_add_rmsnorm(_p(x), _p(residual), _p(weight), ctypes.c_float(eps), _p(y_out), _p(residual_out),
+                                  n, H, DTYPES[x.dtype], _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_fused_add_rmsnorm")
+    return y_out, residual_out
+
+
+def quant(y: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *, out_q: torch.Tensor | None = None,
+          out_scales: torch.Tensor | None = None, stream=None):
+    """rmsq_quant: the quantisation of a [n, H] activation-type tensor.
+    Returns (q, scales)."""
+    L = load()
+    n, H = y.shape
+    if y.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {y.dtype}")
+    if out_q is None:
+        out_q = torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device=y.device)
+    if out_scales is None:
+        out_scales = scales_like(mode, n, H, y.device)
+    st = L.rmsq_quant(_p(y), mode_code(mode), _p(scale_in), _p(out_q), _p(out_scales), n, H, DTYPES[y.dtype],
+                      _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_quant")
+    return out_q, out_scales
 
 
 def silu_mul_quant(gate_up: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *,

@@ -3,8 +3,10 @@
 #include "rmsq_act.cuh"
 
 namespace rmsq {
-cudaError_t launch_act_bf16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Bf16T>(a, stream); }
-cudaError_t launch_act_fp16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Fp16T>(a, stream); }
+cudaError_t launch_act_bf16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Bf16T>(a, true, stream); }
+cudaError_t launch_act_fp16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Fp16T>(a, true, stream); }
+cudaError_t launch_quant_bf16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Bf16T>(a, false, stream); }
+cudaError_t launch_quant_fp16(const LaunchArgs& a, cudaStream_t stream) { return launch_act<Fp16T>(a, false, stream); }
 
 // Same steps as the kernel, two elements per thread, for elementwise checks.
 __global__ void debug_activation_kernel(int kind, const float* in, const float* in2, float* out, int64_t n) {

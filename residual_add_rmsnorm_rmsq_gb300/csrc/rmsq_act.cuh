@@ -110,7 +110,10 @@ __device__ __forceinline__ void act_chunks(const uint4 (&gv)[J], const uint4 (&u
 // the row's amax), thread t the chunks base + t*J .. base + t*J+J-1.
 constexpr int kActMaxThreads = 512;
 
-template <class E, int MODE, int J>
+// SILU: the input row is gate | up and y = silu(gate) * up; otherwise the
+// input is a [n, hidden] T tensor quantised as it is (the second op of the
+// unfused sequence).
+template <class E, int MODE, int J, bool SILU>
 __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs a, const int segs, const int seg) {
     __shared__ float s_max[32];
     __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
@@ -120,8 +123,9 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
     allow_dependents();
     grid_dependency_wait();
 
-    // a.x: the [n, 2d] input; gate chunks of the row, then up chunks
-    const uint4* gp = a.x + (int64_t)row * 2 * a.chunks;
+    // a.x: the [n, 2d] input (gate chunks of the row, then up chunks), or
+    // the [n, d] input without SILU (read as the "gate" half)
+    const uint4* gp = a.x + (int64_t)row * (SILU ? 2 : 1) * a.chunks;
     const uint4* up = gp + a.chunks;
     uint4 gv[J], uv[J];
 #pragma unroll
@@ -131,14 +135,14 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
         for (int j = 0; j + 1 < J; j += 2)
             if (c0 + j < a.chunks) {
                 ld_act_pair(gp + c0 + j, gv[j], gv[j + 1]);
-                ld_act_pair(up + c0 + j, uv[j], uv[j + 1]);
+                if constexpr (SILU) ld_act_pair(up + c0 + j, uv[j], uv[j + 1]);
             }
     } else {
 #pragma unroll
         for (int j = 0; j < J; ++j)
             if (c0 + j < a.chunks) {
                 gv[j] = ld_act(gp + c0 + j);
-                uv[j] = ld_act(up + c0 + j);
+                if constexpr (SILU) uv[j] = ld_act(up + c0 + j);
             }
     }
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
@@ -147,44 +151,53 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
         __syncthreads();
     }
 
-    // The usual case (every gate of the thread within +-87, tested on the bit
-    // patterns: a NaN or infinity fails it) takes the shorter e^x steps, with
-    // identical results.
-    uint32_t in_range = 0xffffffffu;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) in_range &= __vcmpleu2(g[k] & 0x7fff7fffu, E::kBits87 * 0x10001u);
-    }
     float y[J][8];
-    if (in_range == 0xffffffffu)
-        act_chunks<E, J, true>(gv, uv, y);
-    else
-        act_chunks<E, J, false>(gv, uv, y);
+    if constexpr (SILU) {
+        // The usual case (every gate of the thread within +-87, tested on the
+        // bit patterns: a NaN or infinity fails it) takes the shorter e^x
+        // steps, with identical results.
+        uint32_t in_range = 0xffffffffu;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) in_range &= __vcmpleu2(g[k] & 0x7fff7fffu, E::kBits87 * 0x10001u);
+        }
+        if (in_range == 0xffffffffu)
+            act_chunks<E, J, true>(gv, uv, y);
+        else
+            act_chunks<E, J, false>(gv, uv, y);
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const uint32_t g[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { y[j][2 * k] = E::lo(g[k]); y[j][2 * k + 1] = E::hi(g[k]); }
+        }
+    }
     quantize_y<MODE, J>(a, row, y, sin, s_rtab, s_max, tid, nwarps, c0);
 }
 
-template <class E, int MODE>
+template <class E, int MODE, bool SILU>
 const void* pick_act_j(int J) {
     switch (J) {
-    case 1: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 1>);
-    case 2: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 2>);
-    case 4: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 4>);
-    default: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 8>);
+    case 1: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 1, SILU>);
+    case 2: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 2, SILU>);
+    case 4: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 4, SILU>);
+    default: return reinterpret_cast<const void*>(&act_rows_kernel<E, MODE, 8, SILU>);
     }
 }
 
-template <class E>
+template <class E, bool SILU>
 const void* pick_act(int mode, int J) {
     switch (mode) {
-    case kFp8Static: return pick_act_j<E, kFp8Static>(J);
-    case kFp8PerToken: return pick_act_j<E, kFp8PerToken>(J);
-    case kFp8G128Row: return pick_act_j<E, kFp8G128Row>(J);
-    case kFp8G128Col: return pick_act_j<E, kFp8G128Col>(J);
-    case kFp8G64Row: return pick_act_j<E, kFp8G64Row>(J);
-    case kFp8G64Col: return pick_act_j<E, kFp8G64Col>(J);
-    case kNvfp4: return pick_act_j<E, kNvfp4>(J);
+    case kFp8Static: return pick_act_j<E, kFp8Static, SILU>(J);
+    case kFp8PerToken: return pick_act_j<E, kFp8PerToken, SILU>(J);
+    case kFp8G128Row: return pick_act_j<E, kFp8G128Row, SILU>(J);
+    case kFp8G128Col: return pick_act_j<E, kFp8G128Col, SILU>(J);
+    case kFp8G64Row: return pick_act_j<E, kFp8G64Row, SILU>(J);
+    case kFp8G64Col: return pick_act_j<E, kFp8G64Col, SILU>(J);
+    case kNvfp4: return pick_act_j<E, kNvfp4, SILU>(J);
     default: return nullptr;
     }
 }
@@ -204,9 +217,10 @@ constexpr int kActSegThreads = RMSQ_ACT_SEG_THREADS;
 constexpr int kActSegJ = RMSQ_ACT_SEG_J;
 static_assert(kActSegThreads * kActSegJ % 16 == 0, "segments hold whole groups of 128");
 
-// One launch: la.x = gate_up [n, 2d], la.hidden = d.
+// One launch: la.x = gate_up [n, 2d] (silu) or the [n, d] tensor to
+// quantise, la.hidden = d.
 template <class E>
-cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
+cudaError_t launch_act(const LaunchArgs& la, bool silu, cudaStream_t stream) {
     RowArgs a;
     a.x = static_cast<const uint4*>(la.x);
     a.res = nullptr;
@@ -240,7 +254,7 @@ cudaError_t launch_act(const LaunchArgs& la, cudaStream_t stream) {
         threads = ((seg + J - 1) / J + 31) / 32 * 32;
     }
     const int segs = (a.chunks + seg - 1) / seg;
-    const void* fn = pick_act<E>(la.mode, J);
+    const void* fn = silu ? pick_act<E, true>(la.mode, J) : pick_act<E, false>(la.mode, J);
     if (!fn) return cudaErrorInvalidValue;
     int segs_arg = segs, seg_arg = seg;
     void* params[] = {&a, &segs_arg, &seg_arg};

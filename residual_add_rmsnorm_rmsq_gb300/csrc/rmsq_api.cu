@@ -274,6 +274,92 @@ int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_
     return RMSQ_OK;
 }
 
+int rmsq_fused_add_rmsnorm(const void* x, const void* residual, const void* weight, float eps, void* y_out,
+                           void* residual_out, int64_t n_tokens, int64_t hidden, int dtype, void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(RMSQ_FP8_STATIC, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return RMSQ_OK;
+    if (!x || !weight || !y_out) return RMSQ_ERR_INVALID_ARG;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16) || !aligned(residual_out, 16) ||
+        !aligned(y_out, 16))
+        return RMSQ_ERR_ALIGNMENT;
+    const size_t act = static_cast<size_t>(n_tokens * hidden) * 2;
+    const Span X = span(x, act), R = span(residual, act), W = span(weight, hidden * 2),
+               RO = span(residual_out, act), Y = span(y_out, act);
+    if (residual && X.lo != R.lo && overlaps(X, R)) return RMSQ_ERR_ALIAS;
+    if (residual_out) {
+        if (RO.lo != X.lo && overlaps(RO, X)) return RMSQ_ERR_ALIAS;
+        if (RO.lo != R.lo && overlaps(RO, R)) return RMSQ_ERR_ALIAS;
+        if (overlaps(RO, W)) return RMSQ_ERR_ALIAS;
+    }
+    if (overlaps(Y, X) || overlaps(Y, R) || overlaps(Y, W) || overlaps(Y, RO)) return RMSQ_ERR_ALIAS;
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+
+    rmsq::LaunchArgs la = {};
+    la.x = x;
+    la.res = residual;
+    la.w = weight;
+    la.res_out = residual_out;
+    la.q = y_out;
+    la.eps = eps;
+    la.mode = rmsq::kModeNormOnly;
+    la.col_stride = static_cast<int>(n_tokens);
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    la.variant = rmsq::kVariantAuto;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::launch_rows_bf16(la, s) : rmsq::launch_rows_fp16(la, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return RMSQ_OK;
+}
+
+int rmsq_quant(const void* y, int quant_mode, const float* scale_in, void* out_q, void* out_scales,
+               int64_t n_tokens, int64_t hidden, int dtype, void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(quant_mode, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (n_tokens == 0) return RMSQ_OK;
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
+    const bool needs_scale_in = mode == RMSQ_FP8_STATIC || mode == RMSQ_NVFP4;
+    const bool has_scales = mode != RMSQ_FP8_STATIC;
+    if (!y || !out_q) return RMSQ_ERR_INVALID_ARG;
+    if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
+    if (has_scales && !out_scales) return RMSQ_ERR_INVALID_ARG;
+    if (!needs_scale_in) scale_in = nullptr;
+    if (!has_scales) out_scales = nullptr;
+    if (!aligned(y, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    size_t q_bytes = 0, sc_bytes = 0;
+    sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
+    const Span Yi = span(y, static_cast<size_t>(n_tokens * hidden) * 2), Q = span(out_q, q_bytes),
+               SC = span(out_scales, sc_bytes), SI = span(scale_in, 4);
+    const Span outs[2] = {Q, SC};
+    for (const Span& o : outs)
+        if (overlaps(o, Yi) || overlaps(o, SI)) return RMSQ_ERR_ALIAS;
+    if (overlaps(Q, SC)) return RMSQ_ERR_ALIAS;
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+
+    rmsq::LaunchArgs la = {};
+    la.x = y;
+    la.q = out_q;
+    la.scales = out_scales;
+    la.scale_in = scale_in;
+    la.mode = mode;
+    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::launch_quant_bf16(la, s) : rmsq::launch_quant_fp16(la, s);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return RMSQ_OK;
+}
+
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens) {
     return n_tokens < 0 ? 0 : rmsq::nvfp4_dynamic_workspace_bytes(n_tokens);
 }

@@ -22,6 +22,8 @@
 
 namespace rmsq {
 
+static_assert(kModeNormOnly == kNormOnly, "host and kernel codes of the norm-only mode");
+
 // Set by a pipelined CTA that gave up waiting for its copies (this unit's
 // instantiations only).
 static __device__ unsigned int g_pipe_fault;
@@ -88,6 +90,7 @@ const void* pick_kernel(int mode, bool res, bool pipe, int J, int R = 1) {
     case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J, R);
     case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J, R);
     case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J, R);
+    case kNormOnly: return pick_res<E, kNormOnly>(res, pipe, J, R);
     default: return nullptr;
     }
 }

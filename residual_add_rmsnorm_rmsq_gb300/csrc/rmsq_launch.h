@@ -23,6 +23,9 @@ struct LaunchArgs {
     int col_stride;         // column-major scale stride (n, or n rounded up to 4)
 };
 
+// LaunchArgs::mode of the norm alone (the kernels' Mode::kNormOnly).
+constexpr int kModeNormOnly = 8;
+
 constexpr int kVariantAuto = 0;
 constexpr int kVariantDirect = 1;
 constexpr int kVariantPipelined = 2;
@@ -57,6 +60,9 @@ cudaError_t launch_debug_activation(int kind, const float* in, const float* in2,
 // SiLU+Mul + quantisation: a.x = gate_up [n, 2d], a.hidden = d.
 cudaError_t launch_act_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_act_fp16(const LaunchArgs& a, cudaStream_t stream);
+// Quantisation of a T tensor: a.x = [n, d], a.hidden = d.
+cudaError_t launch_quant_bf16(const LaunchArgs& a, cudaStream_t stream);
+cudaError_t launch_quant_fp16(const LaunchArgs& a, cudaStream_t stream);
 // Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
 inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
     const size_t raw = 256 + 4 * static_cast<size_t>(n);

@@ -31,6 +31,9 @@ enum Mode : int {
     // RMSNorm, the row's inv_rms stored in the workspace and the running
     // amax of y folded into the workspace's amax word; no codes.
     kNormAmax = 7,
+    // The norm alone (the first op of the unfused sequence): y rounded to
+    // the activation type, stored at q as a [n, hidden] T tensor.
+    kNormOnly = 8,
 };
 
 // Workspace of the data-derived NVFP4 global scale: word 0 holds the bits of
@@ -336,6 +339,15 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
 #pragma unroll
         for (int j = 0; j < J; ++j) run_max = max_abs8(run_max, y[j]);
         if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
+    } else if constexpr (MODE == kNormOnly) {
+        (void)run_max;
+        uint4* yrow = reinterpret_cast<uint4*>(a.q) + (int64_t)row * a.chunks;
+        const int c0 = tid * J;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+            if (c0 + j < a.chunks)
+                st_stream(yrow + c0 + j, make_uint4(E::pack(y[j][0], y[j][1]), E::pack(y[j][2], y[j][3]),
+                                                    E::pack(y[j][4], y[j][5]), E::pack(y[j][6], y[j][7])));
     } else {
         (void)run_max;
         quantize_y<MODE, J>(a, row, y, sin, rtab, s_max, tid, nwarps, tid * J);
