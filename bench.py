@@ -178,7 +178,7 @@ def kernel_name(wl, mode: str, residual: bool, torch) -> str:
     m = rq.MODES["nvfp4" if mode == "nvfp4_dynamic" else mode]
     chunks = wl.hidden // 8
     if pipelined:
-        return f"pipe_entry<{e}, {m}, {int(residual)}, {2 if chunks <= 1024 else 4}>"
+        return f"pipe_entry<{e}, {m}, {int(residual)}, {2 if chunks <= 1024 else 4}, 1>"
     return f"rows_kernel<{e}, {m}, {int(residual)}, {1 if chunks <= 1024 else 2}>"
 
 

@@ -27,6 +27,14 @@
  *   then one of the quantisation modes below.  All fp32 arithmetic rounds to
  *   nearest even; results are bit-identical to that definition.
  *
+ * Besides that op (rmsq_fused_add_rmsnorm_quant and its variants) the library
+ * has: NVFP4 with the global scale taken from the data
+ * (rmsq_fused_add_rmsnorm_nvfp4_dynamic); scale options E8M0 and TMA-aligned
+ * column-major (RMSQ_QUANT_*); SiLU+Mul + quantisation (rmsq_silu_mul_quant,
+ * the same docs page's "SiLU+Mul + Quantization (fuse_act_quant)"); and the
+ * unfused two-op sequence the fusion replaces (rmsq_fused_add_rmsnorm,
+ * rmsq_quant).
+ *
  * Conventions for every entry point:
  *   - Pointers marked "device" must be addressable by the current CUDA device
  *     (cudaMalloc / torch CUDA tensors, or managed memory).  The caller owns
@@ -125,7 +133,7 @@ typedef enum {
  *               RMSNorm + quant: h = x, nothing is written to residual_out).
  *  weight       device, T[hidden], 16-byte aligned (same dtype as x).
  *  eps          finite, >= 0 (1e-5 and 1e-6 are the values the pages use).
- *  quant_mode   an rmsq_quant_mode.
+ *  quant_mode   an rmsq_quant_mode, optionally OR-ed with RMSQ_QUANT_* options.
  *  scale_in     device, one fp32: the static scale s (FP8_STATIC) or the global
  *               scale gs (NVFP4); ignored (may be NULL) for the dynamic FP8
  *               modes.  Its value must be finite and > 0; it is not checked.
@@ -277,7 +285,7 @@ int rmsq_quant(const void *y, int quant_mode, const float *scale_in, void *out_q
  * 1.2 ulp of e^x over the normal range); the division and products are
  * correctly rounded, so results are reproducible bit for bit.
  *  gate_up     device, [n_tokens, 2 d] bf16/fp16, row-major, 16-byte aligned.
- *  quant_mode  an rmsq_quant_mode.
+ *  quant_mode  an rmsq_quant_mode, optionally OR-ed with RMSQ_QUANT_* options.
  *  scale_in    device fp32: FP8 static scale or NVFP4 global scale (else
  *              ignored, may be NULL).
  *  out_q       device: [n, d] E4M3 bytes, or [n, d/2] E2M1 pairs for NVFP4.
