@@ -365,6 +365,16 @@ int rmsq_debug_convert(int kind, const float *in, uint8_t *out, int64_t n, void 
 int rmsq_debug_activation(int kind, const float *in, const float *in2, float *out, int64_t n,
                           void *stream);
 
+/*
+ * rmsq_debug_bounded_wait — failure detection without a fault: one CTA waits
+ * on a shared-memory barrier that nothing ever completes, with the same
+ * bounded wait the pipelined kernels use on their copies, here limited to
+ * limit_ns (1 .. 1e9).  *gave_up = 1 when every thread gave up and the kernel
+ * returned normally (the expected outcome), 0 if none did, 2 if only some
+ * did.  Synchronous (waits for the device); the context stays usable.
+ */
+int rmsq_debug_bounded_wait(int64_t limit_ns, int *gave_up);
+
 /* Text for an rmsq_status (static storage, never NULL). */
 const char *rmsq_status_string(int status);
 

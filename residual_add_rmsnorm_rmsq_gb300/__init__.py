@@ -52,7 +52,7 @@ EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
            "rmsq_fused_add_rmsnorm", "rmsq_quant",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
-           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation",
+           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
 
@@ -109,6 +109,8 @@ def load(path: str | None = None):
         L.rmsq_debug_convert.restype = ci
         L.rmsq_debug_activation.argtypes = [ci, vp, vp, vp, i64, vp]
         L.rmsq_debug_activation.restype = ci
+        L.rmsq_debug_bounded_wait.argtypes = [i64, ctypes.POINTER(ci)]
+        L.rmsq_debug_bounded_wait.restype = ci
         L.rmsq_status_string.argtypes = [ci]
         L.rmsq_status_string.restype = ctypes.c_char_p
         L.rmsq_last_cuda_error.argtypes = []
@@ -342,6 +344,15 @@ def debug_activation(kind: str, values: torch.Tensor, up: torch.Tensor | None = 
     if st:
         raise RmsqError(st, "rmsq_debug_activation")
     return out
+
+
+def debug_bounded_wait(limit_ns: int) -> int:
+    """Run the bounded-wait check (rmsq_debug_bounded_wait); returns gave_up."""
+    out = ctypes.c_int(-1)
+    st = load().rmsq_debug_bounded_wait(int(limit_ns), ctypes.byref(out))
+    if st:
+        raise RmsqError(st, "rmsq_debug_bounded_wait")
+    return out.value
 
 
 def debug_convert(kind: str, values: torch.Tensor, stream=None) -> torch.Tensor:

@@ -28,6 +28,33 @@ __global__ void debug_activation_kernel(int kind, const float* in, const float* 
     }
 }
 
+// The bounded mbarrier wait of the pipelined kernels, on a barrier that no
+// copy and no thread ever completes: every thread must give up after
+// `limit_ns` and the kernel must return normally, recording the outcome.
+static __device__ int g_wait_outcome;
+__global__ void debug_wait_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(&bar, 0u, limit_ns);
+    const int gave_up = __syncthreads_count(!ok);
+    if (threadIdx.x == 0) g_wait_outcome = gave_up == (int)blockDim.x ? 1 : (gave_up == 0 ? 0 : 2);
+}
+
+cudaError_t debug_bounded_wait(uint64_t limit_ns, int* outcome) {
+    const int unset = -1;
+    cudaError_t e = cudaMemcpyToSymbol(g_wait_outcome, &unset, sizeof(int));
+    if (e != cudaSuccess) return e;
+    debug_wait_kernel<<<1, 64>>>(limit_ns);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(outcome, g_wait_outcome, sizeof(int));
+    return e;
+}
+
 cudaError_t launch_debug_activation(int kind, const float* in, const float* in2, float* out, int64_t n,
                                     cudaStream_t stream) {
     const int64_t pairs = (n + 1) / 2;

@@ -485,6 +485,14 @@ int rmsq_debug_activation(int kind, const float* in, const float* in2, float* ou
     return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
 }
 
+int rmsq_debug_bounded_wait(int64_t limit_ns, int* gave_up) {
+    if (limit_ns <= 0 || limit_ns > 1000000000 || !gave_up) return RMSQ_ERR_INVALID_ARG;
+    const int st = check_device();
+    if (st != RMSQ_OK) return st;
+    const cudaError_t e = rmsq::debug_bounded_wait(static_cast<uint64_t>(limit_ns), gave_up);
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
 const char* rmsq_status_string(int status) {
     switch (status) {
     case RMSQ_OK: return "ok";

@@ -461,12 +461,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Wait for phase `parity` of `bar` to complete; gives up (returns false) after
 // kWaitLimitNs of wall time or 2^24 polls, whichever comes first.
 constexpr uint64_t kWaitLimitNs = 100ull * 1000 * 1000;
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0; i < (1u << 24); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((i & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }

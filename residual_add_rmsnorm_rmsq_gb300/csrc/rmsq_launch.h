@@ -54,6 +54,9 @@ cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);
 // batch amax word and the per-row inv_rms.
 cudaError_t launch_nvfp4_dynamic_bf16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
 cudaError_t launch_nvfp4_dynamic_fp16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);
+// One CTA waits on an mbarrier nothing completes, bounded by limit_ns;
+// *outcome: 1 every thread gave up, 0 none did, 2 some did.  Synchronous.
+cudaError_t debug_bounded_wait(uint64_t limit_ns, int* outcome);
 // The activation's e^x / silu / silu * u, elementwise (kind 0 / 1 / 2).
 cudaError_t launch_debug_activation(int kind, const float* in, const float* in2, float* out, int64_t n,
                                     cudaStream_t stream);
