@@ -341,6 +341,29 @@ class UnfusedBuffers:
         self.rq.quant(self.y[k], self.mode, self.scale_in, out_q=self.q[k], out_scales=self.sc[k], stream=stream)
 
 
+class QkBuffers:
+    """Rotating buffer sets for QK-norm + RoPE (in place on qkv)."""
+
+    def __init__(self, torch, rq, wl, min_total_bytes):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        n, D, nh = wl.n_tokens, wl.head_dim, wl.nq + wl.nkv
+        self.rq, self.wl = rq, wl
+        # q and k heads read and written, the position, the token's cos / sin row, the weights
+        self.bytes = n * (nh * D * 2 * 2 + 8 + D * 4) + 2 * D * 2
+        self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        q0 = torch.from_numpy(wl.qkv.view(np.int16)).view(tdt).cuda()
+        self.qkv = [q0 if i == 0 else q0.clone() for i in range(self.sets)]
+        self.pos = torch.from_numpy(wl.positions).cuda()
+        self.cs = torch.from_numpy(wl.cos_sin).cuda()
+        self.qw = torch.from_numpy(wl.q_weight.view(np.int16)).view(tdt).cuda()
+        self.kw = torch.from_numpy(wl.k_weight.view(np.int16)).view(tdt).cuda()
+
+    def launch(self, k, stream):
+        w = self.wl
+        self.rq.qk_norm_rope(self.qkv[k], self.pos, self.cs, self.qw, self.kw, w.eps, w.nq, w.nkv, w.head_dim,
+                             w.neox, stream=stream)
+
+
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
     """Mean device time per launch (ms) over exactly `steps` launches, CUDA
     events on `stream`.
@@ -592,9 +615,10 @@ def decode_sweep(torch, rq, stream, args):
 
 def sweep(torch, rq, stream, peak, args):
     """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of
-    peak), the unfused two-op sequence beside the fused op on two of them, and
-    SiLU+Mul + quantisation on a Llama-8B-shaped MLP activation (4096 tokens,
-    d = 14336)."""
+    peak), the unfused two-op sequence beside the fused op on two of them,
+    QK-norm + RoPE on a Qwen3-shaped attention input (4096 tokens, 32 + 4 + 4
+    heads of 128), and SiLU+Mul + quantisation on a Llama-8B-shaped MLP
+    activation (4096 tokens, d = 14336)."""
     import rmsq_inputs as ri
     out = {}
     groups = [
@@ -621,6 +645,14 @@ def sweep(torch, rq, stream, peak, args):
                                   "GB/s_moved": round(ub.bytes / (ms / 1e3) / 1e9, 1)}
         del ub, wl
         torch.cuda.empty_cache()
+    qk = ri.qwen_qk(4096)
+    qb = QkBuffers(torch, rq, qk, 4 * L2_BYTES + 1)
+    ms = time_launches(torch, rq, qk, None, qb, args.sweep_steps, 5, stream)
+    gbs = qb.bytes / (ms / 1e3) / 1e9
+    out["qwen_qk_norm_rope_4096"] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                     "tokens_per_s": round(qk.n_tokens / (ms / 1e3), 1), "bytes": qb.bytes}
+    del qb, qk
+    torch.cuda.empty_cache()
     act = ri.llama_mlp(4096)
     for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):
         name = f"llama_mlp_silu_mul_{mode}"

@@ -268,6 +268,32 @@ int rmsq_fused_add_rmsnorm(const void *x, const void *residual, const void *weig
 int rmsq_quant(const void *y, int quant_mode, const float *scale_in, void *out_q, void *out_scales,
                int64_t n_tokens, int64_t hidden, int dtype, void *stream);
 
+/*
+ * rmsq_qk_norm_rope — QK-norm + RoPE in one kernel (vLLM docs "Fusion
+ * torch.compile passes", section "QK Norm + RoPE (enable_qk_norm_rope_fusion)":
+ * split QKV, per-head RMSNorm of Q and K, rotary embedding), in place.
+ *  qkv            device, T[n_tokens, (num_q_heads + 2 num_kv_heads) head_dim]:
+ *                 per token the q heads, then the k heads, then the v heads;
+ *                 16-byte aligned; updated in place (v heads untouched).
+ *  positions      device, int64[n_tokens], 8-byte aligned: each token's position.
+ *  cos_sin_cache  device, fp32[max_positions, head_dim], 16-byte aligned: at
+ *                 row p, cos of the head_dim/2 angles then their sin.
+ *  q_weight, k_weight  device, T[head_dim], 16-byte aligned: the norm weights.
+ * Per q / k head: S = canonical pairwise sum of x^2 over the head,
+ * inv = 1 / sqrt(S / head_dim + eps), y = (x * inv) * w in fp32 (the norm op's
+ * steps); then with c_i, s_i from row positions[t] of the table, each pair
+ * (a, b) becomes (a c - b s, b c + a s) (every product and sum rounded to
+ * fp32 separately), rounded once to T.  is_neox = 1 pairs element i with
+ * i + head_dim/2, 0 pairs 2i with 2i + 1 (GPT-J); angle index i either way.
+ * A token whose position is outside [0, max_positions) is left unchanged.
+ * head_dim 64, 128 or 256 (else RMSQ_ERR_UNSUPPORTED_SHAPE); eps finite,
+ * >= 0; no input may overlap qkv.  Asynchronous on `stream`.
+ */
+int rmsq_qk_norm_rope(void *qkv, const int64_t *positions, const float *cos_sin_cache,
+                      int64_t max_positions, const void *q_weight, const void *k_weight, float eps,
+                      int64_t n_tokens, int num_q_heads, int num_kv_heads, int head_dim, int is_neox,
+                      int dtype, void *stream);
+
 /* Largest d (activation width) of rmsq_silu_mul_quant. */
 #define RMSQ_ACT_MAX_D 32768
 

@@ -123,6 +123,9 @@ def _configure(L):
     L.oracle_add_rmsnorm.restype = ctypes.c_int
     L.oracle_quant.argtypes = [vp, ctypes.c_int, f32, vp, vp, i64, i64, ctypes.c_int, ctypes.c_int]
     L.oracle_quant.restype = ctypes.c_int
+    L.oracle_qk_norm_rope.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    L.oracle_qk_norm_rope.restype = ctypes.c_int
     L.oracle_expf.argtypes, L.oracle_expf.restype = [f32], f32
     L.oracle_silu.argtypes, L.oracle_silu.restype = [f32], f32
     for name in ("oracle_expf_array", "oracle_silu_array"):
@@ -327,6 +330,20 @@ def run_quant(y_t, *, mode: str, scale_in: float = 0.0, dtype: str = "bf16", nth
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return {"q": q, "scales": scales, "residual_out": None}
+
+
+def run_qk_norm_rope(wl) -> np.ndarray:
+    """QK-norm + RoPE on a ``rmsq_inputs.QKWorkload``; returns the updated
+    qkv bit patterns (uint16 [n, (nq + 2 nkv) D])."""
+    qkv = np.ascontiguousarray(wl.qkv, np.uint16).copy()
+    pos = np.ascontiguousarray(wl.positions, np.int64)
+    cs = np.ascontiguousarray(wl.cos_sin, np.float32)
+    rc = lib().oracle_qk_norm_rope(_ptr(qkv), _ptr(pos), _ptr(cs), cs.shape[0], _ptr(wl.q_weight),
+                                   _ptr(wl.k_weight), ctypes.c_float(wl.eps), wl.n_tokens, wl.nq, wl.nkv,
+                                   wl.head_dim, 1 if wl.neox else 0, DTYPES[wl.dtype])
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return qkv
 
 
 def nvfp4_global_scale(y_amax: float) -> float:

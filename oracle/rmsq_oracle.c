@@ -60,6 +60,18 @@
  *      the first op writes y rounded to the activation type T (nearest even)
  *      and the updated residual; the second quantises that T tensor exactly
  *      as step 5 quantises y.
+ *  R20 QK-norm + RoPE (vLLM docs, same page, section "QK Norm + RoPE
+ *      (enable_qk_norm_rope_fusion)": split QKV, per-head RMSNorm of Q and K,
+ *      rotary embedding, in one kernel): each q and k head of a token row is
+ *      normalised like a row of the norm op (canonical sum over head_dim,
+ *      inv = 1/sqrt(S/D + eps), y = (x * inv) * w with the q or k weight),
+ *      kept in fp32, rotated with cos / sin taken from a caller-given fp32
+ *      table [max_pos, D] (cos in the first D/2 columns, sin in the rest) at
+ *      the token's position, each product and each sum rounded separately,
+ *      and written back in place rounded once to T; v is untouched.  NeoX
+ *      pairs element i with i + D/2, GPT-J pairs 2i with 2i+1 (both use
+ *      angle index i).  A token whose position is outside [0, max_pos) is
+ *      left unchanged.
  *  Parity unpinned: NaN / Inf inputs (IEEE propagation, not pinned by any test).
  */
 #include <math.h>
@@ -546,6 +558,49 @@ int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uin
     OracleArgs a = {gate_up, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
                     NULL, y_out, n, d, dtype, 1, NULL, e8m0, col_stride};
     return run_rows(&a, nthreads);
+}
+
+/* R20: QK-norm + RoPE, in place on qkv [n, (nq + 2 nkv) D] (q heads, then k
+ * heads, then v heads of each token).  Returns 0, or -1 on a bad argument. */
+static void norm_rope_head(uint16_t *head, const uint16_t *w, float eps, const float *cs, int D, int neox,
+                           int dtype, float *x, float *sq, float *buf, float *y)
+{
+    for (int i = 0; i < D; ++i) { x[i] = widen(dtype, head[i]); sq[i] = x[i] * x[i]; }
+    const float S = oracle_tree_sum_buf(sq, D, buf);
+    const float inv = 1.0f / sqrtf(S / (float)D + eps);
+    for (int i = 0; i < D; ++i) y[i] = (x[i] * inv) * widen(dtype, w[i]);
+    const int h = D / 2;
+    for (int i = 0; i < h; ++i) {
+        const float c = cs[i], s = cs[h + i];
+        const int a = neox ? i : 2 * i, b = neox ? i + h : 2 * i + 1;
+        const float ya = y[a], yb = y[b];
+        const float oa = ya * c - yb * s;
+        const float ob = yb * c + ya * s;
+        head[a] = narrow(dtype, oa);
+        head[b] = narrow(dtype, ob);
+    }
+}
+
+int oracle_qk_norm_rope(uint16_t *qkv, const int64_t *positions, const float *cos_sin, int64_t max_pos,
+                        const uint16_t *q_w, const uint16_t *k_w, float eps, int64_t n, int nq, int nkv, int D,
+                        int neox, int dtype)
+{
+    if (n < 0 || nq < 0 || nkv < 0 || D <= 0 || D % 2 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    if (!qkv || !positions || !cos_sin || !q_w || !k_w || max_pos <= 0) return -1;
+    float *tmp = (float *)malloc((size_t)D * 4 * sizeof(float) + 8 * sizeof(float) * (size_t)D);
+    if (!tmp) return -2;
+    float *x = tmp, *sq = tmp + D, *y = tmp + 2 * D, *buf = tmp + 3 * D;
+    const int64_t width = (int64_t)(nq + 2 * nkv) * D;
+    for (int64_t t = 0; t < n; ++t) {
+        const int64_t pos = positions[t];
+        if (pos < 0 || pos >= max_pos) continue;
+        const float *cs = cos_sin + pos * D;
+        for (int hd = 0; hd < nq + nkv; ++hd)
+            norm_rope_head(qkv + t * width + (int64_t)hd * D, hd < nq ? q_w : k_w, eps, cs, D, neox, dtype,
+                           x, sq, buf, y);
+    }
+    free(tmp);
+    return 0;
 }
 
 /* R19: the two ops of the unfused sequence.  oracle_add_rmsnorm writes y

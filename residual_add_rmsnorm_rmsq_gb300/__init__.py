@@ -50,7 +50,7 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
-           "rmsq_fused_add_rmsnorm", "rmsq_quant",
+           "rmsq_fused_add_rmsnorm", "rmsq_quant", "rmsq_qk_norm_rope",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
            "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
@@ -92,6 +92,8 @@ def load(path: str | None = None):
         L.rmsq_nvfp4_dynamic_workspace_bytes.restype = ctypes.c_size_t
         L.rmsq_fused_add_rmsnorm.argtypes = [vp, vp, vp, f32, vp, vp, i64, i64, ci, vp]
         L.rmsq_fused_add_rmsnorm.restype = ci
+        L.rmsq_qk_norm_rope.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ci, ci, ci, ci, ci, vp]
+        L.rmsq_qk_norm_rope.restype = ci
         L.rmsq_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
         L.rmsq_quant.restype = ci
         L.rmsq_silu_mul_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
@@ -236,6 +238,27 @@ def quant(y: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *, o
     if st:
         raise RmsqError(st, "rmsq_quant")
     return out_q, out_scales
+
+
+def qk_norm_rope(qkv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor, q_weight: torch.Tensor,
+                 k_weight: torch.Tensor, eps: float, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 is_neox: bool = True, stream=None) -> torch.Tensor:
+    """rmsq_qk_norm_rope on torch CUDA tensors, in place on qkv (returned)."""
+    L = load()
+    if qkv.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {qkv.dtype}")
+    for t in (qkv, positions, cos_sin_cache, q_weight, k_weight):
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    if positions.dtype != torch.int64 or cos_sin_cache.dtype != torch.float32:
+        raise TypeError("positions must be int64 and cos_sin_cache float32")
+    n = qkv.shape[0]
+    st = L.rmsq_qk_norm_rope(_p(qkv), _p(positions), _p(cos_sin_cache), cos_sin_cache.shape[0], _p(q_weight),
+                             _p(k_weight), ctypes.c_float(eps), n, num_q_heads, num_kv_heads, head_dim,
+                             1 if is_neox else 0, DTYPES[qkv.dtype], _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_qk_norm_rope")
+    return qkv
 
 
 def silu_mul_quant(gate_up: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *,

@@ -360,6 +360,50 @@ int rmsq_quant(const void* y, int quant_mode, const float* scale_in, void* out_q
     return RMSQ_OK;
 }
 
+int rmsq_qk_norm_rope(void* qkv, const int64_t* positions, const float* cos_sin_cache, int64_t max_positions,
+                      const void* q_weight, const void* k_weight, float eps, int64_t n_tokens, int num_q_heads,
+                      int num_kv_heads, int head_dim, int is_neox, int dtype, void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens < 0 || num_q_heads < 0 || num_kv_heads < 0 || num_q_heads + num_kv_heads == 0 ||
+        max_positions <= 0 || (is_neox != 0 && is_neox != 1))
+        return RMSQ_ERR_INVALID_ARG;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    if (num_q_heads > 4096 || num_kv_heads > 4096 ||
+        n_tokens * (num_q_heads + num_kv_heads) > static_cast<int64_t>(INT32_MAX))
+        return RMSQ_ERR_UNSUPPORTED_SHAPE;
+    if (n_tokens == 0) return RMSQ_OK;
+    if (!qkv || !positions || !cos_sin_cache || !q_weight || !k_weight) return RMSQ_ERR_INVALID_ARG;
+    if (!aligned(qkv, 16) || !aligned(positions, 8) || !aligned(cos_sin_cache, 16) || !aligned(q_weight, 16) ||
+        !aligned(k_weight, 16))
+        return RMSQ_ERR_ALIGNMENT;
+    const int64_t width = static_cast<int64_t>(num_q_heads + 2 * num_kv_heads) * head_dim;
+    const Span QKV = span(qkv, static_cast<size_t>(n_tokens * width) * 2);
+    const Span ins[4] = {span(positions, static_cast<size_t>(n_tokens) * 8),
+                         span(cos_sin_cache, static_cast<size_t>(max_positions * head_dim) * 4),
+                         span(q_weight, static_cast<size_t>(head_dim) * 2), span(k_weight, static_cast<size_t>(head_dim) * 2)};
+    for (const Span& i : ins)
+        if (overlaps(QKV, i)) return RMSQ_ERR_ALIAS;
+    const int st = check_device();
+    if (st != RMSQ_OK) return st;
+    rmsq::QkLaunch l;
+    l.qkv = qkv;
+    l.positions = positions;
+    l.cos_sin = cos_sin_cache;
+    l.max_pos = max_positions;
+    l.q_weight = q_weight;
+    l.k_weight = k_weight;
+    l.eps = eps;
+    l.n = static_cast<int>(n_tokens);
+    l.nq = num_q_heads;
+    l.nkv = num_kv_heads;
+    l.head_dim = head_dim;
+    l.neox = is_neox == 1;
+    l.fp16 = dtype == RMSQ_FP16;
+    const cudaError_t e = rmsq::launch_qk_norm_rope(l, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens) {
     return n_tokens < 0 ? 0 : rmsq::nvfp4_dynamic_workspace_bytes(n_tokens);
 }

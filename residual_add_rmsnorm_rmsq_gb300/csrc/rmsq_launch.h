@@ -66,6 +66,19 @@ cudaError_t launch_act_fp16(const LaunchArgs& a, cudaStream_t stream);
 // Quantisation of a T tensor: a.x = [n, d], a.hidden = d.
 cudaError_t launch_quant_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_quant_fp16(const LaunchArgs& a, cudaStream_t stream);
+// QK-norm + RoPE, in place on qkv.
+struct QkLaunch {
+    void* qkv;
+    const int64_t* positions;
+    const float* cos_sin;
+    int64_t max_pos;
+    const void* q_weight;
+    const void* k_weight;
+    float eps;
+    int n, nq, nkv, head_dim;
+    bool neox, fp16;
+};
+cudaError_t launch_qk_norm_rope(const QkLaunch& l, cudaStream_t stream);
 // Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
 inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
     const size_t raw = 256 + 4 * static_cast<size_t>(n);

@@ -1,0 +1,20 @@
+// bf16 and fp16 instantiations of the QK-norm + RoPE kernel.
+#include "rmsq_qk.cuh"
+
+namespace rmsq {
+cudaError_t launch_qk_norm_rope(const QkLaunch& l, cudaStream_t stream) {
+    QkArgs a;
+    a.qkv = static_cast<uint32_t*>(l.qkv);
+    a.pos = l.positions;
+    a.cs = l.cos_sin;
+    a.max_pos = l.max_pos;
+    a.qw = static_cast<const uint32_t*>(l.q_weight);
+    a.kw = static_cast<const uint32_t*>(l.k_weight);
+    a.eps = l.eps;
+    a.inv_d = 1.0f / (float)l.head_dim;
+    a.n = l.n;
+    a.nq = l.nq;
+    a.nkv = l.nkv;
+    return l.fp16 ? launch_qk<Fp16T>(a, l.head_dim, l.neox, stream) : launch_qk<Bf16T>(a, l.head_dim, l.neox, stream);
+}
+}  // namespace rmsq

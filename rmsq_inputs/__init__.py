@@ -37,6 +37,7 @@ _CHUNK = 1 << 22
 # stream ids: one independent stream per tensor / purpose
 STREAM_X, STREAM_RES, STREAM_W, STREAM_OUTLIER, STREAM_AUX = 1, 2, 3, 4, 5
 STREAM_GATE, STREAM_UP = 6, 7
+STREAM_QKV, STREAM_POS = 8, 9
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -239,3 +240,54 @@ def make_act_workload(name: str, n_tokens: int, d: int, *, dtype: str = "bf16",
 def llama_mlp(n_tokens: int = 4096, seed: int = 0) -> ActWorkload:
     """Llama-8B-shaped MLP activation: d = 14336 (gate_up [n, 28672]) bf16."""
     return make_act_workload(f"llama_mlp_{n_tokens}x14336", n_tokens, 14336, seed=seed)
+
+
+# ----------------------------------------------------------------------------
+# QK-norm + RoPE (per-head RMSNorm of Q and K before the rotary embedding).
+# ----------------------------------------------------------------------------
+
+@dataclass
+class QKWorkload:
+    """qkv [n, (nq + 2 nkv) D] bit patterns (q heads, k heads, v heads per
+    token), per-token positions, the fp32 cos / sin table [max_pos, D] (cos in
+    the first D/2 columns, sin in the rest) and the q / k norm weights [D]."""
+    name: str
+    n_tokens: int
+    nq: int
+    nkv: int
+    head_dim: int
+    dtype: str
+    eps: float
+    neox: bool
+    qkv: np.ndarray
+    positions: np.ndarray
+    cos_sin: np.ndarray
+    q_weight: np.ndarray
+    k_weight: np.ndarray
+
+
+def rope_table(max_pos: int, head_dim: int, theta: float = 1e6) -> np.ndarray:
+    """cos / sin of pos * theta^(-2i/D), i < D/2, computed in float64 and
+    rounded to fp32 (an input of the op, like a model's cached table)."""
+    half = head_dim // 2
+    inv_freq = theta ** (-np.arange(half, dtype=np.float64) * 2.0 / head_dim)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def make_qk_workload(name: str, n_tokens: int, nq: int = 32, nkv: int = 4, head_dim: int = 128, *,
+                     dtype: str = "bf16", neox: bool = True, max_pos: int = 8192, eps: float = 1e-6,
+                     sigma: float = 1.0, seed: int = 0) -> QKWorkload:
+    """qkv ~ sigma * N(0,1), positions uniform in [0, max_pos), weights 1 + 0.1 N(0,1)."""
+    n, width = int(n_tokens), (nq + 2 * nkv) * head_dim
+    qkv = to_bits(normal(seed, STREAM_QKV, n * width) * sigma, dtype).reshape(n, width)
+    pos = np.minimum((uniform(seed, STREAM_POS, n) * max_pos).astype(np.int64), max_pos - 1)
+    qw = to_bits(1.0 + 0.1 * normal(seed, STREAM_W, head_dim), dtype)
+    kw = to_bits(1.0 + 0.1 * normal(seed, STREAM_AUX, head_dim), dtype)
+    return QKWorkload(name, n, nq, nkv, head_dim, dtype, float(eps), neox, qkv, pos,
+                      rope_table(max_pos, head_dim), qw, kw)
+
+
+def qwen_qk(n_tokens: int = 4096, seed: int = 0) -> QKWorkload:
+    """Qwen3-30B-A3B attention input: 32 q heads, 4 kv heads, head_dim 128, bf16, NeoX rotary."""
+    return make_qk_workload(f"qwen_qk_{n_tokens}", n_tokens, 32, 4, 128, seed=seed)

@@ -26,6 +26,11 @@ MUTANTS = [
     ("col_stored_row_major", "if (col) sc_out[g * a->col_stride + t] = sc;", "if (col) sc_out[t * (H / G) + g] = sc;"),
     ("e8m0_rounds_down", "return f == 0.5f ? x : ldexpf(1.0f, k);", "return ldexpf(1.0f, k - 1);"),
     ("tma_stride_not_padded", "*col_stride = (opts & OR_OPT_TMA) ? (n + 3) / 4 * 4 : n;", "*col_stride = n;"),
+    # QK-norm + RoPE (pinned by test_oracle_qk.py)
+    ("rope_sin_sign", "const float oa = ya * c - yb * s;", "const float oa = ya * c + yb * s;"),
+    ("rope_cos_sin_swapped", "const float c = cs[i], s = cs[h + i];", "const float s = cs[i], c = cs[h + i];"),
+    ("rope_pair_offset", "b = neox ? i + h : 2 * i + 1;", "b = neox ? (i + h + 1) % (2 * h) : 2 * i + 1;"),
+    ("qk_k_heads_use_q_weight", "hd < nq ? q_w : k_w", "q_w"),
     ("group_of_first_half", "for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));",
      "for (int k = 0; k < G / 2; ++k) amax = fmaxf(amax, fabsf(yg[k]));"),
     ("nibbles_swapped", "(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
@@ -71,7 +76,8 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
                         os.path.join(ROOT, "tests", "test_oracle_formats.py"),
                         os.path.join(ROOT, "tests", "test_oracle_op.py"),
                         os.path.join(ROOT, "tests", "test_oracle_act.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_scale_options.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_scale_options.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_qk.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout, r.stdout[-2000:]
