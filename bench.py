@@ -361,7 +361,7 @@ class QkBuffers:
     def launch(self, k, stream):
         w = self.wl
         self.rq.qk_norm_rope(self.qkv[k], self.pos, self.cs, self.qw, self.kw, w.eps, w.nq, w.nkv, w.head_dim,
-                             w.neox, stream=stream)
+                             w.neox, stream=stream, variant=VARIANT)
 
 
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
@@ -645,14 +645,16 @@ def sweep(torch, rq, stream, peak, args):
                                   "GB/s_moved": round(ub.bytes / (ms / 1e3) / 1e9, 1)}
         del ub, wl
         torch.cuda.empty_cache()
-    qk = ri.qwen_qk(4096)
-    qb = QkBuffers(torch, rq, qk, 4 * L2_BYTES + 1)
-    ms = time_launches(torch, rq, qk, None, qb, args.sweep_steps, 5, stream)
-    gbs = qb.bytes / (ms / 1e3) / 1e9
-    out["qwen_qk_norm_rope_4096"] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                     "tokens_per_s": round(qk.n_tokens / (ms / 1e3), 1), "bytes": qb.bytes}
-    del qb, qk
-    torch.cuda.empty_cache()
+    for n_qk in (4096, 16384):
+        qk = ri.qwen_qk(n_qk)
+        qb = QkBuffers(torch, rq, qk, 4 * L2_BYTES + 1)
+        ms = time_launches(torch, rq, qk, None, qb, args.sweep_steps, 5, stream)
+        gbs = qb.bytes / (ms / 1e3) / 1e9
+        out[f"qwen_qk_norm_rope_{n_qk}"] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
+                                           "frac": round(gbs / peak, 4),
+                                           "tokens_per_s": round(qk.n_tokens / (ms / 1e3), 1), "bytes": qb.bytes}
+        del qb, qk
+        torch.cuda.empty_cache()
     act = ri.llama_mlp(4096)
     for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):
         name = f"llama_mlp_silu_mul_{mode}"

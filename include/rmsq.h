@@ -33,7 +33,9 @@
  * column-major (RMSQ_QUANT_*); SiLU+Mul + quantisation (rmsq_silu_mul_quant,
  * the same docs page's "SiLU+Mul + Quantization (fuse_act_quant)"); and the
  * unfused two-op sequence the fusion replaces (rmsq_fused_add_rmsnorm,
- * rmsq_quant).
+ * rmsq_quant); and QK-norm + RoPE on the attention input
+ * (rmsq_qk_norm_rope, the docs page's "QK Norm + RoPE
+ * (enable_qk_norm_rope_fusion)").
  *
  * Conventions for every entry point:
  *   - Pointers marked "device" must be addressable by the current CUDA device
@@ -294,6 +296,22 @@ int rmsq_qk_norm_rope(void *qkv, const int64_t *positions, const float *cos_sin_
                       int64_t n_tokens, int num_q_heads, int num_kv_heads, int head_dim, int is_neox,
                       int dtype, void *stream);
 
+/*
+ * rmsq_qk_norm_rope_ex — rmsq_qk_norm_rope with an explicit rmsq_variant
+ * (RMSQ_ERR_INVALID_ARG for any other value); bit-identical results either
+ * way.  DIRECT: each warp loads its heads straight into registers (lowest
+ * latency for a few tokens).  PIPELINED: persistent CTAs keep the q and k
+ * heads and the cos / sin rows of several tokens in flight as bulk
+ * asynchronous copies into shared memory; it needs two tokens' q and k heads
+ * plus their cos / sin rows within the shared-memory ring (about 110 KB per
+ * CTA) and runs as DIRECT where they do not fit.  AUTO: PIPELINED from eight
+ * tokens per SM up.
+ */
+int rmsq_qk_norm_rope_ex(void *qkv, const int64_t *positions, const float *cos_sin_cache,
+                         int64_t max_positions, const void *q_weight, const void *k_weight, float eps,
+                         int64_t n_tokens, int num_q_heads, int num_kv_heads, int head_dim, int is_neox,
+                         int dtype, void *stream, int variant);
+
 /* Largest d (activation width) of rmsq_silu_mul_quant. */
 #define RMSQ_ACT_MAX_D 32768
 
@@ -356,8 +374,9 @@ int rmsq_set_programmatic_launch(int enable);
 
 /*
  * rmsq_take_fault_flags — reads and clears, on the current device, the flag a
- * pipelined launch sets if it ever gives up waiting (after 100 ms) for its
- * own shared-memory copies; the outputs of such a launch are incomplete.
+ * pipelined launch (norm or QK-norm + RoPE) sets if it ever gives up
+ * waiting (after 100 ms) for its own shared-memory copies; the outputs of
+ * such a launch are incomplete.
  * *flags = 0 when no launch gave up.  Synchronous with respect to the device:
  * call it after the launches of interest have completed.
  */

@@ -50,7 +50,7 @@ VARIANTS = {"auto": 0, "direct": 1, "pipelined": 2}
 EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
-           "rmsq_fused_add_rmsnorm", "rmsq_quant", "rmsq_qk_norm_rope",
+           "rmsq_fused_add_rmsnorm", "rmsq_quant", "rmsq_qk_norm_rope", "rmsq_qk_norm_rope_ex",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
            "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
@@ -70,14 +70,14 @@ _lib = None
 
 
 def load(path: str | None = None):
-    """Load librmsq.so (built by ``__graft_entry__.build()``)."""
+    """Load librmsq.so (built by ``residual_add_rmsnorm_rmsq_gb300._build.build()``)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
         p = path or LIB_PATH
         if not os.path.exists(p):
-            raise RuntimeError(f"librmsq.so not built ({p}); run __graft_entry__.build()")
+            raise RuntimeError(f"librmsq.so not built ({p}); run residual_add_rmsnorm_rmsq_gb300._build.build()")
         L = ctypes.CDLL(p)
         vp, i64, f32, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
         L.rmsq_fused_add_rmsnorm_quant.argtypes = [vp, vp, vp, f32, ci, vp, vp, vp, vp, i64, i64, ci, vp]
@@ -94,6 +94,8 @@ def load(path: str | None = None):
         L.rmsq_fused_add_rmsnorm.restype = ci
         L.rmsq_qk_norm_rope.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ci, ci, ci, ci, ci, vp]
         L.rmsq_qk_norm_rope.restype = ci
+        L.rmsq_qk_norm_rope_ex.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ci, ci, ci, ci, ci, vp, ci]
+        L.rmsq_qk_norm_rope_ex.restype = ci
         L.rmsq_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
         L.rmsq_quant.restype = ci
         L.rmsq_silu_mul_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
@@ -242,8 +244,9 @@ def quant(y: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *, o
 
 def qk_norm_rope(qkv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torch.Tensor, q_weight: torch.Tensor,
                  k_weight: torch.Tensor, eps: float, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 is_neox: bool = True, stream=None) -> torch.Tensor:
-    """rmsq_qk_norm_rope on torch CUDA tensors, in place on qkv (returned)."""
+                 is_neox: bool = True, stream=None, variant: str = "auto") -> torch.Tensor:
+    """rmsq_qk_norm_rope_ex on torch CUDA tensors, in place on qkv (returned);
+    variant "auto", "direct" or "pipelined" (bit-identical results)."""
     L = load()
     if qkv.dtype not in DTYPES:
         raise TypeError(f"unsupported activation dtype {qkv.dtype}")
@@ -253,11 +256,12 @@ def qk_norm_rope(qkv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torc
     if positions.dtype != torch.int64 or cos_sin_cache.dtype != torch.float32:
         raise TypeError("positions must be int64 and cos_sin_cache float32")
     n = qkv.shape[0]
-    st = L.rmsq_qk_norm_rope(_p(qkv), _p(positions), _p(cos_sin_cache), cos_sin_cache.shape[0], _p(q_weight),
-                             _p(k_weight), ctypes.c_float(eps), n, num_q_heads, num_kv_heads, head_dim,
-                             1 if is_neox else 0, DTYPES[qkv.dtype], _stream(stream))
+    st = L.rmsq_qk_norm_rope_ex(_p(qkv), _p(positions), _p(cos_sin_cache), cos_sin_cache.shape[0],
+                                _p(q_weight), _p(k_weight), ctypes.c_float(eps), n, num_q_heads, num_kv_heads,
+                                head_dim, 1 if is_neox else 0, DTYPES[qkv.dtype], _stream(stream),
+                                VARIANTS[variant])
     if st:
-        raise RmsqError(st, "rmsq_qk_norm_rope")
+        raise RmsqError(st, "rmsq_qk_norm_rope_ex")
     return qkv
 
 

@@ -360,10 +360,12 @@ int rmsq_quant(const void* y, int quant_mode, const float* scale_in, void* out_q
     return RMSQ_OK;
 }
 
-int rmsq_qk_norm_rope(void* qkv, const int64_t* positions, const float* cos_sin_cache, int64_t max_positions,
-                      const void* q_weight, const void* k_weight, float eps, int64_t n_tokens, int num_q_heads,
-                      int num_kv_heads, int head_dim, int is_neox, int dtype, void* stream) {
+int rmsq_qk_norm_rope_ex(void* qkv, const int64_t* positions, const float* cos_sin_cache, int64_t max_positions,
+                         const void* q_weight, const void* k_weight, float eps, int64_t n_tokens, int num_q_heads,
+                         int num_kv_heads, int head_dim, int is_neox, int dtype, void* stream, int variant) {
     if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (variant != RMSQ_VARIANT_AUTO && variant != RMSQ_VARIANT_DIRECT && variant != RMSQ_VARIANT_PIPELINED)
+        return RMSQ_ERR_INVALID_ARG;
     if (n_tokens < 0 || num_q_heads < 0 || num_kv_heads < 0 || num_q_heads + num_kv_heads == 0 ||
         max_positions <= 0 || (is_neox != 0 && is_neox != 1))
         return RMSQ_ERR_INVALID_ARG;
@@ -400,8 +402,17 @@ int rmsq_qk_norm_rope(void* qkv, const int64_t* positions, const float* cos_sin_
     l.head_dim = head_dim;
     l.neox = is_neox == 1;
     l.fp16 = dtype == RMSQ_FP16;
+    l.variant = variant == RMSQ_VARIANT_DIRECT ? rmsq::kVariantDirect
+                : variant == RMSQ_VARIANT_PIPELINED ? rmsq::kVariantPipelined : rmsq::kVariantAuto;
     const cudaError_t e = rmsq::launch_qk_norm_rope(l, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
+int rmsq_qk_norm_rope(void* qkv, const int64_t* positions, const float* cos_sin_cache, int64_t max_positions,
+                      const void* q_weight, const void* k_weight, float eps, int64_t n_tokens, int num_q_heads,
+                      int num_kv_heads, int head_dim, int is_neox, int dtype, void* stream) {
+    return rmsq_qk_norm_rope_ex(qkv, positions, cos_sin_cache, max_positions, q_weight, k_weight, eps, n_tokens,
+                                num_q_heads, num_kv_heads, head_dim, is_neox, dtype, stream, RMSQ_VARIANT_AUTO);
 }
 
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens) {
@@ -484,11 +495,12 @@ int rmsq_take_fault_flags(uint32_t* flags) {
     if (!flags) return RMSQ_ERR_INVALID_ARG;
     const int st = check_device();
     if (st != RMSQ_OK) return st;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     cudaError_t e = rmsq::take_pipe_fault_bf16(&a);
     if (e == cudaSuccess) e = rmsq::take_pipe_fault_fp16(&b);
+    if (e == cudaSuccess) e = rmsq::take_pipe_fault_qk(&c);
     if (e != cudaSuccess) return fail_cuda(e);
-    *flags = a | b;
+    *flags = a | b | c;
     return RMSQ_OK;
 }
 

@@ -77,6 +77,7 @@ struct QkLaunch {
     float eps;
     int n, nq, nkv, head_dim;
     bool neox, fp16;
+    int variant;   // kVariantAuto / kVariantDirect / kVariantPipelined
 };
 cudaError_t launch_qk_norm_rope(const QkLaunch& l, cudaStream_t stream);
 // Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
@@ -88,6 +89,7 @@ inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
 // Read and clear the pipelined kernels' fault flags (current device).
 cudaError_t take_pipe_fault_bf16(unsigned int* out);
 cudaError_t take_pipe_fault_fp16(unsigned int* out);
+cudaError_t take_pipe_fault_qk(unsigned int* out);
 cudaError_t launch_convert(int kind, const float* in, uint8_t* out, int64_t n, cudaStream_t stream);
 
 }  // namespace rmsq

@@ -1,4 +1,5 @@
-// bf16 and fp16 instantiations of the QK-norm + RoPE kernel.
+// bf16 and fp16 instantiations of the QK-norm + RoPE kernels (warp and
+// pipelined forms).
 #include "rmsq_qk.cuh"
 
 namespace rmsq {
@@ -15,6 +16,8 @@ cudaError_t launch_qk_norm_rope(const QkLaunch& l, cudaStream_t stream) {
     a.n = l.n;
     a.nq = l.nq;
     a.nkv = l.nkv;
-    return l.fp16 ? launch_qk<Fp16T>(a, l.head_dim, l.neox, stream) : launch_qk<Bf16T>(a, l.head_dim, l.neox, stream);
+    return l.fp16 ? launch_qk<Fp16T>(a, l.head_dim, l.neox, l.variant, stream)
+                  : launch_qk<Bf16T>(a, l.head_dim, l.neox, l.variant, stream);
 }
+cudaError_t take_pipe_fault_qk(unsigned int* out) { return take_pipe_fault(out); }
 }  // namespace rmsq

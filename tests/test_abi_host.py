@@ -166,6 +166,34 @@ def test_nvfp4_dynamic_argument_errors(L):
         assert dyn() == rq.ERR_NO_DEVICE
 
 
+def test_qk_norm_rope_argument_errors(L):
+    vp = ctypes.c_void_p
+    Q, P_, CS, W1, W2 = 0x60000000, 0x61000000, 0x62000000, 0x63000000, 0x64000000
+
+    def qk(qkv=Q, pos=P_, cs=CS, mp=64, qw=W1, kw=W2, eps=1e-6, n=4, nq=2, nkv=1, D=128, neox=1, dt=0, v=0):
+        return L.rmsq_qk_norm_rope_ex(vp(qkv) if qkv else None, vp(pos) if pos else None,
+                                      vp(cs) if cs else None, mp, vp(qw) if qw else None,
+                                      vp(kw) if kw else None, ctypes.c_float(eps), n, nq, nkv, D, neox, dt,
+                                      None, v)
+
+    assert qk(v=3) == rq.ERR_INVALID_ARG and qk(v=-1) == rq.ERR_INVALID_ARG
+    assert qk(dt=2) == rq.ERR_INVALID_ARG
+    assert qk(neox=2) == rq.ERR_INVALID_ARG
+    assert qk(nq=0, nkv=0) == rq.ERR_INVALID_ARG
+    assert qk(mp=0) == rq.ERR_INVALID_ARG
+    assert qk(eps=float("nan")) == rq.ERR_INVALID_ARG
+    assert qk(D=96) == rq.ERR_UNSUPPORTED_SHAPE
+    assert qk(nq=5000) == rq.ERR_UNSUPPORTED_SHAPE
+    assert qk(qkv=0) == rq.ERR_INVALID_ARG
+    assert qk(qkv=Q + 8) == rq.ERR_ALIGNMENT
+    assert qk(pos=P_ + 4) == rq.ERR_ALIGNMENT
+    assert qk(cs=Q + 256) == rq.ERR_ALIAS                   # table inside qkv
+    assert qk(n=0, qkv=0, pos=0, cs=0, qw=0, kw=0) == rq.OK
+    if not torch.cuda.is_available():
+        for v in (0, 1, 2):
+            assert qk(v=v) == rq.ERR_NO_DEVICE
+
+
 def test_process_wide_switches(L):
     """The tuning switches only store settings: valid values are accepted,
     others rejected, and the defaults are put back."""
