@@ -10,8 +10,9 @@ Prints ONE JSON line (rank 0).  ``value`` is algorithmic HBM GB/s (bytes the
 op must move / device time), whole job over all ranks.  Inputs are resident in
 HBM before the timed region; consecutive steps rotate over buffer sets whose
 total size is more than 4x the L2 cache, so no step reads the previous step's
-data from L2.  ``e2e`` is the same metric with the inputs copied from pinned
-host memory and the outputs read back inside the timed region.
+data from L2.  ``e2e`` is the same metric with every step's inputs copied from
+pinned host memory and its outputs read back inside the timed region (copies
+in, launches and copies out pipelined on three streams).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -408,9 +409,14 @@ def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
 
 
 def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
-    """Same op through the public API with host buffers: pinned host -> device
-    copies of x and residual, the launch, device -> pinned host copies of
-    codes, scales and residual_out, all inside the timed region."""
+    """Same op through the public API with host buffers: every step copies its
+    inputs (x, residual) from pinned host memory to the device, launches, and
+    copies its results (codes, scales, residual_out) back to pinned host
+    memory, all inside the timed region.  The steps are pipelined the way a
+    serving loop would run them: host-to-device copies on one stream, the
+    launches on `stream`, device-to-host copies on a third, over two device
+    buffer sets ordered by events, so that step k+1's inputs travel while
+    step k's results come back (the link is full duplex)."""
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
     hx = torch.from_numpy(wl.x.view(np.int16)).view(tdt).pin_memory()
     hr = None if wl.residual is None else torch.from_numpy(wl.residual.view(np.int16)).view(tdt).pin_memory()
@@ -420,28 +426,48 @@ def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
     h2d = hx.numel() * 2 + (0 if hr is None else hr.numel() * 2)
     d2h = hq.numel() + (0 if hs is None else hs.numel() * hs.element_size()) + \
         (0 if hro is None else hro.numel() * 2)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    nb = min(2, bufs.sets)
+    in_free = [None] * nb    # launch that last read set b's inputs
+    out_free = [None] * nb   # copy-out that last read set b's results
 
-    def step():
-        bufs.x[0].copy_(hx, non_blocking=True)
-        if hr is not None:
-            bufs.r[0].copy_(hr, non_blocking=True)
-        bufs.launch(0, stream)
-        hq.copy_(bufs.q[0], non_blocking=True)
-        if hs is not None:
-            hs.copy_(bufs.sc[0], non_blocking=True)
-        if hro is not None:
-            hro.copy_(bufs.ro[0], non_blocking=True)
+    def step(k):
+        b = k % nb
+        with torch.cuda.stream(s_in):
+            if in_free[b] is not None:
+                s_in.wait_event(in_free[b])
+            bufs.x[b].copy_(hx, non_blocking=True)
+            if hr is not None:
+                bufs.r[b].copy_(hr, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        stream.wait_event(ev_in)
+        if out_free[b] is not None:
+            stream.wait_event(out_free[b])
+        bufs.launch(b, stream)
+        ev_k = torch.cuda.Event()
+        ev_k.record(stream)
+        in_free[b] = ev_k
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_k)
+            hq.copy_(bufs.q[b], non_blocking=True)
+            if hs is not None:
+                hs.copy_(bufs.sc[b], non_blocking=True)
+            if hro is not None:
+                hro.copy_(bufs.ro[b], non_blocking=True)
+            ev_o = torch.cuda.Event()
+            ev_o.record(s_out)
+        out_free[b] = ev_o
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+    for k in range(3):
+        step(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)              # before the first copy-in: everything timed depends on it
+    for k in range(steps):
+        step(k)
+    e1.record(s_out)             # after the last copy-out, which waits for everything before it
+    torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     return ms, h2d, d2h
 

@@ -350,11 +350,12 @@ int rmsq_silu_mul_quant(const void *gate_up, int quant_mode, const float *scale_
  * (rows in flight per CTA: 1..8) and ctas_per_sm (cap on resident CTAs per
  * SM: 1..8) and rows_per_iter (rows a CTA works on together: 1 or 2; two
  * share each block reduction's barrier).  0 keeps the automatic choice for
- * that parameter.  A choice that
- * does not fit the row (more than 512 threads, or a ring larger than the
- * shared memory budget) falls back to the automatic one.  Results do not
- * depend on these settings.  Not synchronised with launches running
- * concurrently on other host threads.
+ * that parameter.  The pipelined QK-norm + RoPE kernel takes stages (tokens
+ * in flight per CTA, 2..8) and ctas_per_sm from the same settings.  A choice
+ * that does not fit (more than 512 threads, or a ring larger than the shared
+ * memory budget) falls back to the automatic one.  Results do not depend on
+ * these settings.  Not synchronised with launches running concurrently on
+ * other host threads.
  */
 int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm, int rows_per_iter);
 
