@@ -269,14 +269,19 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
 }
 
-// NVFP4 with a data-derived global scale: zero the workspace's amax word,
-// pass 1 (row kernel, mode kNormAmax, in the requested variant), pass 2
-// (block quantisation).  Both are launched with programmatic dependent launch
-// when it is on, so pass 2's launch overlaps the end of pass 1.
+// NVFP4 with a data-derived global scale: zero the workspace's amax word
+// (a one-thread kernel), pass 1 (row kernel, mode kNormAmax, in the requested
+// variant), pass 2 (block quantisation).  All three are launched with
+// programmatic dependent launch when it is on, so each launch overlaps the
+// end of the kernel before it; each waits for that kernel before touching
+// memory.
 template <class E>
 cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* out_gs,
                                  cudaStream_t stream) {
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(unsigned int), stream);
+    unsigned int* amax_word = static_cast<unsigned int*>(workspace);
+    void* zparams[] = {&amax_word};
+    cudaError_t e = launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_zero_kernel), dim3(1), dim3(32),
+                                  zparams, 0, stream);
     if (e != cudaSuccess) return e;
     LaunchArgs first = la;
     first.mode = kNormAmax;

@@ -114,6 +114,17 @@ __device__ __forceinline__ void nvfp4_dyn_blocks(const uint4* h, const uint4* w,
 // gs = 2688 / amax, 1 when the batch amax is 0.
 __device__ __forceinline__ float nvfp4_dyn_gs(float amax) { return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f; }
 
+// Zeroes the workspace's amax word before pass 1.  A kernel rather than a
+// memset so that it joins the chain of programmatic dependent launches: it
+// may be scheduled while the preceding kernel finishes, waits for it (an
+// earlier call's pass 2 may still read the word) and lets pass 1 launch
+// early in turn.  A memset in its place cost ~3.8 us per call on GB300.
+static __global__ void __launch_bounds__(32) nvfp4_dyn_zero_kernel(unsigned int* amax_word) {
+    allow_dependents();
+    grid_dependency_wait();
+    if (threadIdx.x == 0) *amax_word = 0u;
+}
+
 // Pass 2 as its own kernel, launched after pass 1.
 template <class E>
 __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, const uint4* w,
