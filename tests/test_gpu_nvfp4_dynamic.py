@@ -140,11 +140,13 @@ def test_graph_replay_resets_the_workspace(variant):
         P.compare(got, want, "nvfp4", f"graph replay {wl.name}/{variant}")
 
 
+@pytest.mark.parametrize("pdl", [True, False], ids=["pdl", "plain"])
 @pytest.mark.parametrize("variant", ["auto", "direct"])
-def test_back_to_back_calls_share_a_workspace(variant):
+def test_back_to_back_calls_share_a_workspace(variant, pdl):
     """Three calls queued on one stream with one workspace and no host
-    synchronisation between them: each call's zeroing of the amax word must
-    wait for the previous call's second pass to have read it."""
+    synchronisation between them, with and without programmatic dependent
+    launch: each call's zeroing of the amax word must wait for the previous
+    call's second pass to have read it."""
     wls = [ri.make_workload(f"b2b{i}", 4096, 2048, res_sigma=0.5 + i, seed=500 + i) for i in range(3)]
     ws = torch.full((rq.nvfp4_dynamic_workspace_bytes(4096),), 0x7F, dtype=torch.uint8, device="cuda")
     ins = [(P.dev_act(wl.x, wl.dtype), P.dev_act(wl.residual, wl.dtype), P.dev_act(wl.weight, wl.dtype))
@@ -152,9 +154,14 @@ def test_back_to_back_calls_share_a_workspace(variant):
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
     outs = []
-    for wl, (x, r, w) in zip(wls, ins):
-        outs.append(rq.fused_add_rmsnorm_nvfp4_dynamic(x, r, w, wl.eps, workspace=ws, stream=s, variant=variant))
-    torch.cuda.synchronize()
+    rq.set_programmatic_launch(pdl)
+    try:
+        for wl, (x, r, w) in zip(wls, ins):
+            outs.append(rq.fused_add_rmsnorm_nvfp4_dynamic(x, r, w, wl.eps, workspace=ws, stream=s,
+                                                           variant=variant))
+        torch.cuda.synchronize()
+    finally:
+        rq.set_programmatic_launch(True)
     assert rq.take_fault_flags() == 0
     for wl, (q, sc, gs, ro) in zip(wls, outs):
         want = oracle.run_nvfp4_dynamic(wl.x, wl.residual, wl.weight, eps=wl.eps, dtype=wl.dtype, nthreads=8)
