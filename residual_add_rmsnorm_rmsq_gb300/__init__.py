@@ -38,7 +38,15 @@ OPTIONS = {"e8m0": 0x10, "tma": 0x20}
 def mode_code(mode: str) -> int:
     """The C quant_mode argument for a mode name with optional "+e8m0" / "+tma"."""
     base, *opts = mode.split("+")
+    if base not in MODES or any(o not in OPTIONS for o in opts):
+        raise ValueError(f"unknown quant mode {mode!r}")
     return MODES[base] | sum(OPTIONS[o] for o in opts)
+
+
+def _variant(variant: str) -> int:
+    if variant not in VARIANTS:
+        raise ValueError(f"unknown variant {variant!r} (one of {', '.join(VARIANTS)})")
+    return VARIANTS[variant]
 
 
 # rmsq_dtype
@@ -182,6 +190,7 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     ``variant``: "auto", "direct" or "pipelined" (identical results).
     Returns (q, scales, residual_out).
     """
+    vcode = _variant(variant)
     L = load()
     n, H = x.shape
     if x.dtype not in DTYPES:
@@ -198,7 +207,7 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     st = L.rmsq_fused_add_rmsnorm_quant_ex(_p(x), _p(residual), _p(weight), ctypes.c_float(eps),
                                            mode_code(mode), _p(scale_in), _p(out_q), _p(out_scales),
                                            _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream),
-                                           VARIANTS[variant])
+                                           vcode)
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
@@ -212,6 +221,9 @@ def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, weight: to
     n, H = x.shape
     if x.dtype not in DTYPES:
         raise TypeError(f"unsupported activation dtype {x.dtype}")
+    for t in (x, residual, weight, y_out, residual_out):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
     if y_out is None:
         y_out = torch.empty_like(x)
     if residual is not None and residual_out is None:
@@ -231,6 +243,9 @@ def quant(y: torch.Tensor, mode: str, scale_in: torch.Tensor | None = None, *, o
     n, H = y.shape
     if y.dtype not in DTYPES:
         raise TypeError(f"unsupported activation dtype {y.dtype}")
+    for t in (y, out_q, out_scales, scale_in):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
     if out_q is None:
         out_q = torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device=y.device)
     if out_scales is None:
@@ -247,6 +262,7 @@ def qk_norm_rope(qkv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torc
                  is_neox: bool = True, stream=None, variant: str = "auto") -> torch.Tensor:
     """rmsq_qk_norm_rope_ex on torch CUDA tensors, in place on qkv (returned);
     variant "auto", "direct" or "pipelined" (bit-identical results)."""
+    vcode = _variant(variant)
     L = load()
     if qkv.dtype not in DTYPES:
         raise TypeError(f"unsupported activation dtype {qkv.dtype}")
@@ -259,7 +275,7 @@ def qk_norm_rope(qkv: torch.Tensor, positions: torch.Tensor, cos_sin_cache: torc
     st = L.rmsq_qk_norm_rope_ex(_p(qkv), _p(positions), _p(cos_sin_cache), cos_sin_cache.shape[0],
                                 _p(q_weight), _p(k_weight), ctypes.c_float(eps), n, num_q_heads, num_kv_heads,
                                 head_dim, 1 if is_neox else 0, DTYPES[qkv.dtype], _stream(stream),
-                                VARIANTS[variant])
+                                vcode)
     if st:
         raise RmsqError(st, "rmsq_qk_norm_rope_ex")
     return qkv
@@ -306,6 +322,7 @@ def fused_add_rmsnorm_nvfp4_dynamic(x: torch.Tensor, residual: torch.Tensor | No
     """rmsq_fused_add_rmsnorm_nvfp4_dynamic on torch CUDA tensors: NVFP4 with
     gs = 2688 / amax(all y) computed on the device.  Missing outputs and the
     workspace are allocated.  Returns (q, block_scales, global_scale, residual_out)."""
+    vcode = _variant(variant)
     L = load()
     n, H = x.shape
     if x.dtype not in DTYPES:
@@ -329,7 +346,7 @@ def fused_add_rmsnorm_nvfp4_dynamic(x: torch.Tensor, residual: torch.Tensor | No
         _p(x), _p(residual), _p(weight), ctypes.c_float(eps), _p(out_q), _p(out_scales),
         _p(out_global_scale), _p(residual_out), _p(workspace),
         workspace.numel() * workspace.element_size(), n, H, DTYPES[x.dtype], _stream(stream),
-        VARIANTS[variant])
+        vcode)
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_nvfp4_dynamic")
     return out_q, out_scales, out_global_scale, residual_out
