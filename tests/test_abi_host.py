@@ -166,6 +166,71 @@ def test_nvfp4_dynamic_argument_errors(L):
         assert dyn() == rq.ERR_NO_DEVICE
 
 
+def test_silu_mul_quant_argument_errors(L):
+    vp = ctypes.c_void_p
+    GU, Q, SC, SI = 0x50000000, 0x51000000, 0x52000000, 0x53000000
+
+    def act(gu=GU, mode=1, si=0, q=Q, sc=SC, n=4, d=64, dt=0):
+        return L.rmsq_silu_mul_quant(vp(gu) if gu else None, mode, vp(si) if si else None, vp(q) if q else None,
+                                     vp(sc) if sc else None, n, d, dt, None)
+
+    assert act(dt=2) == rq.ERR_INVALID_ARG
+    assert act(mode=7) == rq.ERR_INVALID_ARG
+    assert act(mode=0x40 | 1) == rq.ERR_INVALID_ARG              # unknown option bit
+    assert act(n=-1) == rq.ERR_INVALID_ARG and act(d=0) == rq.ERR_INVALID_ARG
+    assert act(d=60) == rq.ERR_UNSUPPORTED_SHAPE                  # not a multiple of 8
+    assert act(mode=2, d=64 + 8) == rq.ERR_UNSUPPORTED_SHAPE      # not a multiple of the group
+    assert act(mode=6, si=SI, d=24) == rq.ERR_UNSUPPORTED_SHAPE   # NVFP4 needs d % 16
+    assert act(d=32768 + 8) == rq.ERR_UNSUPPORTED_SHAPE           # above the largest d
+    assert act(n=0, gu=0, q=0, sc=0) == rq.OK
+    assert act(gu=0) == rq.ERR_INVALID_ARG
+    assert act(sc=0) == rq.ERR_INVALID_ARG                        # dynamic mode needs scales
+    assert act(mode=0) == rq.ERR_INVALID_ARG                      # static needs scale_in
+    assert act(gu=GU + 8) == rq.ERR_ALIGNMENT
+    assert act(sc=SC + 2) == rq.ERR_ALIGNMENT
+    assert act(q=GU + 64) == rq.ERR_ALIAS                         # codes over the input
+    assert act(sc=Q + 16) == rq.ERR_ALIAS                         # scales over the codes
+    if not torch.cuda.is_available():
+        assert act() == rq.ERR_NO_DEVICE
+        assert act(d=32768) == rq.ERR_NO_DEVICE                   # wider than the norm op allows: fine here
+
+
+def test_unfused_ops_argument_errors(L):
+    vp = ctypes.c_void_p
+    X, R, W, Y, RO, Q, SC = 0x40000000, 0x41000000, 0x42000000, 0x43000000, 0x44000000, 0x45000000, 0x46000000
+
+    def norm(x=X, r=R, w=W, eps=1e-6, y=Y, ro=RO, n=4, H=64, dt=0):
+        return L.rmsq_fused_add_rmsnorm(vp(x) if x else None, vp(r) if r else None, vp(w) if w else None,
+                                        ctypes.c_float(eps), vp(y) if y else None, vp(ro) if ro else None,
+                                        n, H, dt, None)
+
+    def qnt(y=Y, mode=1, si=0, q=Q, sc=SC, n=4, H=64, dt=0):
+        return L.rmsq_quant(vp(y) if y else None, mode, vp(si) if si else None, vp(q) if q else None,
+                            vp(sc) if sc else None, n, H, dt, None)
+
+    assert norm(dt=2) == rq.ERR_INVALID_ARG
+    assert norm(eps=-1.0) == rq.ERR_INVALID_ARG and norm(eps=float("nan")) == rq.ERR_INVALID_ARG
+    assert norm(H=60) == rq.ERR_UNSUPPORTED_SHAPE and norm(H=16392) == rq.ERR_UNSUPPORTED_SHAPE
+    assert norm(y=0) == rq.ERR_INVALID_ARG
+    assert norm(ro=0) == rq.ERR_INVALID_ARG                       # residual without residual_out
+    assert norm(x=X + 8) == rq.ERR_ALIGNMENT and norm(y=Y + 4) == rq.ERR_ALIGNMENT
+    assert norm(y=X + 16) == rq.ERR_ALIAS                         # y over x
+    assert norm(ro=W) == rq.ERR_ALIAS                             # residual_out over the weight
+    assert norm(n=0, x=0, r=0, w=0, y=0, ro=0) == rq.OK
+    assert qnt(dt=2) == rq.ERR_INVALID_ARG
+    assert qnt(mode=7) == rq.ERR_INVALID_ARG
+    assert qnt(mode=0) == rq.ERR_INVALID_ARG                      # static needs scale_in
+    assert qnt(sc=0) == rq.ERR_INVALID_ARG
+    assert qnt(mode=2, H=96) == rq.ERR_UNSUPPORTED_SHAPE
+    assert qnt(q=Y + 64) == rq.ERR_ALIAS
+    assert qnt(n=0, y=0, q=0, sc=0) == rq.OK
+    if not torch.cuda.is_available():
+        assert norm() == rq.ERR_NO_DEVICE
+        assert norm(r=0, ro=0) == rq.ERR_NO_DEVICE                # no residual
+        assert norm(ro=R) == rq.ERR_NO_DEVICE                     # in place
+        assert qnt() == rq.ERR_NO_DEVICE
+
+
 def test_qk_norm_rope_argument_errors(L):
     vp = ctypes.c_void_p
     Q, P_, CS, W1, W2 = 0x60000000, 0x61000000, 0x62000000, 0x63000000, 0x64000000
