@@ -80,3 +80,27 @@ def test_out_of_range_positions_leave_the_token_unchanged(orc):
     got = orc.run_qk_norm_rope(wl)
     assert np.array_equal(got[1], wl.qkv[1]) and np.array_equal(got[3], wl.qkv[3])
     assert not np.array_equal(got[0], wl.qkv[0])
+
+
+@pytest.mark.parametrize("neox", [True, False], ids=["neox", "gptj"])
+def test_quarter_turn_is_an_exact_swap(orc, neox):
+    """cos = 0, sin = 1 at every angle: each product is exact (y * 0, y * 1)
+    and so is each sum, so a pair (a, b) becomes (-b, a) with no rounding,
+    i.e. the norm op's rounded y with the pair swapped and the first element
+    negated (compared as values: a zero product may carry either sign)."""
+    D = 128
+    wl = ri.make_qk_workload("qk90", 7, 4, 2, D, neox=neox, max_pos=8, seed=11)
+    wl.positions[:] = 5
+    wl.cos_sin[5, :D // 2] = 0.0
+    wl.cos_sin[5, D // 2:] = 1.0
+    got = orc.run_qk_norm_rope(wl)
+    for h in range(6):
+        x = wl.qkv[:, h * D:(h + 1) * D]
+        w = wl.q_weight if h < 4 else wl.k_weight
+        y = _widen(orc.run_add_rmsnorm(x, None, w, eps=wl.eps)["y_t"])
+        want = np.empty_like(y)
+        if neox:
+            want[:, :D // 2], want[:, D // 2:] = -y[:, D // 2:], y[:, :D // 2]
+        else:
+            want[:, 0::2], want[:, 1::2] = -y[:, 1::2], y[:, 0::2]
+        assert np.array_equal(_widen(got[:, h * D:(h + 1) * D]), want), h
