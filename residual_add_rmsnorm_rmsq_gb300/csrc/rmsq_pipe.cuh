@@ -45,9 +45,11 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    if (tid < 64 && (tid & 31) >= nwarps)   // slots of absent warps read as 0
-#pragma unroll
-        for (int r = 0; r < R; ++r) s_sum[tid >> 5][r][tid & 31] = 0.0f;
+    // Slots of absent warps read as 0, in both halves of the double buffer and
+    // for every row of a group, whatever the CTA size (a one-warp CTA has
+    // only 32 threads to clear 2 * R * 31 slots).
+    for (int i = tid; i < 2 * R * 32; i += blockDim.x)
+        if ((i & 31) >= nwarps) (&s_sum[0][0][0])[i] = 0.0f;
     allow_dependents();
     grid_dependency_wait();
     __syncthreads();
