@@ -229,9 +229,11 @@ size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
  * RMSQ_NOALLOC_MAX_TOKENS bytes, about 257 KiB), present on every device that
  * loads the library until the process exits.  n_tokens above
  * RMSQ_NOALLOC_MAX_TOKENS returns RMSQ_ERR_UNSUPPORTED_SHAPE (use the entry
- * point with a workspace for larger batches).  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress with that device
- * current); make that first call before any stream capture.  Every call on a
+ * point with a workspace for larger batches).  Every call looks up the
+ * array's device address in the current device's context
+ * (cudaGetSymbolAddress), so a reset of the device's primary context between
+ * calls is followed; the first call on a device may load the library's device
+ * code there: make that first call before any stream capture.  Every call on a
  * device shares the one array and leaves its contents behind; the call zeroes
  * what must start at zero (the amax word) itself.  Calls whose work overlaps on
  * the GPU (other streams, or other host threads) race on the array: order them.

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "rmsq.h"
+#include "rmsq_abi.h"
 #include "rmsq_launch.h"
 
 namespace {
@@ -18,8 +19,13 @@ std::atomic<int> g_cc[kMaxDevices];
 // Device count: -1 = not yet queried.
 std::atomic<int> g_device_count{-1};
 
+}  // namespace
+
+namespace rmsq_abi {
+
 int fail_cuda(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();   // a non-sticky error is not left pending for later calls
     return RMSQ_ERR_CUDA;
 }
 
@@ -50,6 +56,13 @@ int check_device() {
     }
     return cc == 103 ? RMSQ_OK : RMSQ_ERR_UNSUPPORTED_DEVICE;
 }
+
+}  // namespace rmsq_abi
+
+namespace {
+
+using rmsq_abi::check_device;
+using rmsq_abi::fail_cuda;
 
 int group_of(int mode) {
     switch (mode) {

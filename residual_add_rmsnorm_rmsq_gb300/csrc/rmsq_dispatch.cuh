@@ -113,8 +113,10 @@ inline cudaError_t launch_kernel(const void* fn, dim3 grid, dim3 block, void** p
     return cudaLaunchKernelExC(&cfg, fn, params);
 }
 
-// Occupancy of a pipelined instantiation for a given ring size, cached.
+// Occupancy of a pipelined instantiation for a given ring size, cached per
+// device.
 struct OccEntry {
+    int dev;
     const void* fn;
     int smem;
     int threads;
@@ -124,23 +126,19 @@ struct OccEntry {
 // Shared-memory ring budget per CTA (two CTAs per SM).
 constexpr int kPipeSmemBudget = 110 * 1024;
 
-// The opt-in dynamic shared memory limit of a pipelined instantiation is set
-// once, to the full ring budget, so that no later launch ever lowers it below
-// what another launch of the same function needs.
-inline cudaError_t ensure_smem_limit(const void* fn) {
-    static std::mutex mu;
-    static const void* done[256];
-    static int used = 0;
-    std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < used; ++i)
-        if (done[i] == fn) return cudaSuccess;
+// The opt-in dynamic shared memory limit of a pipelined instantiation (the
+// full ring budget, so that no launch ever lowers it below what another
+// launch of the same function needs) and its carve-out preference.  Function
+// attributes belong to the context of the current device, so they are set
+// before every launch (a host-side call, no device work): a second device, or
+// a device whose primary context was reset, never gets a launch without them.
+inline cudaError_t set_smem_attributes(const void* fn) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
     // Prefer the largest shared-memory carve-out so that the rings of several
     // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
     if (e == cudaSuccess && RMSQ_MAX_SMEM_CARVEOUT)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
-    if (e == cudaSuccess && used < 256) done[used++] = fn;
     return e;
 }
 
@@ -148,15 +146,19 @@ inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t
     static std::mutex mu;
     static OccEntry cache[64];
     static int used = 0;
-    *err = ensure_smem_limit(fn);
+    *err = set_smem_attributes(fn);
+    if (*err != cudaSuccess) return 0;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return 0;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-        if (cache[i].fn == fn && cache[i].smem == smem && cache[i].threads == threads) return cache[i].blocks;
+        if (cache[i].dev == dev && cache[i].fn == fn && cache[i].smem == smem && cache[i].threads == threads)
+            return cache[i].blocks;
     int blocks = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, smem);
     if (*err != cudaSuccess) return 0;
-    if (used < 64) cache[used++] = {fn, smem, threads, blocks};
+    if (used < 64) cache[used++] = {dev, fn, smem, threads, blocks};
     return blocks;
 }
 
