@@ -30,9 +30,10 @@ MODES = {
 }
 DTYPES = {"bf16": 0, "fp16": 1}
 # Scale options, appended to a mode name with "+": "e8m0" (dynamic scales
-# rounded up to a power of two) and "tma" (column-major scales with the
-# stride padded to a multiple of 4).
-OPTIONS = {"e8m0": 0x10, "tma": 0x20}
+# rounded up to a power of two), "ue8m0" (those scales stored as one UE8M0
+# byte each) and "tma" (column-major scales with the stride padded to 16
+# bytes: a multiple of 4 fp32 scales or of 16 bytes).
+OPTIONS = {"e8m0": 0x10, "tma": 0x20, "ue8m0": 0x40}
 
 
 def mode_code(mode: str) -> int:
@@ -126,11 +127,11 @@ def _configure(L):
     L.oracle_qk_norm_rope.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int]
     L.oracle_qk_norm_rope.restype = ctypes.c_int
-    L.oracle_expf.argtypes, L.oracle_expf.restype = [f32], f32
     L.oracle_silu.argtypes, L.oracle_silu.restype = [f32], f32
-    for name in ("oracle_expf_array", "oracle_silu_array"):
-        getattr(L, name).argtypes = [vp, vp, i64]
-        getattr(L, name).restype = None
+    L.oracle_silu_array.argtypes = [vp, vp, i64]
+    L.oracle_silu_array.restype = None
+    L.oracle_quant_f32.argtypes = [vp, ctypes.c_int, f32, vp, vp, i64, i64, ctypes.c_int]
+    L.oracle_quant_f32.restype = ctypes.c_int
     return L
 
 
@@ -189,18 +190,22 @@ def tree_sum(v) -> float:
 
 def scale_shape(mode: str, n: int, H: int):
     """Shape and dtype of the scale output of ``mode`` for an [n, H] input
-    (column-major with "+tma": [H/G, n rounded up to 4])."""
+    (column-major with "+tma": [H/G, n rounded up to 4], or to 16 with
+    "+ue8m0"; one uint8 per scale with "+ue8m0")."""
     base = base_mode(mode)
     if base == "fp8_static":
         return None
-    if base == "fp8_per_token":
-        return (n,), np.float32
     if base == "nvfp4":
         return (n, H // 16), np.uint8
+    opts = mode.split("+")[1:]
+    dt = np.uint8 if "ue8m0" in opts else np.float32
+    if base == "fp8_per_token":
+        return (n,), dt
     G = GROUP[base]
     if base.endswith("_col"):
-        return (H // G, (n + 3) // 4 * 4 if "+tma" in mode else n), np.float32
-    return (n, H // G), np.float32
+        per16 = 16 if "ue8m0" in opts else 4
+        return (H // G, (n + per16 - 1) // per16 * per16 if "tma" in opts else n), dt
+    return (n, H // G), dt
 
 
 def run(x, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
@@ -250,16 +255,9 @@ def run_nvfp4_dynamic(x, residual, weight, *, eps: float, dtype: str = "bf16",
     return {"q": q, "scales": sc, "residual_out": ro, "global_scale": gs}
 
 
-def expf(v) -> np.ndarray:
-    """The oracle's e^x (Cody-Waite reduction, degree-7 Taylor polynomial) elementwise."""
-    v = _f32(v)
-    out = np.empty(v.shape, np.float32)
-    lib().oracle_expf_array(_ptr(v), _ptr(out), v.size)
-    return out
-
-
 def silu(v) -> np.ndarray:
-    """silu(g) = g / (1 + e^-g) elementwise, in the oracle's binary32 steps."""
+    """silu(g) = g / (1 + e^-g) elementwise: evaluated in binary64, rounded once
+    to binary32 (reading R15)."""
     v = _f32(v)
     out = np.empty(v.shape, np.float32)
     lib().oracle_silu_array(_ptr(v), _ptr(out), v.size)
@@ -284,6 +282,21 @@ def run_silu_mul(gate_up, *, mode: str, scale_in: float = 0.0, dtype: str = "bf1
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return {"q": q, "scales": scales, "residual_out": None, "y": y}
+
+
+def run_quant_f32(y, *, mode: str, scale_in: float = 0.0, nthreads: int = 1) -> dict:
+    """The quantisation step alone on given fp32 rows y [n, d] (any producer's
+    activations): ``q`` and ``scales`` laid out as for the fused op."""
+    y = np.ascontiguousarray(y, np.float32)
+    n, d = y.shape
+    q = np.zeros((n, d // 2) if mode == "nvfp4" else (n, d), np.uint8)
+    ss = scale_shape(mode, n, d)
+    scales = None if ss is None else np.zeros(ss[0], ss[1])
+    rc = lib().oracle_quant_f32(_ptr(y), mode_code(mode), ctypes.c_float(scale_in), _ptr(q), _ptr(scales), n, d,
+                                int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": scales, "residual_out": None}
 
 
 def run_silu_mul_workload(wl, mode: str, *, scale_in: float | None = None, want_y: bool = False,

@@ -42,11 +42,13 @@
  *      (fuse_act_quant)": silu_and_mul on the gated up-projection, then the
  *      quantisation, no full-precision activation tensor in between): each
  *      row of the input holds the gate g in its first d elements and the up
- *      projection u in the next d; a = silu(g) * u with
- *      silu(g) = g / (1 + e^-g), kept in fp32 like y; then the same
- *      quantisation as the norm op.
- *  R16 e^x is oracle_expf below (the pages do not fix an exp routine; the GPU
- *      evaluates the same steps).
+ *      projection u in the next d; silu(g) = g / (1 + e^-g) is its plain
+ *      definition, evaluated in binary64 (the C library's exp) from the exact
+ *      widening of g and rounded once to binary32; a = silu(g) * u is one
+ *      binary32 product, kept in fp32 like y; then the same quantisation as
+ *      the norm op.
+ *  R16 (no exp routine of its own: the pages fix none, and the definition of
+ *      silu above needs only the binary64 exponential.)
  *  R17 E8M0 scale option (blog, "Why this design", item 3: E8M0 scales,
  *      column-major scales and TMA alignment registered as combinable
  *      options): a dynamic (per-token or group) scale is rounded up to the
@@ -55,6 +57,11 @@
  *  R18 TMA-aligned option for column-major group scales: the stride between
  *      the scale columns of consecutive groups is n_tokens rounded up to a
  *      multiple of 4 (16 bytes); the padding entries are not written.
+ *  R21 UE8M0 byte option (the same item of the blog): the power-of-two scale
+ *      of R17 is stored as one byte, its biased binary32 exponent (the UE8M0
+ *      encoding: byte e stands for 2^(e - 127)), in the same layouts; with
+ *      the TMA-aligned column layout the stride is n_tokens rounded up to 16
+ *      (16 bytes).  Codes are those of R17.
  *  R19 the unfused sequence the fusion replaces (vLLM docs, same page,
  *      fuse_norm_quant: rms_norm / fused_add_rms_norm followed by quant_fp8):
  *      the first op writes y rounded to the activation type T (nearest even)
@@ -82,7 +89,7 @@
 
 enum { OR_BF16 = 0, OR_FP16 = 1 };
 /* Option bits of the mode argument (R17, R18). */
-enum { OR_OPT_E8M0 = 0x10, OR_OPT_TMA = 0x20 };
+enum { OR_OPT_E8M0 = 0x10, OR_OPT_TMA = 0x20, OR_OPT_UE8M0 = 0x40 };
 enum {
     OR_FP8_STATIC = 0,
     OR_FP8_PER_TOKEN = 1,
@@ -209,51 +216,17 @@ float oracle_e2m1_decode(uint8_t c)
 }
 
 /* ------------------------------------------------------------------------ */
-/* e^x (reading R16).                                                       */
+/* silu (reading R15).                                                      */
 /* ------------------------------------------------------------------------ */
 
-/* W. J. Cody and W. Waite, "Software Manual for the Elementary Functions"
- * (1980), exponential: write x = n ln2 + r with n the integer nearest to
- * x log2(e), so that |r| <= ln2 / 2 (about 0.347); ln2 is split into a high
- * part with 15 significant bits (n times it is exact for |n| < 512) and the
- * rest, and r = (x - n ln2_hi) - n ln2_lo is formed with two fused
- * multiply-adds; e^r is the Taylor polynomial sum r^k / k!, k = 0..7, in
- * Horner form with one fused multiply-add per step (truncation error below
- * r^8 / 8! < 2^-27 relative); e^x = e^r 2^n, the scaling split in two steps
- * where 2^n alone is not a normal binary32.  Every step is one binary32
- * operation (fmaf: one rounding of the exact a * b + c), rounded to nearest
- * even, in the order written. */
-static float pow2i(int k) { return bits_to_float((uint32_t)(k + 127) << 23); }   /* -126 <= k <= 127 */
-
-float oracle_expf(float x)
-{
-    if (x != x) return x;
-    if (x > 89.0f) return INFINITY;      /* e^89 > FLT_MAX */
-    if (x < -104.0f) return 0.0f;        /* e^-104 < half the smallest subnormal */
-    const float log2e = 1.44269502162933349609375f;         /* RN(log2 e) */
-    const float ln2_hi = 0.693145751953125f;               /* 0x3f317200 */
-    const float ln2_lo = 1.428606765330187045e-06f;        /* RN(ln2 - ln2_hi) */
-    const float n = rintf(x * log2e);
-    const float r = fmaf(-n, ln2_lo, fmaf(-n, ln2_hi, x));
-    /* 1/k! rounded to binary32, k = 7 .. 0 */
-    float p = 1.98412701e-4f;                               /* 1/5040 */
-    p = fmaf(p, r, 1.38888892e-3f);                         /* 1/720 */
-    p = fmaf(p, r, 8.33333377e-3f);                         /* 1/120 */
-    p = fmaf(p, r, 4.16666679e-2f);                         /* 1/24 */
-    p = fmaf(p, r, 1.66666672e-1f);                         /* 1/6 */
-    p = fmaf(p, r, 0.5f);
-    p = fmaf(p, r, 1.0f);
-    p = fmaf(p, r, 1.0f);
-    const int k = (int)n;
-    if (k > 127) return (p * pow2i(127)) * pow2i(k - 127);
-    if (k < -126) return (p * pow2i(k + 64)) * pow2i(-64);
-    return p * pow2i(k);
-}
-
-/* silu(g) = g / (1 + e^-g) (reading R15). */
+/* silu(g) = g / (1 + e^-g), in binary64 from the exact widening of g, rounded
+ * once to binary32.  The binary64 evaluation carries about 2^-52 relative
+ * error, far below the binary32 rounding.  Non-finite g is outside the
+ * readings (R13). */
 float oracle_silu(float g)
 {
-    return g / (1.0f + oracle_expf(-g));
+    const double gd = (double)g;
+    return (float)(gd / (1.0 + exp(-gd)));
 }
 
 /* ------------------------------------------------------------------------ */
@@ -302,8 +275,9 @@ typedef struct {
     int silu_mul;            /* 1: the SiLU+Mul op, x = [n, 2H] gate | up (R15);
                                 2: quantisation of x alone (R19) */
     uint16_t *y_t_out;       /* R19: y rounded to T instead of step 5 */
-    int e8m0;                /* R17 */
+    int e8m0;                /* R17: 1 = power-of-two fp32 scales; R21: 2 = their UE8M0 bytes */
     int64_t col_stride;      /* column-major scale stride: n, or n rounded up to 4 (R18) */
+    const float *y_in;       /* silu_mul == 3: step 5 alone on these fp32 rows [n, H] */
 } OracleArgs;
 
 /* The smallest power of two >= x, for a positive normal x: x = f 2^k with
@@ -320,13 +294,15 @@ static int split_mode(int mode, int64_t n, int *base, int *e8m0, int64_t *col_st
 {
     *base = mode & 0xf;
     const int opts = mode & ~0xf;
-    if (*base < 0 || *base > 6 || (opts & ~(OR_OPT_E8M0 | OR_OPT_TMA))) return -1;
+    if (*base < 0 || *base > 6 || (opts & ~(OR_OPT_E8M0 | OR_OPT_TMA | OR_OPT_UE8M0))) return -1;
     const int dynamic = *base >= OR_FP8_PER_TOKEN && *base <= OR_FP8_G64_COL;
     const int col = *base == OR_FP8_G128_COL || *base == OR_FP8_G64_COL;
-    if ((opts & OR_OPT_E8M0) && !dynamic) return -1;
+    if ((opts & (OR_OPT_E8M0 | OR_OPT_UE8M0)) && !dynamic) return -1;
     if ((opts & OR_OPT_TMA) && !col) return -1;
-    *e8m0 = (opts & OR_OPT_E8M0) != 0;
-    *col_stride = (opts & OR_OPT_TMA) ? (n + 3) / 4 * 4 : n;
+    *e8m0 = (opts & OR_OPT_UE8M0) ? 2 : (opts & OR_OPT_E8M0) != 0;
+    /* R18 / R21: 16 bytes between scale columns: 4 fp32 scales or 16 UE8M0 bytes */
+    const int64_t per16 = (opts & OR_OPT_UE8M0) ? 16 : 4;
+    *col_stride = (opts & OR_OPT_TMA) ? (n + per16 - 1) / per16 * per16 : n;
     return 0;
 }
 
@@ -353,6 +329,20 @@ static int group_size(int mode)
     }
 }
 
+/* A dynamic scale into element i of the scale tensor: fp32, or with the
+ * UE8M0 byte option (R21) the biased exponent of the power-of-two scale,
+ * bits 30..23 of its binary32 pattern (byte e stands for 2^(e - 127)). */
+static void store_scale(const OracleArgs *a, int64_t i, float sc)
+{
+    if (a->e8m0 == 2) {
+        uint32_t u;
+        memcpy(&u, &sc, 4);
+        ((uint8_t *)a->out_scales)[i] = (uint8_t)((u >> 23) & 0xffu);
+    } else {
+        ((float *)a->out_scales)[i] = sc;
+    }
+}
+
 /* Step 5 of the op: quantisation of the fp32 row y (R4-R8). */
 static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
 {
@@ -366,7 +356,7 @@ static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
         for (int64_t i = 0; i < H; ++i) amax = fmaxf(amax, fabsf(y[i]));
         float sc = fmaxf(amax / 448.0f, 1e-12f);
         if (a->e8m0) sc = pow2_ceil(sc);
-        ((float *)a->out_scales)[t] = sc;
+        store_scale(a, t, sc);
         for (int64_t i = 0; i < H; ++i) q[t * H + i] = oracle_e4m3_encode(y[i] / sc);
     } else if (a->mode == OR_NVFP4) {
         float gs = a->scale_in;
@@ -388,15 +378,13 @@ static void quantize_row(const OracleArgs *a, int64_t t, const float *y)
     } else {
         int G = group_size(a->mode);
         int col = (a->mode == OR_FP8_G128_COL || a->mode == OR_FP8_G64_COL);
-        float *sc_out = (float *)a->out_scales;
         for (int64_t g = 0; g < H / G; ++g) {
             const float *yg = y + G * g;
             float amax = 0.0f;
             for (int k = 0; k < G; ++k) amax = fmaxf(amax, fabsf(yg[k]));
             float sc = fmaxf(amax / 448.0f, 1e-12f);
             if (a->e8m0) sc = pow2_ceil(sc);
-            if (col) sc_out[g * a->col_stride + t] = sc;
-            else sc_out[t * (H / G) + g] = sc;
+            store_scale(a, col ? g * a->col_stride + t : t * (H / G) + g, sc);
             for (int k = 0; k < G; ++k) q[t * H + G * g + k] = oracle_e4m3_encode(yg[k] / sc);
         }
     }
@@ -479,7 +467,8 @@ static void *run_span(void *p)
     sp->ok = s.h && s.sq && s.y && s.buf;
     if (sp->ok)
         for (int64_t t = sp->r0; t < sp->r1; ++t) {
-            if (sp->a->silu_mul == 2) oracle_quant_row(sp->a, t, &s);
+            if (sp->a->silu_mul == 3) quantize_row(sp->a, t, sp->a->y_in + t * H);
+            else if (sp->a->silu_mul == 2) oracle_quant_row(sp->a, t, &s);
             else if (sp->a->silu_mul) oracle_act_row(sp->a, t, &s);
             else oracle_row(sp->a, t, &s);
         }
@@ -560,6 +549,23 @@ int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uin
     return run_rows(&a, nthreads);
 }
 
+/* Step 5 alone (R4-R8, R17, R18) on given fp32 rows y [n, d]: the
+ * quantisation any producer of fp32 activations feeds.  Returns 0, or -1 /
+ * -2 like oracle_fused_add_rmsnorm_quant. */
+int oracle_quant_f32(const float *y, int mode, float scale_in, uint8_t *out_q, void *out_scales, int64_t n,
+                     int64_t d, int nthreads)
+{
+    int e8m0;
+    int64_t col_stride;
+    if (n < 0 || split_mode(mode, n, &mode, &e8m0, &col_stride)) return -1;
+    if (d <= 0 || !y || !out_q || (mode != OR_FP8_STATIC && !out_scales)) return -1;
+    if (mode == OR_NVFP4 && d % 16) return -1;
+    if (group_size(mode) && d % group_size(mode)) return -1;
+    OracleArgs a = {NULL, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
+                    NULL, NULL, n, d, OR_BF16, 3, NULL, e8m0, col_stride, y};
+    return run_rows(&a, nthreads);
+}
+
 /* R20: QK-norm + RoPE, in place on qkv [n, (nq + 2 nkv) D] (q heads, then k
  * heads, then v heads of each token).  Returns 0, or -1 on a bad argument. */
 static void norm_rope_head(uint16_t *head, const uint16_t *w, float eps, const float *cs, int D, int neox,
@@ -629,12 +635,6 @@ int oracle_quant(const uint16_t *y_t, int mode, float scale_in, uint8_t *out_q, 
     OracleArgs a = {y_t, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
                     NULL, NULL, n, H, dtype, 2, NULL, e8m0, col_stride};
     return run_rows(&a, nthreads);
-}
-
-/* Array form of oracle_expf, for the accuracy checks. */
-void oracle_expf_array(const float *v, float *out, int64_t n)
-{
-    for (int64_t i = 0; i < n; ++i) out[i] = oracle_expf(v[i]);
 }
 
 void oracle_silu_array(const float *v, float *out, int64_t n)

@@ -1,7 +1,24 @@
-"""SiLU+Mul + quantisation on the GPU against the oracle, bit for bit.
+"""SiLU+Mul + quantisation on the GPU against the oracle.
 
-Same bar as the norm op: codes and scales identical (the CUDA path evaluates
-e^x, the division and the products in the oracle's binary32 steps).
+The oracle takes silu from its plain definition (binary64, rounded once); the
+CUDA path evaluates e^x, the sum and the division in binary32 steps, so its
+activation a = silu(g) * u can sit a few ulps from the oracle's.  Two checks,
+therefore, on every workload:
+
+1. exactness of the quantisation: the kernel's codes and scales equal the
+   oracle's quantisation step applied to the kernel's own activations (read
+   back through the library's elementwise debug entry), bit for bit;
+2. the bar against the independent oracle: codes within one step on at most
+   1e-4 of the elements, every scale within ACT_SCALE_ULP binary32 ulps of
+   the oracle's (a per-token / group scale moves only when its amax element's
+   activation does); both counts are printed.
+
+ACT_SCALE_ULP follows from the arithmetic: the kernel's e^x is within
+1.2 ulp (2^-23 relative each), 1 + e^-g and the division round once each
+(2^-24), so its silu is within 4.4 * 2^-24 of the exact value; the oracle's
+is within 2^-24; both products with u round once more (2^-24 each).  The two
+activations are therefore within 7.4 * 2^-24 relative, at most 7.4 ulps, and
+the scale's own rounding adds at most one.
 """
 import numpy as np
 import pytest
@@ -15,6 +32,9 @@ import rmsq_inputs as ri
 pytestmark = pytest.mark.gpu
 MODES = ["fp8_static", "fp8_per_token", "fp8_group128_row", "fp8_group128_col", "fp8_group64_row",
          "fp8_group64_col", "nvfp4"]
+ACT_SCALE_ULP = 8
+EXP_ULP = 1.5           # the kernel's e^x: Cody-Waite reduction + degree-7 Taylor polynomial
+SILU_ULP = 4.5          # its silu: e^x, then 1 + e^-g and the division rounded once each
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,10 +50,50 @@ def run_gpu(wl, mode, scale_in):
     return {"q": q.cpu().numpy(), "scales": None if sc is None else sc.cpu().numpy(), "residual_out": None}
 
 
+def kernel_activations(wl):
+    """The kernel's own a = silu(g) * u, elementwise on the device."""
+    gu = P.dev_act(wl.gate_up, wl.dtype).float()
+    d = wl.d
+    a = rq.debug_activation("silu_mul", gu[:, :d].contiguous(), gu[:, d:].contiguous())
+    torch.cuda.synchronize()
+    return a.cpu().numpy()
+
+
+def _ulps(got: np.ndarray, want: np.ndarray) -> np.ndarray:
+    """Distance in binary32 ulps between positive floats (their bit patterns)."""
+    return np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
+
+
 def check(wl, mode, nthreads=8):
     want = oracle.run_silu_mul_workload(wl, mode, nthreads=nthreads)
     got = run_gpu(wl, mode, want["scale_in"])
-    return P.compare(got, want, mode, f"{wl.name}/{mode}")
+    label = f"{wl.name}/{mode}"
+    # 1. the quantisation of the kernel's own activations, bit for bit
+    mine = oracle.run_quant_f32(kernel_activations(wl), mode=mode, scale_in=want["scale_in"] or 0.0,
+                                nthreads=nthreads)
+    assert np.array_equal(got["q"], mine["q"]), f"{label}: codes differ from the quantisation of the kernel's a"
+    if mine["scales"] is not None:
+        assert np.array_equal(got["scales"].view(np.uint8), mine["scales"].view(np.uint8)), label
+    # 2. against the independent oracle
+    steps = P.code_steps(got["q"], want["q"], mode)
+    n_bad = int(np.count_nonzero(steps))
+    report = {"label": label, "elements": int(steps.size), "mismatches": n_bad,
+              "fraction": n_bad / max(1, steps.size), "max_step": int(steps.max()) if steps.size else 0}
+    if want["scales"] is not None:
+        g, w = got["scales"], want["scales"]
+        if g.dtype == np.float32:
+            d_ulp = _ulps(g, w)
+            report["scales"] = int(g.size)
+            report["scale_mismatches"] = int(np.count_nonzero(d_ulp))
+            report["scale_max_ulp"] = int(d_ulp.max()) if d_ulp.size else 0
+            assert report["scale_max_ulp"] <= ACT_SCALE_ULP, report
+        else:   # NVFP4 block scales: E4M3 codes of amax / 6 * gs
+            sd = P.code_steps(g, w, "fp8_static")
+            report["scale_mismatches"] = int(np.count_nonzero(sd))
+            assert int(sd.max()) <= 1 and np.count_nonzero(sd) <= max(1, P.MAX_MISMATCH_FRAC * sd.size), report
+    print(f"parity {report}")
+    assert report["fraction"] <= P.MAX_MISMATCH_FRAC and report["max_step"] <= P.MAX_STEP, report
+    return report
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -53,7 +113,7 @@ def test_ragged_and_wide_rows(d):
 
 def test_extreme_gate_range():
     """Gates from -120 to 100: e^-g overflows to inf (silu = -0), underflows to
-    0 and passes through the subnormal range; results still bit-exact."""
+    0 and passes through the subnormal range; results still within the bar."""
     for mode in ("fp8_per_token", "fp8_group128_row", "nvfp4"):
         wl = ri.make_act_workload("act_range", 64, 1024, gate_range=(-120.0, 100.0), seed=21)
         check(wl, mode)
@@ -86,24 +146,46 @@ def _all_bf16_values():
 
 @pytest.mark.parametrize("kind", ["exp", "exp_mid", "silu"])
 def test_activation_steps_on_every_bf16_input(kind):
-    """The GPU's e^x (both step sequences) and silu against the oracle's on all
-    finite bf16 values (and their negations, for e^-g), element by element."""
+    """The GPU's e^x (both step sequences) and silu on all finite bf16 values
+    (and their negations, for e^-g), against the double-precision
+    definitions, within the bounds of their binary32 steps."""
     x = _all_bf16_values()
     x = np.concatenate([x, -x]).astype(np.float32)
     if kind == "exp_mid":
         x = x[np.abs(x) <= 87.0]
-    got = rq.debug_activation(kind, torch.from_numpy(x).cuda()).cpu().numpy()
-    want = oracle.expf(x) if kind.startswith("exp") else oracle.silu(x)
-    bad = got.view(np.uint32) != want.view(np.uint32)
-    bad &= ~(np.isnan(got) & np.isnan(want))
-    assert not bad.any(), (int(bad.sum()), x[bad][:8].tolist(), got[bad][:8].tolist(), want[bad][:8].tolist())
+    got = rq.debug_activation(kind, torch.from_numpy(x).cuda()).cpu().numpy().astype(np.float64)
+    x64 = x.astype(np.float64)
+    with np.errstate(over="ignore"):
+        want = np.exp(x64) if kind.startswith("exp") else x64 / (1.0 + np.exp(-x64))
+    fin = np.isfinite(want) & (np.abs(want) >= 2.0 ** -126) & (np.abs(want) <= 3.0e38)
+    if kind == "silu":
+        # below g = -88.7, e^-g overflows binary32 and the kernel's silu is -0,
+        # where the exact value is below 2^-120 in magnitude (it quantises to
+        # a zero code under any scale the 1e-12 floor allows)
+        low = x64 < -88.0
+        assert np.all(np.abs(got[low]) <= np.abs(want[low])) and np.all(np.abs(want[low]) < 2.0 ** -120)
+        fin &= ~low
+    sp = np.spacing(np.abs(want[fin]).astype(np.float32)).astype(np.float64)
+    err = np.abs(got[fin] - want[fin]) / sp
+    bound = EXP_ULP if kind.startswith("exp") else SILU_ULP
+    assert err.max() <= bound, (err.max(), x[fin][np.argmax(err)])
+    # outside the normal range: overflow to inf, underflow to (signed) zero
+    big = np.isfinite(x64) & ~np.isfinite(want)
+    assert np.all(np.isinf(got[big]))
+    tiny = np.abs(want) < 2.0 ** -151        # well below half the smallest subnormal
+    assert np.all(got[tiny] == 0.0)
 
 
 def test_silu_mul_on_random_pairs():
+    """silu(g) * u from the debug entry: within the activation bound of the
+    double-precision product."""
     rng = np.random.default_rng(1)
     g = rng.normal(0, 3, 2_000_003).astype(np.float32)
     u = rng.normal(0, 1, g.size).astype(np.float32)
     got = rq.debug_activation("silu_mul", torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()).cpu().numpy()
-    want = (oracle.silu(g) * u).astype(np.float32)
-    bad = got.view(np.uint32) != want.view(np.uint32)
-    assert not bad.any(), (int(bad.sum()), g[bad][:8].tolist(), got[bad][:8].tolist(), want[bad][:8].tolist())
+    g64 = g.astype(np.float64)
+    want = g64 / (1.0 + np.exp(-g64)) * u.astype(np.float64)
+    ok = np.abs(want) > 1e-30
+    sp = np.spacing(np.abs(want[ok]).astype(np.float32)).astype(np.float64)
+    err = np.abs(got[ok].astype(np.float64) - want[ok]) / sp
+    assert err.max() <= SILU_ULP + 1.0, err.max()

@@ -23,9 +23,14 @@ MUTANTS = [
      "widen(a->dtype, xr[i]) - widen(a->dtype, a->residual[t * H + i])"),
     ("times_scale", "oracle_e4m3_encode(y[i] / sc)", "oracle_e4m3_encode(y[i] * sc)"),
     ("scale_over_447", "amax / 448.0f", "amax / 447.0f"),
-    ("col_stored_row_major", "if (col) sc_out[g * a->col_stride + t] = sc;", "if (col) sc_out[t * (H / G) + g] = sc;"),
+    ("col_stored_row_major", "store_scale(a, col ? g * a->col_stride + t : t * (H / G) + g, sc);",
+     "store_scale(a, t * (H / G) + g, sc);"),
+    ("ue8m0_mantissa_byte", "((uint8_t *)a->out_scales)[i] = (uint8_t)((u >> 23) & 0xffu);",
+     "((uint8_t *)a->out_scales)[i] = (uint8_t)((u >> 15) & 0xffu);"),
+    ("ue8m0_tma_stride_of_4", "const int64_t per16 = (opts & OR_OPT_UE8M0) ? 16 : 4;", "const int64_t per16 = 4;"),
     ("e8m0_rounds_down", "return f == 0.5f ? x : ldexpf(1.0f, k);", "return ldexpf(1.0f, k - 1);"),
-    ("tma_stride_not_padded", "*col_stride = (opts & OR_OPT_TMA) ? (n + 3) / 4 * 4 : n;", "*col_stride = n;"),
+    ("tma_stride_not_padded", "*col_stride = (opts & OR_OPT_TMA) ? (n + per16 - 1) / per16 * per16 : n;",
+     "*col_stride = n;"),
     # QK-norm + RoPE (pinned by test_oracle_qk.py)
     ("rope_sin_sign", "const float oa = ya * c - yb * s;", "const float oa = ya * c + yb * s;"),
     ("rope_cos_sin_swapped", "const float c = cs[i], s = cs[h + i];", "const float s = cs[i], c = cs[h + i];"),
@@ -46,11 +51,10 @@ MUTANTS = [
     ("bf16_truncates", "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1;", ""),
     ("fp16_subnormal_step", "float k = rintf(ldexpf(a, 24));", "float k = rintf(ldexpf(a, 23));"),
     # SiLU+Mul (pinned by test_oracle_act.py)
-    ("exp_term_dropped", "    p = fmaf(p, r, 4.16666679e-2f);                         /* 1/24 */\n", ""),
-    ("exp_ln2_lo_dropped", "fmaf(-n, ln2_lo, fmaf(-n, ln2_hi, x))", "fmaf(-n, ln2_hi, x)"),
-    ("exp_no_subnormal_step", "if (k < -126) return (p * pow2i(k + 64)) * pow2i(-64);",
-     "if (k < -126) return 0.0f;"),
-    ("silu_sign_slip", "return g / (1.0f + oracle_expf(-g));", "return g / (1.0f + oracle_expf(g));"),
+    ("silu_sign_slip", "gd / (1.0 + exp(-gd))", "gd / (1.0 + exp(gd))"),
+    ("silu_sigmoid_only", "gd / (1.0 + exp(-gd))", "1.0 / (1.0 + exp(-gd))"),
+    ("silu_without_one", "gd / (1.0 + exp(-gd))", "gd / exp(-gd)"),
+    ("silu_in_binary32", "return (float)(gd / (1.0 + exp(-gd)));", "return g / (1.0f + expf(-g));"),
     ("gate_up_swapped", "const uint16_t *g = a->x + t * 2 * d, *u = g + d;",
      "const uint16_t *u = a->x + t * 2 * d, *g = u + d;"),
 ]
