@@ -116,16 +116,24 @@ typedef enum {
  *                          s = 2^ceil(log2 max(amax / 448, 1e-12)); it is
  *                          still stored as fp32 (its E8M0 byte is the
  *                          exponent field, bits 30..23), q = e4m3(y / s).
+ *  RMSQ_QUANT_UE8M0        the same power-of-two scale, stored as one byte
+ *                          (per-token and group modes only): the UE8M0
+ *                          encoding, byte e standing for 2^(e - 127) (the
+ *                          biased exponent of the fp32 scale).  out_scales is
+ *                          then u8 with the layouts below (1-byte aligned);
+ *                          implies RMSQ_QUANT_E8M0, codes are the same.
  *  RMSQ_QUANT_TMA_ALIGNED  column-major group scales (_COL modes only) use a
- *                          stride of n_tokens rounded up to a multiple of 4
- *                          (16 bytes) between groups: [hidden/G, round4(n)];
- *                          the padding entries are not written.
+ *                          stride of n_tokens rounded up to 16 bytes of scales
+ *                          between groups: [hidden/G, round4(n)] fp32 scales,
+ *                          or [hidden/G, round16(n)] UE8M0 bytes; the padding
+ *                          entries are not written.
  * Any other bit, or an option with a mode it does not apply to, is
  * RMSQ_ERR_INVALID_ARG.
  */
 #define RMSQ_QUANT_MODE_MASK 0x0f
 #define RMSQ_QUANT_E8M0 0x10
 #define RMSQ_QUANT_TMA_ALIGNED 0x20
+#define RMSQ_QUANT_UE8M0 0x40
 
 /*
  * rmsq_fused_add_rmsnorm_quant — one launch of the fused op over n_tokens rows.
@@ -141,8 +149,9 @@ typedef enum {
  *               modes.  Its value must be finite and > 0; it is not checked.
  *  out_q        device, u8[n_tokens, hidden] (FP8) or u8[n_tokens, hidden/2]
  *               (NVFP4), 16-byte aligned.
- *  out_scales   device; fp32 per-token / per-group scales (4-byte aligned) or
- *               u8 NVFP4 block scales; ignored (may be NULL) for FP8_STATIC.
+ *  out_scales   device; fp32 per-token / per-group scales (4-byte aligned),
+ *               their UE8M0 bytes (RMSQ_QUANT_UE8M0), or u8 NVFP4 block
+ *               scales; ignored (may be NULL) for FP8_STATIC.
  *               rmsq_query_sizes gives the byte sizes.
  *  residual_out device, T[n_tokens, hidden], 16-byte aligned; NULL exactly when
  *               residual is NULL.  It may be the same pointer as residual (the
@@ -348,11 +357,11 @@ int rmsq_silu_mul_quant(const void *gate_up, int quant_mode, const float *scale_
 
 /*
  * rmsq_set_pipeline_config — process-wide tuning of the PIPELINED variant:
- * chunks_per_thread (16-byte chunks of a row per thread: 1, 2 or 4), stages
- * (rows in flight per CTA: 1..8) and ctas_per_sm (cap on resident CTAs per
- * SM: 1..8) and rows_per_iter (rows a CTA works on together: 1 or 2; two
- * share each block reduction's barrier).  0 keeps the automatic choice for
- * that parameter.  The pipelined QK-norm + RoPE kernel takes stages (tokens
+ * chunks_per_thread (16-byte chunks of a row per thread: 1, 2, 4 or 8),
+ * stages (rows in flight per CTA: 1..8) and ctas_per_sm (cap on resident
+ * CTAs per SM: 1..32).  rows_per_iter (0, 1 or 2) is accepted and has no
+ * effect: the norm kernels work on one row per CTA iteration.  0 keeps the
+ * automatic choice for that parameter.  The pipelined QK-norm + RoPE kernel takes stages (tokens
  * in flight per CTA, 2..8) and ctas_per_sm from the same settings.  A choice
  * that does not fit (more than 512 threads, or a ring larger than the shared
  * memory budget) falls back to the automatic one.  Results do not depend on

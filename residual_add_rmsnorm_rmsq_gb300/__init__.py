@@ -30,9 +30,10 @@ MODES = {
     "fp8_group64_col": 5,
     "nvfp4": 6,
 }
-# Scale options (RMSQ_QUANT_E8M0, RMSQ_QUANT_TMA_ALIGNED), appended to a mode
-# name with "+": e.g. "fp8_group128_col+e8m0+tma".
-OPTIONS = {"e8m0": 0x10, "tma": 0x20}
+# Scale options (RMSQ_QUANT_E8M0, RMSQ_QUANT_TMA_ALIGNED, RMSQ_QUANT_UE8M0),
+# appended to a mode name with "+": e.g. "fp8_group128_col+e8m0+tma",
+# "fp8_per_token+ue8m0".
+OPTIONS = {"e8m0": 0x10, "tma": 0x20, "ue8m0": 0x40}
 
 
 def mode_code(mode: str) -> int:
@@ -161,18 +162,21 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def scales_like(mode: str, n_tokens: int, hidden: int, device) -> torch.Tensor | None:
     """An output tensor of the right shape and dtype for the scales of ``mode``
-    (column-major with "+tma": [hidden/G, n_tokens rounded up to 4])."""
-    base = mode.split("+")[0]
+    (column-major with "+tma": [hidden/G, n_tokens rounded up to 16 bytes of
+    scales]; uint8 with "+ue8m0")."""
+    base, *opts = mode.split("+")
     if base == "fp8_static":
         return None
-    if base == "fp8_per_token":
-        return torch.empty(n_tokens, dtype=torch.float32, device=device)
     if base == "nvfp4":
         return torch.empty(n_tokens, hidden // 16, dtype=torch.uint8, device=device)
+    dt = torch.uint8 if "ue8m0" in opts else torch.float32
+    if base == "fp8_per_token":
+        return torch.empty(n_tokens, dtype=dt, device=device)
     G = 128 if "128" in base else 64
-    cols = (n_tokens + 3) // 4 * 4 if "+tma" in mode else n_tokens
+    per16 = 16 if "ue8m0" in opts else 4
+    cols = (n_tokens + per16 - 1) // per16 * per16 if "tma" in opts else n_tokens
     shape = (hidden // G, cols) if base.endswith("_col") else (n_tokens, hidden // G)
-    return torch.empty(shape, dtype=torch.float32, device=device)
+    return torch.empty(shape, dtype=dt, device=device)
 
 
 def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weight: torch.Tensor,

@@ -237,6 +237,7 @@ cudaError_t launch_act(const LaunchArgs& la, bool silu, cudaStream_t stream) {
     a.pair = a.chunks % 2 == 0 && reinterpret_cast<uintptr_t>(la.x) % 32 == 0 &&
              reinterpret_cast<uintptr_t>(la.q) % 16 == 0;
     a.e8m0 = la.e8m0;
+    a.ue8m0 = la.ue8m0;
     a.col_stride = la.col_stride;
     int J, threads, seg;
     if (la.mode == kFp8PerToken) {   // one CTA per row

@@ -78,14 +78,20 @@ int group_of(int mode) {
 // (E8M0) or with column-major group scales (TMA-aligned stride).
 bool options_valid(int quant_mode) {
     const int base = quant_mode & RMSQ_QUANT_MODE_MASK, opts = quant_mode & ~RMSQ_QUANT_MODE_MASK;
-    if (opts & ~(RMSQ_QUANT_E8M0 | RMSQ_QUANT_TMA_ALIGNED)) return false;
+    if (opts & ~(RMSQ_QUANT_E8M0 | RMSQ_QUANT_TMA_ALIGNED | RMSQ_QUANT_UE8M0)) return false;
     const bool dynamic = base >= RMSQ_FP8_PER_TOKEN && base <= RMSQ_FP8_GROUP64_COL;
     const bool col = base == RMSQ_FP8_GROUP128_COL || base == RMSQ_FP8_GROUP64_COL;
-    return !((opts & RMSQ_QUANT_E8M0) && !dynamic) && !((opts & RMSQ_QUANT_TMA_ALIGNED) && !col);
+    return !((opts & (RMSQ_QUANT_E8M0 | RMSQ_QUANT_UE8M0)) && !dynamic) &&
+           !((opts & RMSQ_QUANT_TMA_ALIGNED) && !col);
 }
 
+// Bytes per dynamic FP8 scale: 4 (fp32), 1 with the UE8M0 byte option.
+int scale_elem_bytes(int quant_mode) { return (quant_mode & RMSQ_QUANT_UE8M0) ? 1 : 4; }
+
+// Column-major stride: n, or n rounded up to 16 bytes of scales.
 int64_t col_stride_of(int quant_mode, int64_t n) {
-    return (quant_mode & RMSQ_QUANT_TMA_ALIGNED) ? (n + 3) / 4 * 4 : n;
+    const int64_t per16 = 16 / scale_elem_bytes(quant_mode);
+    return (quant_mode & RMSQ_QUANT_TMA_ALIGNED) ? (n + per16 - 1) / per16 * per16 : n;
 }
 
 int check_shape(int quant_mode, int64_t n, int64_t hidden) {
@@ -105,13 +111,14 @@ void sizes_of(int quant_mode, int64_t n, int64_t hidden, size_t* q, size_t* sc) 
     *q = static_cast<size_t>(mode == RMSQ_NVFP4 ? n * (hidden / 2) : n * hidden);
     switch (mode) {
     case RMSQ_FP8_STATIC: *sc = 0; break;
-    case RMSQ_FP8_PER_TOKEN: *sc = static_cast<size_t>(n) * 4; break;
+    case RMSQ_FP8_PER_TOKEN: *sc = static_cast<size_t>(n) * scale_elem_bytes(quant_mode); break;
     case RMSQ_NVFP4: *sc = static_cast<size_t>(n * (hidden / 16)); break;
     case RMSQ_FP8_GROUP128_COL:
     case RMSQ_FP8_GROUP64_COL:
-        *sc = static_cast<size_t>(col_stride_of(quant_mode, n) * (hidden / group_of(mode))) * 4;
+        *sc = static_cast<size_t>(col_stride_of(quant_mode, n) * (hidden / group_of(mode))) *
+              scale_elem_bytes(quant_mode);
         break;
-    default: *sc = static_cast<size_t>(n * (hidden / group_of(mode))) * 4; break;
+    default: *sc = static_cast<size_t>(n * (hidden / group_of(mode))) * scale_elem_bytes(quant_mode); break;
     }
 }
 
@@ -151,9 +158,10 @@ void set_programmatic_launch(bool on) { g_pdl.store(on, std::memory_order_relaxe
 extern "C" {
 
 int rmsq_set_pipeline_config(int chunks_per_thread, int stages, int ctas_per_sm, int rows_per_iter) {
-    if (chunks_per_thread != 0 && chunks_per_thread != 1 && chunks_per_thread != 2 && chunks_per_thread != 4)
+    if (chunks_per_thread != 0 && chunks_per_thread != 1 && chunks_per_thread != 2 && chunks_per_thread != 4 &&
+        chunks_per_thread != 8)
         return RMSQ_ERR_INVALID_ARG;
-    if (stages < 0 || stages > 8 || ctas_per_sm < 0 || ctas_per_sm > 8) return RMSQ_ERR_INVALID_ARG;
+    if (stages < 0 || stages > 8 || ctas_per_sm < 0 || ctas_per_sm > 32) return RMSQ_ERR_INVALID_ARG;
     if (rows_per_iter < 0 || rows_per_iter > 2) return RMSQ_ERR_INVALID_ARG;
     rmsq::set_pipe_tuning({chunks_per_thread, stages, ctas_per_sm, rows_per_iter});
     return RMSQ_OK;
@@ -190,7 +198,7 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     if (!aligned(x, 16) || !aligned(residual, 16) || !aligned(weight, 16) ||
         !aligned(residual_out, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4))
         return RMSQ_ERR_ALIGNMENT;
-    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, scale_elem_bytes(quant_mode))) return RMSQ_ERR_ALIGNMENT;
 
     size_t q_bytes = 0, sc_bytes = 0;
     sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
@@ -223,7 +231,8 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     la.scale_in = scale_in;
     la.eps = eps;
     la.mode = mode;
-    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.e8m0 = (quant_mode & (RMSQ_QUANT_E8M0 | RMSQ_QUANT_UE8M0)) != 0;
+    la.ue8m0 = (quant_mode & RMSQ_QUANT_UE8M0) != 0;
     la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(hidden);
@@ -257,7 +266,7 @@ int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_
     if (!needs_scale_in) scale_in = nullptr;
     if (!has_scales) out_scales = nullptr;
     if (!aligned(gate_up, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4)) return RMSQ_ERR_ALIGNMENT;
-    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, scale_elem_bytes(quant_mode))) return RMSQ_ERR_ALIGNMENT;
 
     size_t q_bytes = 0, sc_bytes = 0;
     sizes_of(quant_mode, n_tokens, d, &q_bytes, &sc_bytes);
@@ -277,7 +286,8 @@ int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_
     la.scales = out_scales;
     la.scale_in = scale_in;
     la.mode = mode;
-    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.e8m0 = (quant_mode & (RMSQ_QUANT_E8M0 | RMSQ_QUANT_UE8M0)) != 0;
+    la.ue8m0 = (quant_mode & RMSQ_QUANT_UE8M0) != 0;
     la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(d);
@@ -345,7 +355,7 @@ int rmsq_quant(const void* y, int quant_mode, const float* scale_in, void* out_q
     if (!needs_scale_in) scale_in = nullptr;
     if (!has_scales) out_scales = nullptr;
     if (!aligned(y, 16) || !aligned(out_q, 16) || !aligned(scale_in, 4)) return RMSQ_ERR_ALIGNMENT;
-    if (mode != RMSQ_NVFP4 && !aligned(out_scales, 4)) return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, scale_elem_bytes(quant_mode))) return RMSQ_ERR_ALIGNMENT;
     size_t q_bytes = 0, sc_bytes = 0;
     sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
     const Span Yi = span(y, static_cast<size_t>(n_tokens * hidden) * 2), Q = span(out_q, q_bytes),
@@ -363,7 +373,8 @@ int rmsq_quant(const void* y, int quant_mode, const float* scale_in, void* out_q
     la.scales = out_scales;
     la.scale_in = scale_in;
     la.mode = mode;
-    la.e8m0 = (quant_mode & RMSQ_QUANT_E8M0) != 0;
+    la.e8m0 = (quant_mode & (RMSQ_QUANT_E8M0 | RMSQ_QUANT_UE8M0)) != 0;
+    la.ue8m0 = (quant_mode & RMSQ_QUANT_UE8M0) != 0;
     la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
     la.n = static_cast<int>(n_tokens);
     la.hidden = static_cast<int>(hidden);

@@ -304,6 +304,30 @@ __device__ __forceinline__ void fp8_chunk2(const float (&a)[8], const float (&b)
     }
 }
 
+// Two chunks a, b under their own scales sa, sb (reciprocal brackets ra, rb):
+// the same test as fp8_chunk2, the products formed in packed pairs
+// (a[k] * ra, b[k] * rb).
+__device__ __forceinline__ void fp8_chunk2s(const float (&a)[8], const float (&b)[8], float sa, float sb,
+                                            Fp8Recips ra, Fp8Recips rb, uint2& ca, uint2& cb) {
+    uint32_t dna[4], dnb[4], diff = 0u;
+    const float2 dn = make_float2(ra.rdn, rb.rdn), up = make_float2(ra.rup, rb.rup);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float2 e0 = make_float2(a[2 * p], b[2 * p]), e1 = make_float2(a[2 * p + 1], b[2 * p + 1]);
+        const float2 d0 = mul2_rn(e0, dn), d1 = mul2_rn(e1, dn);
+        const float2 u0 = mul2_rn(e0, up), u1 = mul2_rn(e1, up);
+        dna[p] = e4m3x2(d0.x, d1.x);
+        dnb[p] = e4m3x2(d0.y, d1.y);
+        diff |= (dna[p] ^ e4m3x2(u0.x, u1.x)) | ((dnb[p] ^ e4m3x2(u0.y, u1.y)) << 16);
+    }
+    ca = make_uint2(dna[0] | (dna[1] << 16), dna[2] | (dna[3] << 16));
+    cb = make_uint2(dnb[0] | (dnb[1] << 16), dnb[2] | (dnb[3] << 16));
+    if (diff != 0u) {   // rare: redo both chunks exactly
+        ca = fp8_chunk_exact(a, sa);
+        cb = fp8_chunk_exact(b, sb);
+    }
+}
+
 // Pairwise tree over the squares of eight consecutive elements, in packed
 // pairs: (h0, h2) and (h1, h3) squared and added give the two level-1 nodes
 // h0^2 + h1^2 and h2^2 + h3^2 at once (likewise for h4..h7).

@@ -50,11 +50,9 @@ static __device__ unsigned int g_pipe_fault;
 #define RMSQ_PAIR_ACCESS 1
 #endif
 
-template <class E, int MODE, bool RES, int J, int R>
-__global__ void __launch_bounds__(kPipeMaxThreads,
-                                  (J == 4 ? 1 : RES ? RMSQ_PIPE_MIN_BLOCKS : RMSQ_PIPE_MIN_BLOCKS_NORES))
-pipe_entry(const RowArgs a, const int stages) {
-    pipe_body<E, MODE, RES, J, R>(a, stages, &g_pipe_fault);
+template <class E, int MODE, bool RES, int J>
+__global__ void __launch_bounds__(kPipeMaxThreads, 1) pipe_entry(const RowArgs a, const int stages) {
+    pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
 }
 
 template <class E, int MODE, bool RES>
@@ -63,34 +61,34 @@ const void* pick_direct(int J) {
     return reinterpret_cast<const void*>(&rows_kernel<E, MODE, RES, 2>);
 }
 
-// Two rows per iteration exist for one and two chunks per thread.
 template <class E, int MODE, bool RES>
-const void* pick_pipe(int J, int R) {
-    if (J == 1) return R == 2 ? reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1, 2>)
-                              : reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1, 1>);
-    if (J == 2) return R == 2 ? reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2, 2>)
-                              : reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2, 1>);
-    return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 4, 1>);
+const void* pick_pipe(int J) {
+    switch (J) {
+    case 1: return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 1>);
+    case 2: return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 2>);
+    case 4: return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 4>);
+    default: return reinterpret_cast<const void*>(&pipe_entry<E, MODE, RES, 8>);
+    }
 }
 
 template <class E, int MODE>
-const void* pick_res(bool res, bool pipe, int J, int R) {
-    if (pipe) return res ? pick_pipe<E, MODE, true>(J, R) : pick_pipe<E, MODE, false>(J, R);
+const void* pick_res(bool res, bool pipe, int J) {
+    if (pipe) return res ? pick_pipe<E, MODE, true>(J) : pick_pipe<E, MODE, false>(J);
     return res ? pick_direct<E, MODE, true>(J) : pick_direct<E, MODE, false>(J);
 }
 
 template <class E>
-const void* pick_kernel(int mode, bool res, bool pipe, int J, int R = 1) {
+const void* pick_kernel(int mode, bool res, bool pipe, int J) {
     switch (mode) {
-    case kFp8Static: return pick_res<E, kFp8Static>(res, pipe, J, R);
-    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, pipe, J, R);
-    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, pipe, J, R);
-    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, pipe, J, R);
-    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J, R);
-    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J, R);
-    case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J, R);
-    case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J, R);
-    case kNormOnly: return pick_res<E, kNormOnly>(res, pipe, J, R);
+    case kFp8Static: return pick_res<E, kFp8Static>(res, pipe, J);
+    case kFp8PerToken: return pick_res<E, kFp8PerToken>(res, pipe, J);
+    case kFp8G128Row: return pick_res<E, kFp8G128Row>(res, pipe, J);
+    case kFp8G128Col: return pick_res<E, kFp8G128Col>(res, pipe, J);
+    case kFp8G64Row: return pick_res<E, kFp8G64Row>(res, pipe, J);
+    case kFp8G64Col: return pick_res<E, kFp8G64Col>(res, pipe, J);
+    case kNvfp4: return pick_res<E, kNvfp4>(res, pipe, J);
+    case kNormAmax: return pick_res<E, kNormAmax>(res, pipe, J);
+    case kNormOnly: return pick_res<E, kNormOnly>(res, pipe, J);
     default: return nullptr;
     }
 }
@@ -198,28 +196,32 @@ inline RowArgs make_row_args(const LaunchArgs& la) {
     a.pair = RMSQ_PAIR_ACCESS && a.chunks % 2 == 0 && on(la.x, 32) && on(la.res, 32) &&
              on(la.res_out, 32) && on(la.q, 16);
     a.e8m0 = la.e8m0;
+    a.ue8m0 = la.ue8m0;
     a.col_stride = la.col_stride;
     return a;
 }
 
-// Launch shape of the pipelined kernel: chunks per thread J, rows per
-// iteration R, threads, ring stages and bytes.
+// Launch shape of the pipelined kernel: chunks per thread J, threads, ring
+// stages and bytes.
 struct PipePlan {
-    int J, R, threads, stages, smem;
+    int J, threads, stages, smem;
 };
+
+// Chunks per thread by default: 4 from 256 chunks (hidden 2048) up, so that
+// a warp's fixed per-row work (reductions, inverse RMS, scale) is spread
+// over 1024 elements; 2 for narrower rows.
+inline int pipe_default_j(int chunks) { return chunks >= 256 ? 4 : 2; }
 
 inline PipePlan pipe_plan(const RowArgs& a, bool res) {
     const PipeTuning tune = get_pipe_tuning();
-    auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
+    auto threads_for = [&](int j) { return ((a.chunks + 32 * j - 1) / (32 * j)) * 32; };
     PipePlan p;
-    p.J = a.chunks <= 1024 ? 2 : 4;
-    if ((tune.chunks_per_thread == 1 || tune.chunks_per_thread == 2 || tune.chunks_per_thread == 4) &&
-        threads_for(tune.chunks_per_thread) <= kPipeMaxThreads)
-        p.J = tune.chunks_per_thread;
+    p.J = pipe_default_j(a.chunks);
+    if (threads_for(p.J) > kPipeMaxThreads) p.J = 8;
+    const int tj = tune.chunks_per_thread;
+    if ((tj == 1 || tj == 2 || tj == 4 || tj == 8) && threads_for(tj) <= kPipeMaxThreads) p.J = tj;
     p.threads = threads_for(p.J);
-    const int row_slot = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
-    p.R = (tune.rows_per_iter == 2 && p.J <= 2 && 2 * row_slot <= kPipeSmemBudget) ? 2 : 1;
-    const int stage_bytes = p.R * row_slot;
+    const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
     p.stages = pipe_stages(stage_bytes);
     if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
         p.stages = tune.stages;
@@ -254,7 +256,7 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
 
     if (pipe) {
         const PipePlan p = pipe_plan(a, res);
-        const void* fn = pick_kernel<E>(la.mode, res, true, p.J, p.R);
+        const void* fn = pick_kernel<E>(la.mode, res, true, p.J);
         if (!fn) return cudaErrorInvalidValue;
         int grid = 0;
         err = pipe_grid(fn, p, a.n, &grid);

@@ -20,7 +20,8 @@ struct LaunchArgs {
     int hidden;
     int variant;            // kVariant*
     bool e8m0;              // dynamic scales rounded up to a power of two
-    int col_stride;         // column-major scale stride (n, or n rounded up to 4)
+    bool ue8m0;             // ... and stored as one UE8M0 byte each
+    int col_stride;         // column-major scale stride (n, or n rounded up to 16 bytes)
 };
 
 // LaunchArgs::mode of the norm alone (the kernels' Mode::kNormOnly).
@@ -37,7 +38,7 @@ struct PipeTuning {
     int chunks_per_thread;
     int stages;
     int ctas_per_sm;
-    int rows_per_iter;      // 1 or 2 (0 = automatic)
+    int rows_per_iter;      // accepted for the API, unused: one row per CTA iteration
 };
 PipeTuning get_pipe_tuning();
 void set_pipe_tuning(const PipeTuning& t);

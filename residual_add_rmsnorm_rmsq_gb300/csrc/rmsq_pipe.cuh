@@ -1,18 +1,24 @@
-// Pipelined row kernel: persistent CTAs, each walking groups of R rows
-// (rows blockIdx.x + (k*R + r) * gridDim.x for r < R); the x and residual rows
-// of the next `stages` groups are in flight as bulk asynchronous copies (TMA,
-// 1-D) into a ring of shared-memory stages while the current group is
-// computed.  One elected thread issues the copies; a stage is refilled right
-// after the CTA barrier that follows its last shared-memory read.  The weight
-// row is loaded once into registers (every row of the launch uses it).
+// Pipelined row kernel: persistent CTAs, each walking the rows blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the x and residual rows of the next `stages`
+// rows are in flight as bulk asynchronous copies (TMA, 1-D) into a ring of
+// shared-memory stages while the current row is computed.  One elected
+// thread issues the copies; a stage is refilled right after the CTA barrier
+// that follows its last shared-memory read.
 //
-// R = 2 interleaves two rows: their reductions share each CTA barrier, so the
-// latency of the per-row dependency chain (block reductions, IEEE divide and
-// square root) is paid once per two rows.
+// Data-to-thread mapping (coalesced): lane l of warp w holds the chunks
+// c = (w * J + j) * 32 + l, j = 0 .. J-1, of a row (a chunk is 16 bytes, 8
+// elements).  A warp's j-th access covers 512 contiguous bytes, so the ring
+// reads are free of bank conflicts and the residual and code stores are
+// fully coalesced.  The canonical pairwise tree of the sum of squares maps
+// onto it without reordering: the tree over a chunk's 8 elements, an xor
+// butterfly over the lanes for each j (bits 0..4 of the chunk index), the
+// tree over j (the next log2 J bits), then the tree over the warps' sums
+// (zero-padded, exact).
 //
-// Per row the arithmetic is the same as the direct kernel's (rmsq_rowmath.cuh):
-// the canonical pairwise tree for the sum of squares, correctly rounded
-// inverse RMS, fp32 y, then the quantisation mode.
+// Per row the arithmetic is the direct kernel's (rmsq_rowmath.cuh): the
+// canonical tree, correctly rounded inverse RMS, y = (h * inv) * w in fp32,
+// then the quantisation mode; only the order in which the threads visit the
+// elements differs, never a rounding.
 //
 // Every wait on a stage is bounded (mbar_wait_bounded).  If one ever gives up,
 // the CTA records it in `fault`, drains the copies it still has in flight
@@ -26,158 +32,335 @@ namespace rmsq {
 constexpr int kMaxStages = 8;
 constexpr int kPipeMaxThreads = 512;
 
-template <class E, int MODE, bool RES, int J, int R>
+// The warp's node of the canonical tree over its 32 * J chunks (the same
+// value in every lane): leaf trees of the lane's chunks, the lane butterfly
+// of each j (two j at a time in packed pairs), then the tree over j.
+template <int J>
+__device__ __forceinline__ float co_warp_sum(const float (&h)[J][8]) {
+    if constexpr (J == 1) {
+        return warp_tree_sum(leaf8_sumsq(h[0]));
+    } else {
+        float p[J];
+#pragma unroll
+        for (int j = 0; j < J; j += 2) {
+            float2 v = leaf8_sumsq2(h[j], h[j + 1]);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1)
+                v = add2_rn(v, make_float2(__shfl_xor_sync(kFull, v.x, o), __shfl_xor_sync(kFull, v.y, o)));
+            p[j] = v.x;
+            p[j + 1] = v.y;
+        }
+#pragma unroll
+        for (int len = J; len > 1; len >>= 1)
+#pragma unroll
+            for (int i = 0; i < len / 2; ++i) p[i] = __fadd_rn(p[2 * i], p[2 * i + 1]);
+        return p[0];
+    }
+}
+
+// Weights of the thread's chunks, loaded once per CTA: widened to fp32 for
+// one or two chunks per thread; kept packed (and widened per row) for more,
+// where the registers serve occupancy better.
+template <class E, int J>
+struct CoWeights {
+    static constexpr bool kPacked = J >= 4;
+    float f[kPacked ? 1 : J][8];
+    uint32_t p[kPacked ? J : 1][4];
+
+    __device__ __forceinline__ void load(const uint4* w, int c0, int chunks) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int c = c0 + 32 * j;
+            const uint4 v = c < chunks ? ld_weight(w + c) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if constexpr (kPacked) {
+                    p[j][k] = ws[k];
+                } else {
+                    f[j][2 * k] = E::lo(ws[k]);
+                    f[j][2 * k + 1] = E::hi(ws[k]);
+                }
+            }
+        }
+    }
+    // The packed words pass through an empty volatile asm on every use, so
+    // that the compiler cannot hoist their widening out of the row loop
+    // (which would bring back the registers the packing saves).
+    __device__ __forceinline__ float get(int j, int k) const {
+        if constexpr (kPacked) {
+            uint32_t v = p[j][k >> 1];
+            asm volatile("" : "+r"(v));
+            return (k & 1) ? E::hi(v) : E::lo(v);
+        } else {
+            return f[j][k];
+        }
+    }
+};
+
+// y = (h * inv) * w in place over h, in packed pairs (element k of chunks j
+// and j + 1; elements k and k + 1 of the one chunk when J == 1).
+template <class E, int J>
+__device__ __forceinline__ void co_y(float (&h)[J][8], const CoWeights<E, J>& w, float inv) {
+    const float2 iv = make_float2(inv, inv);
+    if constexpr (J == 1) {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float2 t = mul2_rn(mul2_rn(make_float2(h[0][k], h[0][k + 1]), iv),
+                                     make_float2(w.get(0, k), w.get(0, k + 1)));
+            h[0][k] = t.x;
+            h[0][k + 1] = t.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; j += 2)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 t = mul2_rn(mul2_rn(make_float2(h[j][k], h[j + 1][k]), iv),
+                                         make_float2(w.get(j, k), w.get(j + 1, k)));
+                h[j][k] = t.x;
+                h[j + 1][k] = t.y;
+            }
+    }
+}
+
+// E4M3 codes of the thread's chunks, chunk j divided by s[j], stored as 8
+// bytes per chunk (a warp's j-th store is 256 contiguous bytes).
+template <int J>
+__device__ __forceinline__ void co_store_fp8(const RowArgs& a, int row, const float (&y)[J][8], const float (&s)[J],
+                                             const Fp8Recips (&rc)[J], int c0) {
+    uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
+    uint2 codes[J];
+    if constexpr (J == 1) {
+        codes[0] = fp8_chunk(y[0], s[0], rc[0]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < J; j += 2) fp8_chunk2s(y[j], y[j + 1], s[j], s[j + 1], rc[j], rc[j + 1], codes[j], codes[j + 1]);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+        if (c0 + 32 * j < a.chunks) st_stream(qrow + c0 + 32 * j, codes[j]);
+}
+
+template <class E, int MODE, bool RES, int J>
 __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, unsigned int* fault) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
-    __shared__ __align__(16) float s_sum[2][R][32];
-    __shared__ float s_max[2][R][32];
+    __shared__ __align__(16) float s_sum[2][32];
+    __shared__ float s_max[32];
+    __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int c0 = tid * J;
+    const int c0 = warp * J * 32 + lane;   // the thread's first chunk; the others follow at strides of 32
     const int G = gridDim.x;
     const uint32_t row_bytes = static_cast<uint32_t>(a.chunks) * 16u;
-    const uint32_t slot_bytes = RES ? 2u * row_bytes : row_bytes;   // one row of x (+ residual)
-    const uint32_t stage_bytes = R * slot_bytes;
+    const uint32_t stage_bytes = RES ? 2u * row_bytes : row_bytes;   // one row of x (+ residual)
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
     }
-    // Slots of absent warps read as 0, in both halves of the double buffer and
-    // for every row of a group, whatever the CTA size (a one-warp CTA has
-    // only 32 threads to clear 2 * R * 31 slots).
-    for (int i = tid; i < 2 * R * 32; i += blockDim.x)
-        if ((i & 31) >= nwarps) (&s_sum[0][0][0])[i] = 0.0f;
+    // Slots of absent warps read as 0, in both halves of the double buffer,
+    // whatever the CTA size.
+    for (int i = tid; i < 64; i += blockDim.x)
+        if ((i & 31) >= nwarps) (&s_sum[0][0])[i] = 0.0f;
     allow_dependents();
     grid_dependency_wait();
     __syncthreads();
 
-    // Thread 0: start the copies of row group k into stage s.
-    uint64_t policy = 0;
-    auto issue = [&](int k, int s) {
-        unsigned char* dst = ring + (size_t)s * stage_bytes;
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (blockIdx.x + (k * R + r) * G < a.n) bytes += slot_bytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = blockIdx.x + (k * R + r) * G;
-            if (row >= a.n) break;
-            bulk_g2s(dst + r * slot_bytes, a.x + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
-            if constexpr (RES)
-                bulk_g2s(dst + r * slot_bytes + row_bytes, a.res + (int64_t)row * a.chunks, row_bytes,
-                         &full[s], policy);
-        }
-    };
-    // The first pass of the data-derived NVFP4 scale is followed by a pass
-    // that reads h again: without a residual h is x, kept in L2.
+    // Thread 0: start the copies of `row` into stage s.  The first pass of
+    // the data-derived NVFP4 scale is followed by a pass that reads h again:
+    // without a residual h is x, kept in L2 at normal priority.
     constexpr bool KEEP = MODE == kNormAmax;
+    uint64_t policy = 0;
+    auto issue = [&](int row, int s) {
+        unsigned char* dst = ring + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        bulk_g2s(dst, a.x + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
+        if constexpr (RES) bulk_g2s(dst + row_bytes, a.res + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
+    };
     if (tid == 0) {
         policy = (KEEP && !RES) ? l2_policy_evict_normal() : l2_policy_evict_first();
         for (int k = 0; k < stages; ++k) {
-            if (blockIdx.x + k * R * G >= a.n) break;
-            issue(k, k);
+            if (blockIdx.x + k * G >= a.n) break;
+            issue(blockIdx.x + k * G, k);
         }
     }
 
-    float wv[J][8];
-    {
-        uint4 wraw[J];
-#pragma unroll
-        for (int j = 0; j < J; ++j)
-            wraw[j] = (c0 + j < a.chunks) ? ld_weight(a.w + c0 + j) : make_uint4(0u, 0u, 0u, 0u);
-        widen_weights<E, J>(wraw, wv);
-    }
+    CoWeights<E, J> wts;
+    wts.load(a.w, c0, a.chunks);
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
-    __shared__ float s_rtab[MODE == kNvfp4 ? 128 : 1];
-    if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the first barrier
+    if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the first row's barrier
+    Fp8Recips rc_static = {0.0f, 0.0f};
+    if constexpr (MODE == kFp8Static) rc_static = fp8_recips(sin);
 
-    int k = 0;
+    int s = 0, buf = 0;
+    uint32_t parity = 0;
+    int row = blockIdx.x;
     bool faulted = false;
     float run_max = 0.0f;
-    for (;; ++k) {
-        const int row0 = blockIdx.x + k * R * G;
-        if (row0 >= a.n) break;
-        const int s = k % stages;
-        const uint32_t parity = static_cast<uint32_t>(k / stages) & 1u;
+    for (; row < a.n; row += G) {
         const bool ok = mbar_wait_bounded(&full[s], parity);
 
-        uint32_t hw[R][J][4];
-        float acc[R];
+        // h = T(x + r) (h = x without a residual), the write-back, widened.
+        float h[J][8];
+        {
+            const uint4* sx = reinterpret_cast<const uint4*>(ring + (size_t)s * stage_bytes);
+            uint4* ro = a.res_out + (int64_t)row * a.chunks;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int row = row0 + r * G;
-            acc[r] = 0.0f;
+            for (int j = 0; j < J; ++j) {
+                const int c = c0 + 32 * j;
+                uint32_t hw[4] = {0u, 0u, 0u, 0u};
+                if (ok && c < a.chunks) {
+                    const uint4 xv = sx[c];
+                    hw[0] = xv.x; hw[1] = xv.y; hw[2] = xv.z; hw[3] = xv.w;
+                    if constexpr (RES) {
+                        const uint4 rv = sx[a.chunks + c];
+                        const uint32_t rs[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-            for (int j = 0; j < J; ++j) hw[r][j][0] = hw[r][j][1] = hw[r][j][2] = hw[r][j][3] = 0u;
-            if (ok && row < a.n) {
-                const uint4* sx =
-                    reinterpret_cast<const uint4*>(ring + (size_t)s * stage_bytes + (size_t)r * slot_bytes);
-                uint4 xv[J], rv[J];
-#pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    xv[j] = rv[j] = make_uint4(0u, 0u, 0u, 0u);
-                    if (c0 + j < a.chunks) {
-                        xv[j] = sx[c0 + j];
-                        if constexpr (RES) rv[j] = sx[a.chunks + c0 + j];
+                        for (int k = 0; k < 4; ++k) hw[k] = E::add2(hw[k], rs[k]);
+                        const uint4 v = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        if constexpr (KEEP) st_keep(ro + c, v);
+                        else st_stream(ro + c, v);
                     }
                 }
-                acc[r] = combine_chunks<E, RES, J, KEEP>(xv, rv, hw[r], a.res_out + (int64_t)row * a.chunks,
-                                                         c0, a.chunks, a.pair);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) { h[j][2 * k] = E::lo(hw[k]); h[j][2 * k + 1] = E::hi(hw[k]); }
             }
         }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            acc[r] = warp_tree_sum(acc[r]);
-            if (lane == 0) s_sum[k & 1][r][warp] = acc[r];
-        }
+        const float wsum = co_warp_sum<J>(h);
+        if (lane == 0) s_sum[buf][warp] = wsum;
         // All reads of stage s are done once every thread is past this barrier.
         if (__syncthreads_or(!ok)) {
             faulted = true;
             break;
         }
-        if (tid == 0 && blockIdx.x + (k + stages) * R * G < a.n) issue(k + stages, s);
+        if (tid == 0 && row + stages * G < a.n) issue(row + stages * G, s);
 
-        float inv[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            inv[r] = inv_rms(warp_slots_tree_sum<kPipeMaxThreads / 32>(s_sum[k & 1][r], nwarps), a);
+        const float inv = inv_rms(warp_slots_tree_sum<kPipeMaxThreads / 32>(s_sum[buf], nwarps), a);
+        co_y<E, J>(h, wts, inv);   // h now holds y
 
-        if constexpr (MODE == kFp8PerToken && R > 1) {
-            // The rows' amax reductions share one barrier.
-            float y[R][J][8];
+        if constexpr (MODE == kNormAmax) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                compute_y<E, J>(hw[r], wv, inv[r], y[r]);
-                per_token_warp_amax<J>(y[r], s_max[k & 1][r], lane, warp);
-            }
+            for (int j = 0; j < J; ++j) run_max = max_abs8(run_max, h[j]);
+            if (tid == 0) static_cast<float*>(a.scales)[kWsInvOffset + row] = inv;
+        } else if constexpr (MODE == kNormOnly) {
+            uint4* yrow = reinterpret_cast<uint4*>(a.q) + (int64_t)row * a.chunks;
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+                if (c0 + 32 * j < a.chunks)
+                    st_stream(yrow + c0 + 32 * j, make_uint4(E::pack(h[j][0], h[j][1]), E::pack(h[j][2], h[j][3]),
+                                                             E::pack(h[j][4], h[j][5]), E::pack(h[j][6], h[j][7])));
+        } else if constexpr (MODE == kFp8Static) {
+            float sv[J];
+            Fp8Recips rc[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) { sv[j] = sin; rc[j] = rc_static; }
+            co_store_fp8<J>(a, row, h, sv, rc, c0);
+        } else if constexpr (MODE == kFp8PerToken) {
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) m = max_abs8(m, h[j]);
+            m = warp_max_nonneg(m);
+            if (lane == 0) s_max[warp] = m;
             __syncthreads();
+            m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
+            float sc = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+            if (a.e8m0) sc = pow2_ceil(sc);
+            if (tid == 0) store_scale(a, row, sc);
+            const Fp8Recips r1 = fp8_recips(sc);
+            float sv[J];
+            Fp8Recips rc[J];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-                if (row0 + r * G < a.n)
-                    per_token_finish<J>(a, row0 + r * G, y[r], s_max[k & 1][r], tid, nwarps);
+            for (int j = 0; j < J; ++j) { sv[j] = sc; rc[j] = r1; }
+            co_store_fp8<J>(a, row, h, sv, rc, c0);
+        } else if constexpr (MODE == kNvfp4) {
+            // 16-element blocks are chunk pairs (2m, 2m + 1): lane pairs.
+            const float gs = sin;
+            uint8_t* bsc = static_cast<uint8_t*>(a.scales) + (int64_t)row * (a.hidden / 16);
+            uint32_t* qrow = reinterpret_cast<uint32_t*>(a.q + (int64_t)row * (a.hidden / 2));
+            float r[J];
+            uint32_t sb[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                float m = max_abs8(0.0f, h[j]);
+                m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+                sb[j] = e4m3x2(__fmul_rn(__fdiv_rn(m, 6.0f), gs), 0.0f) & 0xffu;
+                r[j] = s_rtab[sb[j]];   // gs / decode(sb), 0 for a zero block scale
+            }
+#pragma unroll
+            for (int j = 0; j < J; j += (J == 1 ? 1 : 2)) {
+                uint32_t codes[2];
+                if constexpr (J == 1) {
+                    float v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) {
+                        const float2 t = mul2_rn(make_float2(h[0][k], h[0][k + 1]), make_float2(r[0], r[0]));
+                        v[k] = t.x; v[k + 1] = t.y;
+                    }
+                    codes[0] = e2m1x8(v);
+                } else {
+                    float v0[8], v1[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float2 t = mul2_rn(make_float2(h[j][k], h[j + 1][k]), make_float2(r[j], r[j + 1]));
+                        v0[k] = t.x; v1[k] = t.y;
+                    }
+                    codes[0] = e2m1x8(v0);
+                    codes[1] = e2m1x8(v1);
+                }
+#pragma unroll
+                for (int u = 0; u < (J == 1 ? 1 : 2); ++u) {
+                    const int c = c0 + 32 * (j + u);
+                    if (c < a.chunks) {
+                        st_stream(qrow + c, codes[u]);
+                        if ((lane & 1) == 0) bsc[c >> 1] = (uint8_t)sb[j + u];
+                    }
+                }
+            }
         } else {
-            // No barrier inside quantize_row for these modes (per-token only with R == 1,
-            // where every thread takes the r == 0 call).
+            // FP8 per group of G contiguous elements: G / 8 lanes of one j.
+            constexpr int GL = ModeTraits<MODE>::group / 8;
+            float sv[J];
+            Fp8Recips rc[J];
 #pragma unroll
-            for (int r = 0; r < R; ++r)
-                if (r == 0 || row0 + r * G < a.n)
-                    quantize_row<E, MODE, J>(a, row0 + r * G, hw[r], wv, inv[r], sin, s_rtab, s_max[k & 1][r],
-                                             tid, nwarps, run_max);
+            for (int j = 0; j < J; ++j) {
+                const float m = lanes_max<GL>(max_abs8(0.0f, h[j]));
+                float sc = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
+                if (a.e8m0) sc = pow2_ceil(sc);
+                sv[j] = sc;
+                rc[j] = fp8_recips(sc);
+                const int c = c0 + 32 * j;
+                if (c < a.chunks && (lane % GL) == 0) {
+                    const int g = c / GL;
+                    if constexpr (ModeTraits<MODE>::col) store_scale(a, (int64_t)g * a.col_stride + row, sc);
+                    else store_scale(a, (int64_t)row * (a.hidden / ModeTraits<MODE>::group) + g, sc);
+                }
+            }
+            co_store_fp8<J>(a, row, h, sv, rc, c0);
+        }
+
+        buf ^= 1;
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
-    if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max[0][0], tid, nwarps);
+    if constexpr (MODE == kNormAmax) flush_amax(a, run_max, s_max, tid, nwarps);
 
     if (faulted && tid == 0) {
         atomicOr(fault, 1u);
-        // Copies issued for row groups k .. k + stages - 1 may still be in flight.
-        for (int kk = k; kk < k + stages; ++kk) {
-            if (blockIdx.x + kk * R * G >= a.n) break;
-            mbar_wait_bounded(&full[kk % stages], static_cast<uint32_t>(kk / stages) & 1u);
+        // Copies issued for this row and the next stages - 1 rows may still be in flight.
+        for (int i = 0; i < stages; ++i) {
+            if (row + i * G >= a.n) break;
+            int ss = s + i;
+            uint32_t pp = parity;
+            if (ss >= stages) {
+                ss -= stages;
+                pp ^= 1u;
+            }
+            mbar_wait_bounded(&full[ss], pp);
         }
     }
 }

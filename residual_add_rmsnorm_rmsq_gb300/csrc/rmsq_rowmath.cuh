@@ -60,7 +60,8 @@ struct RowArgs {
     // residual_out start on 32 bytes and the codes on 16 bytes.
     bool pair;
     bool e8m0;        // dynamic scales rounded up to a power of two
-    int col_stride;   // column-major scale stride: n, or n rounded up to 4
+    bool ue8m0;       // ... and stored as one UE8M0 byte each (the biased exponent)
+    int col_stride;   // column-major scale stride: n, or n rounded up to 16 bytes
 };
 
 // The smallest power of two >= s for a positive normal s: s itself when its
@@ -68,6 +69,14 @@ struct RowArgs {
 __device__ __forceinline__ float pow2_ceil(float s) {
     const uint32_t u = __float_as_uint(s);
     return (u & 0x007fffffu) == 0u ? s : __uint_as_float((u & 0x7f800000u) + 0x00800000u);
+}
+
+// A dynamic FP8 scale into element i of the scale tensor: fp32, or with the
+// UE8M0 byte option its biased exponent (the scale is then a power of two,
+// 2^(byte - 127)).
+__device__ __forceinline__ void store_scale(const RowArgs& a, int64_t i, float s) {
+    if (a.ue8m0) static_cast<uint8_t*>(a.scales)[i] = static_cast<uint8_t>(__float_as_uint(s) >> 23);
+    else static_cast<float*>(a.scales)[i] = s;
 }
 
 template <int MODE> struct ModeTraits {
@@ -234,7 +243,7 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
     const float m = warp_max_nonneg(lane < nwarps ? s_max[lane] : 0.0f);
     float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
     if (a.e8m0) s = pow2_ceil(s);
-    if (tid == 0) static_cast<float*>(a.scales)[row] = s;
+    if (tid == 0) store_scale(a, row, s);
     store_fp8_codes<J>(a, row, y, s, tid * J);
 }
 
@@ -317,9 +326,8 @@ __device__ __forceinline__ void quantize_y(const RowArgs& a, int row, const floa
             if (a.e8m0) s = pow2_ceil(s);
             if (c0 < a.chunks && (c0 % (G / 8)) == 0) {
                 const int g = c0 / (G / 8);
-                float* sc = static_cast<float*>(a.scales);
-                if constexpr (ModeTraits<MODE>::col) sc[(int64_t)g * a.col_stride + row] = s;
-                else sc[(int64_t)row * (a.hidden / G) + g] = s;
+                if constexpr (ModeTraits<MODE>::col) store_scale(a, (int64_t)g * a.col_stride + row, s);
+                else store_scale(a, (int64_t)row * (a.hidden / G) + g, s);
             }
         }
         store_fp8_codes<J>(a, row, y, s, c0);

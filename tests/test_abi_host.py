@@ -55,6 +55,15 @@ def test_query_sizes(L):
     assert rq.query_sizes("fp8_group64_col+e8m0", 3, 256) == (768, 48)
     assert rq.query_sizes("fp8_group64_col+tma", 3, 256) == (768, 4 * 4 * 4)
     assert rq.query_sizes("fp8_group128_col+e8m0+tma", 9, 256) == (9 * 256, 2 * 12 * 4)
+    # UE8M0 bytes: one byte per scale; with TMA alignment the stride pads to 16
+    assert rq.query_sizes("fp8_per_token+ue8m0", 4, 64) == (256, 4)
+    assert rq.query_sizes("fp8_group64_row+ue8m0", 3, 256) == (768, 12)
+    assert rq.query_sizes("fp8_group128_col+ue8m0+tma", 9, 256) == (9 * 256, 2 * 16)
+    assert rq.query_sizes("fp8_group128_col+ue8m0+tma", 17, 256) == (17 * 256, 2 * 32)
+    for bad in ("fp8_static+ue8m0", "nvfp4+ue8m0"):
+        with pytest.raises(rq.RmsqError) as ei:
+            rq.query_sizes(bad, 4, 256)
+        assert ei.value.status == rq.ERR_INVALID_ARG
 
 
 A, B, C, D, E, F = (0x10000000 * k for k in range(1, 7))   # far-apart fake addresses
@@ -67,6 +76,13 @@ def call(L, x=A, res=B, w=C, eps=1e-6, mode=1, s_in=None, q=D, sc=E, ro=F, n=4, 
                                           vp(s_in) if s_in else None, vp(q) if q else None,
                                           vp(sc) if sc else None, vp(ro) if ro else None,
                                           n, H, dt, None)
+
+
+def test_byte_scales_need_no_word_alignment(L):
+    """fp32 scales must start on 4 bytes; UE8M0 bytes on any address (the
+    call then fails only on the missing device, after every argument check)."""
+    assert call(L, mode=1, sc=E + 2) == rq.ERR_ALIGNMENT
+    assert call(L, mode=1 | 0x40, sc=E + 2) in (rq.ERR_NO_DEVICE, rq.ERR_UNSUPPORTED_DEVICE)
 
 
 def test_argument_errors(L):
@@ -91,7 +107,8 @@ def test_argument_errors(L):
     assert call(L, mode=0x10 | 6, s_in=A + 0x100) == rq.ERR_INVALID_ARG   # E8M0 with NVFP4
     assert call(L, mode=0x20 | 2) == rq.ERR_INVALID_ARG                   # TMA with row-major scales
     assert call(L, mode=0x20 | 1) == rq.ERR_INVALID_ARG                   # TMA with per-token
-    assert call(L, mode=0x40 | 1) == rq.ERR_INVALID_ARG                   # unknown bit
+    assert call(L, mode=0x80 | 1) == rq.ERR_INVALID_ARG                   # unknown bit
+    assert call(L, mode=0x40 | 0, s_in=A + 0x100) == rq.ERR_INVALID_ARG   # UE8M0 with a static scale
     assert call(L, mode=0x10 | 1) == rq.ERR_NO_DEVICE                     # valid: reaches the device check
     assert call(L, mode=0x30 | 3, H=128) == rq.ERR_NO_DEVICE
 
@@ -176,7 +193,7 @@ def test_silu_mul_quant_argument_errors(L):
 
     assert act(dt=2) == rq.ERR_INVALID_ARG
     assert act(mode=7) == rq.ERR_INVALID_ARG
-    assert act(mode=0x40 | 1) == rq.ERR_INVALID_ARG              # unknown option bit
+    assert act(mode=0x80 | 1) == rq.ERR_INVALID_ARG              # unknown option bit
     assert act(n=-1) == rq.ERR_INVALID_ARG and act(d=0) == rq.ERR_INVALID_ARG
     assert act(d=60) == rq.ERR_UNSUPPORTED_SHAPE                  # not a multiple of 8
     assert act(mode=2, d=64 + 8) == rq.ERR_UNSUPPORTED_SHAPE      # not a multiple of the group

@@ -24,6 +24,7 @@ def test_mode_and_variant_names():
                                       "fp8_group64_row", "fp8_group64_col", "nvfp4")] == list(range(7))
     assert rq.mode_code("fp8_group128_col+e8m0+tma") == 3 | 0x10 | 0x20
     assert rq.mode_code("fp8_per_token+e8m0") == 1 | 0x10
+    assert rq.mode_code("fp8_group64_col+ue8m0+tma") == 5 | 0x40 | 0x20
     assert rq.VARIANTS == {"auto": 0, "direct": 1, "pipelined": 2}
     with pytest.raises(ValueError):
         rq.mode_code("fp8_group32_row")

@@ -226,14 +226,16 @@ def test_static_scale_sweep():
 
 @pytest.mark.parametrize("mode", ["fp8_group64_col", "fp8_per_token", "nvfp4", "fp8_static"])
 def test_pipelined_launch_shapes_do_not_change_results(mode):
-    """Chunks per thread, ring depth, CTAs per SM and rows per iteration
-    (including an odd row count, so the last two-row group has one row)."""
+    """Chunks per thread (1 to 8: one to sixteen warps per row), ring depth and
+    CTAs per SM, on an odd row count; the rows-per-iteration setting is
+    accepted and changes nothing."""
     wl = ri.make_workload("shapes", 701, 4096, res_sigma=2.0, seed=36)
     s_in = 0.05 if mode == "fp8_static" else None
     want = oracle.run_workload(wl, mode, scale_in=s_in, nthreads=8)
     try:
         for J, stages, cps, rows in ((1, 2, 1, 1), (2, 1, 2, 1), (4, 8, 3, 1), (2, 6, 0, 0), (0, 3, 4, 1),
-                                     (2, 2, 0, 2), (1, 1, 2, 2), (2, 3, 1, 2), (4, 2, 0, 2)):
+                                     (2, 2, 0, 2), (1, 1, 2, 2), (2, 3, 1, 2), (4, 2, 0, 2), (8, 2, 0, 0),
+                                     (8, 1, 12, 0), (4, 3, 20, 0)):
             rq.set_pipeline_config(J, stages, cps, rows)
             got = P.run_gpu(wl, mode, want["scale_in"], variant="pipelined")
             P.compare(got, want, mode, f"{mode} shape J{J} s{stages} c{cps} r{rows}")
