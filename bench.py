@@ -3,8 +3,10 @@
 
 One step = one launch of the fused kernel over the whole batch (all steps of
 the path: residual add, residual write-back, RMSNorm, scale, quantise, pack).
-Default workload: the Llama-8B-shaped layer, 4096 tokens x 4096 hidden bf16,
-residual add on, FP8 E4M3 dynamic per-token scales.
+Default workload: the DeepSeek-V3-shaped layer, 8192 tokens x 7168 hidden
+bf16 with 1 % outlier channels, residual add on, FP8 E4M3 per-group scales
+(group 128, row-major) -- the largest configuration of the path that fits one
+GPU.
 
 Prints ONE JSON line (rank 0).  ``value`` is algorithmic HBM GB/s (bytes the
 op must move / device time), whole job over all ranks.  Inputs are resident in
@@ -12,7 +14,11 @@ HBM before the timed region; consecutive steps rotate over buffer sets whose
 total size is more than 4x the L2 cache, so no step reads the previous step's
 data from L2.  ``e2e`` is the same metric with every step's inputs copied from
 pinned host memory and its outputs read back inside the timed region (copies
-in, launches and copies out pipelined on three streams).
+in, launches and copies out pipelined on three streams).  ``parity`` compares
+the outputs of a timed step with the oracle over every row (computed in the
+CPU-baseline leg, after the timed region).  ``clocks`` are nvidia-smi samples
+over a window of continuous replays of the same launches that brackets the
+timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -291,10 +297,13 @@ class ActBuffers:
         if mode == "fp8_static":
             self.scale_in = torch.tensor([wl.static_scale or 0.05], dtype=torch.float32, device="cuda")
         elif mode == "nvfp4":
-            # gs = 2688 / amax over the batch, from the library's per-token scales
-            # (amax = 448 * scale), computed once outside the timed region
-            _, sc = rq.silu_mul_quant(g0, "fp8_per_token")
-            self.scale_in = (2688.0 / (sc.max() * 448.0)).reshape(1).float()
+            # the workload's rule, gs = 2688 / amax of the activations over the
+            # batch: the library's own a = silu(g) * u (its elementwise debug
+            # entry), its amax and one fp32 division, outside the timed region
+            a = rq.debug_activation("silu_mul", g0[:, :d].float().contiguous(), g0[:, d:].float().contiguous())
+            amax = a.abs().max().reshape(1)
+            self.scale_in = torch.tensor([2688.0], dtype=torch.float32, device="cuda") / amax
+            del a
         else:
             self.scale_in = None
         self.gu, self.q, self.sc = [], [], []
@@ -365,47 +374,72 @@ class QkBuffers:
                              w.neox, stream=stream, variant=VARIANT)
 
 
+class Replayer:
+    """The launches of a timed region as CUDA graphs: one graph of one launch
+    per buffer set (in rotation order) replayed steps // sets times, plus a
+    graph of the remaining launches, so the device runs the K kernels back to
+    back instead of waiting on Python between them.  Every launch goes through
+    the same public call.  Eager warm-up launches come first (they also fill
+    the library's per-function caches before capture)."""
+
+    def __init__(self, torch, bufs, steps, warmup, stream):
+        self.torch, self.bufs, self.steps, self.stream = torch, bufs, steps, stream
+
+        def capture(count):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+                for i in range(count):
+                    bufs.launch(i % bufs.sets, stream)
+            return g
+
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, bufs.sets)):
+                bufs.launch(i % bufs.sets, stream)
+            torch.cuda.synchronize()
+            self.reps, rem = divmod(steps, bufs.sets)
+            self.g_full = capture(bufs.sets) if self.reps else None
+            self.g_rem = capture(rem) if rem else None
+            for g in (self.g_full, self.g_rem):          # one untimed replay of each graph
+                if g is not None:
+                    g.replay()
+            torch.cuda.synchronize()
+
+    def timed(self) -> float:
+        """Mean device time per launch (ms) over exactly `steps` launches,
+        CUDA events on the launching stream."""
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for _ in range(self.reps):
+                self.g_full.replay()
+            if self.g_rem is not None:
+                self.g_rem.replay()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / self.steps
+
+    def soak(self, seconds: float) -> int:
+        """Untimed replays of the same launches for about `seconds` of wall
+        time (the device kept as busy as in the timed region); returns the
+        launches run."""
+        torch = self.torch
+        g = self.g_full or self.g_rem
+        per = self.bufs.sets if self.g_full is not None else self.steps
+        done, t0 = 0, time.time()
+        with torch.cuda.stream(self.stream):
+            while time.time() - t0 < seconds:
+                for _ in range(16):
+                    g.replay()
+                done += 16 * per
+                torch.cuda.synchronize()
+        return done
+
+
 def time_launches(torch, rq, wl, mode, bufs, steps, warmup, stream):
-    """Mean device time per launch (ms) over exactly `steps` launches, CUDA
-    events on `stream`.
-
-    The launches (one per buffer set, in rotation order) are captured once in
-    a CUDA graph through the same public call; the timed region replays it
-    steps // sets times plus a graph of the remaining launches, so the device
-    runs the K kernels back to back instead of waiting on Python between
-    them.  Eager warm-up launches come first (they also fill the library's
-    per-function caches before capture).
-    """
-    def launch(i):
-        bufs.launch(i % bufs.sets, stream)
-
-    def capture(count):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-            for i in range(count):
-                launch(i)
-        return g
-
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, bufs.sets)):
-            launch(i)
-        torch.cuda.synchronize()
-        reps, rem = divmod(steps, bufs.sets)
-        g_full = capture(bufs.sets) if reps else None
-        g_rem = capture(rem) if rem else None
-        for g in (g_full, g_rem):          # one untimed replay of each graph
-            if g is not None:
-                g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / steps
+    """Mean device time per launch (ms) over exactly `steps` launches (see
+    Replayer)."""
+    return Replayer(torch, bufs, steps, warmup, stream).timed()
 
 
 def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
@@ -472,17 +506,25 @@ def e2e_measure(torch, rq, wl, mode, bufs, steps, stream):
     return ms, h2d, d2h
 
 
-def cpu_baseline(wl, mode, budget_s: float = 20.0) -> dict:
+def _oracle_scale_in(wl, mode, scale_in):
+    return scale_in if scale_in is not None else (wl.static_scale if mode == "fp8_static" else 0.0)
+
+
+def cpu_baseline(wl, mode, scale_in=None, budget_s: float = 20.0) -> dict:
     """The oracle as it stands, row-parallel over the process's cores, on a
     bounded prefix of the workload's rows; median of 3 runs."""
     import oracle
     cores = len(os.sched_getaffinity(0))
-    scale = wl.static_scale if mode == "fp8_static" else (1000.0 if mode == "nvfp4" else 0.0)
+    scale = _oracle_scale_in(wl, mode, scale_in)
     rows = min(wl.n_tokens, 256)
-    while True:
-        t = time.perf_counter()
+
+    def run(rows):
         oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
                    eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+
+    while True:
+        t = time.perf_counter()
+        run(rows)
         dt = time.perf_counter() - t
         if rows >= wl.n_tokens or dt * 3 * 4 > budget_s / 2:
             break
@@ -490,14 +532,50 @@ def cpu_baseline(wl, mode, budget_s: float = 20.0) -> dict:
     times = []
     for _ in range(3):
         t = time.perf_counter()
-        oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
-                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+        run(rows)
         times.append(time.perf_counter() - t)
     med = statistics.median(times)
     nbytes = algorithmic_bytes(mode, rows, wl.hidden, 2, wl.residual is not None)
     return {"value": round(nbytes / med / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "tokens_per_s": round(rows / med, 1),
             "sample": f"first {rows} of {wl.n_tokens} rows, median of 3 runs, {cores} threads"}
+
+
+def parity_vs_oracle(wl, mode, scale_in, got: dict) -> dict:
+    """Part of the CPU-baseline leg, run after the timed region: the oracle on
+    every row of the workload, compared element by element with the outputs
+    of one timed step (`got`: host arrays q, scales, residual_out).  Codes:
+    the number of elements that differ and the largest difference in code
+    steps; scales and residual_out: whether they are identical bit for bit."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    want = oracle.run(wl.x, wl.residual, wl.weight, eps=wl.eps, mode=mode,
+                      scale_in=_oracle_scale_in(wl, mode, scale_in), dtype=wl.dtype, nthreads=cores)
+    if mode == "nvfp4":
+        g = np.stack([got["q"] & 0xF, got["q"] >> 4], -1).astype(np.int32)
+        w = np.stack([want["q"] & 0xF, want["q"] >> 4], -1).astype(np.int32)
+        sg, sw, mg, mw = g >> 3, w >> 3, g & 7, w & 7
+    else:
+        g, w = got["q"].astype(np.int32), want["q"].astype(np.int32)
+        sg, sw, mg, mw = g >> 7, w >> 7, g & 0x7F, w & 0x7F
+    steps = np.where(sg == sw, np.abs(mg - mw), mg + mw)
+    bad = int(np.count_nonzero(steps))
+    out = {"elements": int(steps.size), "mismatches": bad, "fraction": bad / max(1, steps.size),
+           "max_step": int(steps.max()) if steps.size else 0, "bar": "<= 1 step on <= 1e-4 of the codes"}
+    if want["scales"] is not None:
+        ws = want["scales"].reshape(-1).view(np.uint8)
+        gs = got["scales"].reshape(-1).view(np.uint8)
+        out["scales_bitexact"] = bool(np.array_equal(ws, gs))
+    if want["residual_out"] is not None:
+        out["residual_bitexact"] = bool(np.array_equal(want["residual_out"], got["residual_out"]))
+    return out
+
+
+def workload_config(name: str, wl, mode: str) -> dict:
+    """The config object of the JSON line, the same in both arms."""
+    return {"workload": name, "n_tokens": wl.n_tokens, "hidden": wl.hidden, "quant_mode": mode,
+            "residual": wl.residual is not None, "eps": wl.eps, "act_dtype": wl.dtype,
+            "l2": "inputs larger than L2: consecutive GPU steps rotate over buffer sets of > 4x L2"}
 
 
 # --------------------------------------------------------------------------- arms
@@ -535,11 +613,9 @@ def run_reference(args, rank, world):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "tokens_per_s": round(rows / dt, 1),
-        "config": {"workload": args.workload, "n_tokens": wl.n_tokens, "hidden": wl.hidden,
-                   "quant_mode": mode, "residual": wl.residual is not None,
-                   "step_sample_rows": rows, "l2": "host (CPU oracle)"},
+        "config": workload_config(args.workload, wl, mode),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"first {rows} of {wl.n_tokens} rows per step"},
+                         "sample": f"first {rows} of {wl.n_tokens} rows per step (host cores, no GPU)"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -565,24 +641,35 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # warm-up, then the timed region (clocks sampled during it)
+    # warm-up, then the timed region, bracketed by untimed replays of the same
+    # launches so that the clock samples cover a window of the same load
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0))) if rank == 0 else None
-    time_launches(torch, rq, wl, mode, bufs, 1, args.warmup, stream)
+    rep = Replayer(torch, bufs, args.steps, args.warmup, stream)
     barrier()
     t_wall0 = time.time()
-    ms = time_launches(torch, rq, wl, mode, bufs, args.steps, 0, stream)
+    soaked = rep.soak(args.clock_window / 2)
+    ms = rep.timed()
+    soaked += rep.soak(args.clock_window / 2)
     t_wall1 = time.time()
     barrier()
     ms = max_over_ranks(ms, dist, "cuda")
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     if sampler:
         sampler.stop()
+        clocks["window"] = (f"{(t_wall1 - t_wall0) * 1e3:.0f} ms of back-to-back replays of the timed launches "
+                            f"({soaked} untimed + {args.steps} timed)")
 
     per_launch = bufs.bytes
     value, tokens_s = whole_job_rates(per_launch, wl.n_tokens, world, ms)
 
     if rank != 0:
         return
+    # outputs of one timed step (buffer set 0), for the parity check below
+    got = {"q": bufs.q[0].cpu().numpy(),
+           "scales": None if bufs.sc[0] is None else bufs.sc[0].cpu().numpy(),
+           "residual_out": None if bufs.ro[0] is None else
+           bufs.ro[0].view(torch.int16).cpu().numpy().view(np.uint16)}
+    scale_in = None if bufs.scale_in is None else float(bufs.scale_in.cpu().item())
     peak, peak_kind = measured_peak()
     achieved = per_launch / (ms / 1e3) / 1e9
     digest = kernel_digest()
@@ -598,11 +685,10 @@ def run_ours(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, shapes of the pages' workloads)",
         "tokens_per_s": round(tokens_s, 1),
-        "config": {"workload": args.workload, "n_tokens": wl.n_tokens, "hidden": wl.hidden,
-                   "quant_mode": mode, "residual": bufs.res, "eps": wl.eps, "variant": VARIANT,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"rotating {bufs.sets} buffer sets ({bufs.sets * per_launch / 1e6:.0f} MB > 4x L2)",
-                   "bytes_per_step": per_launch},
+        "config": workload_config(args.workload, wl, mode),
+        "launch": {"variant": VARIANT, "kernel": kname, "buffer_sets": bufs.sets,
+                   "bytes_per_step": per_launch,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -616,24 +702,46 @@ def run_ours(args, rank, world, dist):
         line["modes"] = sweep(torch, rq, stream, peak, args)
         line["decode_us_per_call"] = decode_sweep(torch, rq, stream, args)
     if not args.no_cpu and world == 1:
-        line["cpu_baseline"] = cpu_baseline(wl, mode)
+        line["cpu_baseline"] = cpu_baseline(wl, mode, scale_in)
+        line["parity"] = parity_vs_oracle(wl, mode, scale_in, got)
     print(json.dumps(line), flush=True)
 
 
+def eager_us_per_call(torch, bufs, calls, stream) -> float:
+    """Microseconds per call when the calls are issued one by one from the
+    host on one stream (no graph): what an engine without graph capture sees,
+    host launch cost included."""
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            bufs.launch(i % bufs.sets, stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(calls):
+            bufs.launch(i % bufs.sets, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / calls
+
+
 def decode_sweep(torch, rq, stream, args):
-    """Decode batches (fp16, hidden 8192, n = 1 .. 256): device microseconds
-    per call, back to back from a CUDA graph, every quant mode +- residual.
+    """Decode batches (fp16, hidden 8192, n = 1 .. 256), every quant mode +-
+    residual: microseconds per call replayed back to back from a CUDA graph
+    ("graph"), and issued one by one from the host on a stream ("stream").
     Eight buffer sets rotate (at most 15 MB in all), so these inputs are
     L2-resident, as a decode step's activations usually are."""
     import rmsq_inputs as ri
-    out = {}
+    out = {"graph": {}, "stream": {}}
     for residual in (True, False):
         for n in ri.DECODE_TOKENS:
             wl = ri.decode(n, residual=residual)
             for mode in ("fp8_static", "fp8_per_token", "fp8_group128_row", "nvfp4"):
+                key = f"{mode}{'' if residual else '_nores'}"
                 bufs = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1, max_sets=8)
                 ms = time_launches(torch, rq, wl, mode, bufs, args.decode_steps, 5, stream)
-                out.setdefault(f"{mode}{'' if residual else '_nores'}", {})[str(n)] = round(ms * 1e3, 3)
+                out["graph"].setdefault(key, {})[str(n)] = round(ms * 1e3, 3)
+                out["stream"].setdefault(key, {})[str(n)] = round(
+                    eager_us_per_call(torch, bufs, args.decode_steps, stream), 3)
                 del bufs
     torch.cuda.empty_cache()
     return out
@@ -712,7 +820,9 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama_fp8_per_token")
+    ap.add_argument("--workload", default="dsv3_fp8_group128_row")
+    ap.add_argument("--clock-window", type=float, default=0.4,
+                    help="seconds of untimed replays around the timed region, for the clock samples")
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=200)

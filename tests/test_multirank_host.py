@@ -73,7 +73,11 @@ def test_reference_arm_json_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
-    assert d["config"]["workload"] == "llama_fp8_per_token"
+    assert d["config"]["workload"] == "dsv3_fp8_group128_row"
+    # the same config object as the GPU arm prints for this workload
+    import rmsq_inputs as ri
+    assert d["config"] == json.loads(json.dumps(bench.workload_config("dsv3_fp8_group128_row", ri.dsv3(8192),
+                                                                       "fp8_group128_row")))
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
