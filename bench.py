@@ -177,7 +177,9 @@ def profiled_traffic(kernel_name: str, digest: str):
 def kernel_name(wl, mode: str, residual: bool, torch) -> str:
     """Name (as ncu prints it, without the namespace) of the row kernel the
     library launches for this workload: the pipelined kernel from 4 rows per SM
-    on (direct kernel below), 2 chunks of 8 per thread up to hidden 8192."""
+    on (direct kernel below); its chunks per thread: 2 with a residual, 4
+    without from hidden 2048 up, doubled while a row would need more than 512
+    threads)."""
     import residual_add_rmsnorm_rmsq_gb300 as rq
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     pipelined = VARIANT == "pipelined" or (VARIANT == "auto" and wl.n_tokens >= 4 * sms)
@@ -185,7 +187,10 @@ def kernel_name(wl, mode: str, residual: bool, torch) -> str:
     m = rq.MODES["nvfp4" if mode == "nvfp4_dynamic" else mode]
     chunks = wl.hidden // 8
     if pipelined:
-        return f"pipe_entry<{e}, {m}, {int(residual)}, {2 if chunks <= 1024 else 4}, 1>"
+        j = 4 if (not residual and chunks >= 256) else 2
+        while j < 8 and -(-chunks // (32 * j)) * 32 > 512:
+            j *= 2
+        return f"pipe_entry<{e}, {m}, {int(residual)}, {j}>"
     return f"rows_kernel<{e}, {m}, {int(residual)}, {1 if chunks <= 1024 else 2}>"
 
 

@@ -323,6 +323,45 @@ int rmsq_qk_norm_rope_ex(void *qkv, const int64_t *positions, const float *cos_s
                          int64_t n_tokens, int num_q_heads, int num_kv_heads, int head_dim, int is_neox,
                          int dtype, void *stream, int variant);
 
+/* Most ranks rmsq_allreduce_add_rmsnorm_quant sums. */
+#define RMSQ_MAX_ALLREDUCE_RANKS 8
+
+/*
+ * rmsq_allreduce_add_rmsnorm_quant — the tensor-parallel all-reduce fused with
+ * the residual add, RMSNorm and quantisation (vLLM docs "Fusion torch.compile
+ * passes", section "AllReduce + RMSNorm (fuse_allreduce_rms)": all-reduce ->
+ * RMSNorm (+ residual add) (-> FP8 static or NVFP4 quantisation), worth it at
+ * small token counts).  One-shot, by loads: for every row the kernel reads
+ * the row of each rank's partial sums, adds them in rank order in fp32 and
+ * rounds the sum once to T:
+ *   x = T(fp32(partials[0]) + fp32(partials[1]) + ... + fp32(partials[n_ranks-1]))
+ * and then computes exactly rmsq_fused_add_rmsnorm_quant on that x (every
+ * quant_mode and option; the same outputs and layouts).
+ *  partials     HOST array of n_ranks (1 .. RMSQ_MAX_ALLREDUCE_RANKS) device
+ *               pointers, each T[n_tokens, hidden], 16-byte aligned, that
+ *               the current device can read: its own memory, or another
+ *               GPU's memory mapped into this device's address space (CUDA
+ *               IPC or peer access, set up by the caller; the library maps
+ *               nothing).  The pointer values are copied at the call.
+ *  Every other argument as in rmsq_fused_add_rmsnorm_quant (residual may be
+ *  NULL; residual_out == residual is the in-place update).
+ * Ordering: the kernel does not wait for other GPUs.  Every rank's partials
+ * must be complete before the launch in `stream`'s order (for instance a
+ * stream wait on an event each producer recorded, or a host barrier after
+ * the producers synchronised); with peer buffers the caller also keeps them
+ * alive and unmodified until the call completes.  Each rank that needs the
+ * result calls this on its own device with the same partials (a one-shot
+ * all-reduce), or on its own slice of rows (pointers and n_tokens of that
+ * slice) followed by an all-gather of the outputs (a two-shot one).
+ * No output may overlap a partial; RMSQ_ERR_INVALID_ARG for a NULL array or
+ * pointer or a bad n_ranks.  Asynchronous on `stream`.
+ */
+int rmsq_allreduce_add_rmsnorm_quant(const void *const *partials, int n_ranks, const void *residual,
+                                     const void *weight, float eps, int quant_mode,
+                                     const float *scale_in, void *out_q, void *out_scales,
+                                     void *residual_out, int64_t n_tokens, int64_t hidden,
+                                     int dtype, void *stream);
+
 /* Largest d (activation width) of rmsq_silu_mul_quant. */
 #define RMSQ_ACT_MAX_D 32768
 

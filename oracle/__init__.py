@@ -130,6 +130,9 @@ def _configure(L):
     L.oracle_silu.argtypes, L.oracle_silu.restype = [f32], f32
     L.oracle_silu_array.argtypes = [vp, vp, i64]
     L.oracle_silu_array.restype = None
+    L.oracle_allreduce_add_rmsnorm_quant.argtypes = [vp, ctypes.c_int, vp, vp, f32, ctypes.c_int, f32, vp, vp, vp,
+                                                     vp, i64, i64, ctypes.c_int, ctypes.c_int]
+    L.oracle_allreduce_add_rmsnorm_quant.restype = ctypes.c_int
     L.oracle_quant_f32.argtypes = [vp, ctypes.c_int, f32, vp, vp, i64, i64, ctypes.c_int]
     L.oracle_quant_f32.restype = ctypes.c_int
     return L
@@ -230,6 +233,27 @@ def run(x, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
         _ptr(x), _ptr(res), _ptr(weight), ctypes.c_float(eps), mode_code(mode),
         ctypes.c_float(scale_in), _ptr(q), _ptr(scales), _ptr(res_out), _ptr(y),
         n, H, DTYPES[dtype], int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return {"q": q, "scales": scales, "residual_out": res_out, "y": y}
+
+
+def run_allreduce(partials, residual, weight, *, eps: float, mode: str, scale_in: float = 0.0,
+                  dtype: str = "bf16", want_y: bool = False, nthreads: int = 1) -> dict:
+    """All-reduce + the fused op (reading R22): ``partials`` uint16 [R, n, H]
+    (one [n, H] tensor per rank); outputs as for ``run``."""
+    p = np.ascontiguousarray(partials, np.uint16)
+    R, n, H = p.shape
+    weight = np.ascontiguousarray(weight, np.uint16)
+    res = None if residual is None else np.ascontiguousarray(residual, np.uint16)
+    q = np.zeros((n, H // 2) if base_mode(mode) == "nvfp4" else (n, H), np.uint8)
+    ss = scale_shape(mode, n, H)
+    scales = None if ss is None else np.zeros(ss[0], ss[1])
+    res_out = None if res is None else np.zeros((n, H), np.uint16)
+    y = np.zeros((n, H), np.float32) if want_y else None
+    rc = lib().oracle_allreduce_add_rmsnorm_quant(
+        _ptr(p), R, _ptr(res), _ptr(weight), ctypes.c_float(eps), mode_code(mode), ctypes.c_float(scale_in),
+        _ptr(q), _ptr(scales), _ptr(res_out), _ptr(y), n, H, DTYPES[dtype], int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle failed with code {rc}")
     return {"q": q, "scales": scales, "residual_out": res_out, "y": y}

@@ -57,6 +57,11 @@
  *  R18 TMA-aligned option for column-major group scales: the stride between
  *      the scale columns of consecutive groups is n_tokens rounded up to a
  *      multiple of 4 (16 bytes); the padding entries are not written.
+ *  R22 all-reduce + RMSNorm (vLLM docs, same page, section "AllReduce +
+ *      RMSNorm (fuse_allreduce_rms)": the tensor-parallel all-reduce fused
+ *      with the following residual add, RMSNorm and quantisation): the
+ *      reduced activation is the rank-order binary32 sum of the ranks'
+ *      partial tensors, rounded once to T; it is the x of the fused op.
  *  R21 UE8M0 byte option (the same item of the blog): the power-of-two scale
  *      of R17 is stored as one byte, its biased binary32 exponent (the UE8M0
  *      encoding: byte e stands for 2^(e - 127)), in the same layouts; with
@@ -547,6 +552,29 @@ int oracle_silu_mul_quant(const uint16_t *gate_up, int mode, float scale_in, uin
     OracleArgs a = {gate_up, NULL, NULL, 0.0f, mode, scale_in, out_q, out_scales,
                     NULL, y_out, n, d, dtype, 1, NULL, e8m0, col_stride};
     return run_rows(&a, nthreads);
+}
+
+/* R22: all-reduce + residual add + RMSNorm + quantisation.  partials holds
+ * nranks [n, H] tensors one after the other; x = T(sum of their widened
+ * values in rank order, binary32), then the fused op on x.  Returns 0, or -1
+ * / -2 like oracle_fused_add_rmsnorm_quant. */
+int oracle_allreduce_add_rmsnorm_quant(const uint16_t *partials, int nranks, const uint16_t *residual,
+                                       const uint16_t *weight, float eps, int mode, float scale_in,
+                                       uint8_t *out_q, void *out_scales, uint16_t *residual_out, float *y_out,
+                                       int64_t n, int64_t H, int dtype, int nthreads)
+{
+    if (!partials || nranks < 1 || n < 0 || H <= 0 || (dtype != OR_BF16 && dtype != OR_FP16)) return -1;
+    uint16_t *x = (uint16_t *)malloc((size_t)(n * H > 0 ? n * H : 1) * sizeof(uint16_t));
+    if (!x) return -2;
+    for (int64_t i = 0; i < n * H; ++i) {
+        float acc = widen(dtype, partials[i]);
+        for (int r = 1; r < nranks; ++r) acc = acc + widen(dtype, partials[(int64_t)r * n * H + i]);
+        x[i] = narrow(dtype, acc);
+    }
+    const int rc = oracle_fused_add_rmsnorm_quant(x, residual, weight, eps, mode, scale_in, out_q, out_scales,
+                                                  residual_out, y_out, n, H, dtype, nthreads);
+    free(x);
+    return rc;
 }
 
 /* Step 5 alone (R4-R8, R17, R18) on given fp32 rows y [n, d]: the

@@ -60,6 +60,7 @@ EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic", "rmsq_nvfp4_dynamic_workspace_bytes",
            "rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc", "rmsq_silu_mul_quant",
            "rmsq_fused_add_rmsnorm", "rmsq_quant", "rmsq_qk_norm_rope", "rmsq_qk_norm_rope_ex",
+           "rmsq_allreduce_add_rmsnorm_quant",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
            "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
@@ -105,6 +106,9 @@ def load(path: str | None = None):
         L.rmsq_qk_norm_rope.restype = ci
         L.rmsq_qk_norm_rope_ex.argtypes = [vp, vp, vp, i64, vp, vp, f32, i64, ci, ci, ci, ci, ci, vp, ci]
         L.rmsq_qk_norm_rope_ex.restype = ci
+        L.rmsq_allreduce_add_rmsnorm_quant.argtypes = [ctypes.POINTER(vp), ci, vp, vp, f32, ci, vp, vp, vp, vp,
+                                                       i64, i64, ci, vp]
+        L.rmsq_allreduce_add_rmsnorm_quant.restype = ci
         L.rmsq_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
         L.rmsq_quant.restype = ci
         L.rmsq_silu_mul_quant.argtypes = [vp, ci, vp, vp, vp, i64, i64, ci, vp]
@@ -215,6 +219,57 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor | None, weig
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_quant")
     return out_q, out_scales, residual_out
+
+
+MAX_ALLREDUCE_RANKS = 8
+
+
+def allreduce_add_rmsnorm_quant(partials, residual: torch.Tensor | None, weight: torch.Tensor, eps: float,
+                                mode: str, scale_in: torch.Tensor | None = None, *,
+                                out_q: torch.Tensor | None = None, out_scales: torch.Tensor | None = None,
+                                residual_out: torch.Tensor | None = None, stream=None):
+    """rmsq_allreduce_add_rmsnorm_quant: ``partials`` is a sequence of [n, H]
+    tensors, one per rank (each readable by the current device), summed in
+    rank order; then the fused op on the sum.  Returns (q, scales, residual_out)."""
+    L = load()
+    parts = list(partials)
+    if not 1 <= len(parts) <= MAX_ALLREDUCE_RANKS:
+        raise ValueError(f"1 to {MAX_ALLREDUCE_RANKS} partial tensors")
+    x = parts[0]
+    n, H = x.shape
+    if x.dtype not in DTYPES:
+        raise TypeError(f"unsupported activation dtype {x.dtype}")
+    for t in parts:
+        if t.shape != x.shape or t.dtype != x.dtype:
+            raise ValueError("every partial must have the first one's shape and dtype")
+    for t in parts + [residual, weight, residual_out, out_q, out_scales, scale_in]:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    if out_q is None:
+        out_q = torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device=x.device)
+    if out_scales is None:
+        out_scales = scales_like(mode, n, H, x.device)
+    if residual is not None and residual_out is None:
+        residual_out = torch.empty_like(residual)
+    arr = (ctypes.c_void_p * len(parts))(*[t.data_ptr() for t in parts])
+    st = L.rmsq_allreduce_add_rmsnorm_quant(arr, len(parts), _p(residual), _p(weight), ctypes.c_float(eps),
+                                            mode_code(mode), _p(scale_in), _p(out_q), _p(out_scales),
+                                            _p(residual_out), n, H, DTYPES[x.dtype], _stream(stream))
+    if st:
+        raise RmsqError(st, "rmsq_allreduce_add_rmsnorm_quant")
+    return out_q, out_scales, residual_out
+
+
+def row_slice(n_tokens: int, world: int, rank: int) -> tuple[int, int]:
+    """Rows [begin, end) of `rank` when `world` ranks split a batch for a
+    two-shot all-reduce + norm (each rank reduces and normalises its slice,
+    then the slices are gathered): contiguous, as equal as possible, the
+    first n % world ranks one row longer."""
+    if world < 1 or not 0 <= rank < world or n_tokens < 0:
+        raise ValueError("bad world / rank / n_tokens")
+    q, r = divmod(n_tokens, world)
+    begin = rank * q + min(rank, r)
+    return begin, begin + q + (1 if rank < r else 0)
 
 
 def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor | None, weight: torch.Tensor, eps: float, *,

@@ -21,7 +21,8 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "librmsq.so")
 
-UNITS = ["rmsq_api.cu", "rmsq_rows_bf16.cu", "rmsq_rows_fp16.cu", "rmsq_noalloc.cu", "rmsq_act.cu", "rmsq_qk.cu"]
+UNITS = ["rmsq_api.cu", "rmsq_rows_bf16.cu", "rmsq_rows_fp16.cu", "rmsq_noalloc.cu", "rmsq_act.cu", "rmsq_qk.cu",
+         "rmsq_allreduce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-ftz=false", "-prec-div=true",
                      "-prec-sqrt=true", "-fmad=true", "-Xcompiler", "-fPIC,-O2",

@@ -244,6 +244,76 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     return RMSQ_OK;
 }
 
+int rmsq_allreduce_add_rmsnorm_quant(const void* const* partials, int n_ranks, const void* residual,
+                                     const void* weight, float eps, int quant_mode, const float* scale_in,
+                                     void* out_q, void* out_scales, void* residual_out, int64_t n_tokens,
+                                     int64_t hidden, int dtype, void* stream) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (!partials || n_ranks < 1 || n_ranks > RMSQ_MAX_ALLREDUCE_RANKS) return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(quant_mode, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (!std::isfinite(eps) || eps < 0.0f) return RMSQ_ERR_INVALID_ARG;
+    if (n_tokens == 0) return RMSQ_OK;
+    const int mode = quant_mode & RMSQ_QUANT_MODE_MASK;
+    const bool needs_scale_in = mode == RMSQ_FP8_STATIC || mode == RMSQ_NVFP4;
+    const bool has_scales = mode != RMSQ_FP8_STATIC;
+    if (!weight || !out_q) return RMSQ_ERR_INVALID_ARG;
+    for (int r = 0; r < n_ranks; ++r)
+        if (!partials[r]) return RMSQ_ERR_INVALID_ARG;
+    if ((residual == nullptr) != (residual_out == nullptr)) return RMSQ_ERR_INVALID_ARG;
+    if (needs_scale_in && !scale_in) return RMSQ_ERR_INVALID_ARG;
+    if (has_scales && !out_scales) return RMSQ_ERR_INVALID_ARG;
+    if (!needs_scale_in) scale_in = nullptr;
+    if (!has_scales) out_scales = nullptr;
+    for (int r = 0; r < n_ranks; ++r)
+        if (!aligned(partials[r], 16)) return RMSQ_ERR_ALIGNMENT;
+    if (!aligned(residual, 16) || !aligned(weight, 16) || !aligned(residual_out, 16) || !aligned(out_q, 16) ||
+        !aligned(scale_in, 4))
+        return RMSQ_ERR_ALIGNMENT;
+    if (mode != RMSQ_NVFP4 && !aligned(out_scales, scale_elem_bytes(quant_mode))) return RMSQ_ERR_ALIGNMENT;
+
+    size_t q_bytes = 0, sc_bytes = 0;
+    sizes_of(quant_mode, n_tokens, hidden, &q_bytes, &sc_bytes);
+    const size_t act = static_cast<size_t>(n_tokens * hidden) * 2;
+    const Span R = span(residual, act), W = span(weight, hidden * 2), RO = span(residual_out, act),
+               Q = span(out_q, q_bytes), SC = span(out_scales, sc_bytes), SI = span(scale_in, 4);
+    const Span outs[3] = {RO, Q, SC};
+    for (int r = 0; r < n_ranks; ++r) {
+        const Span P = span(partials[r], act);
+        for (const Span& o : outs)
+            if (overlaps(o, P)) return RMSQ_ERR_ALIAS;
+    }
+    if (residual_out) {
+        if (RO.lo != R.lo && overlaps(RO, R)) return RMSQ_ERR_ALIAS;
+        if (overlaps(RO, W) || overlaps(RO, SI)) return RMSQ_ERR_ALIAS;
+    }
+    const Span qs[2] = {Q, SC};
+    for (const Span& o : qs)
+        if (overlaps(o, R) || overlaps(o, W) || overlaps(o, RO) || overlaps(o, SI)) return RMSQ_ERR_ALIAS;
+    if (overlaps(Q, SC)) return RMSQ_ERR_ALIAS;
+
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+    rmsq::LaunchArgs la = {};
+    la.res = residual;
+    la.w = weight;
+    la.res_out = residual_out;
+    la.q = out_q;
+    la.scales = out_scales;
+    la.scale_in = scale_in;
+    la.eps = eps;
+    la.mode = mode;
+    la.e8m0 = (quant_mode & (RMSQ_QUANT_E8M0 | RMSQ_QUANT_UE8M0)) != 0;
+    la.ue8m0 = (quant_mode & RMSQ_QUANT_UE8M0) != 0;
+    la.col_stride = static_cast<int>(col_stride_of(quant_mode, n_tokens));
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    la.variant = rmsq::kVariantDirect;
+    const cudaError_t e = rmsq::launch_allreduce_rows(la, partials, n_ranks, dtype == RMSQ_FP16,
+                                                      static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? RMSQ_OK : fail_cuda(e);
+}
+
 int rmsq_silu_mul_quant(const void* gate_up, int quant_mode, const float* scale_in, void* out_q,
                         void* out_scales, int64_t n_tokens, int64_t d, int dtype, void* stream) {
     if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;

@@ -207,17 +207,20 @@ struct PipePlan {
     int J, threads, stages, smem;
 };
 
-// Chunks per thread by default: 4 from 256 chunks (hidden 2048) up, so that
-// a warp's fixed per-row work (reductions, inverse RMS, scale) is spread
-// over 1024 elements; 2 for narrower rows.
-inline int pipe_default_j(int chunks) { return chunks >= 256 ? 4 : 2; }
+// Chunks per thread by default (measured on GB300): with a residual the
+// kernel is bound by HBM and two chunks per thread (more threads per row,
+// more loads in flight) are fastest; without one it is bound by instruction
+// issue, and four chunks per thread from 256 chunks (hidden 2048) up spread a
+// warp's fixed per-row work (reductions, inverse RMS, scale) over 1024
+// elements.
+inline int pipe_default_j(int chunks, bool res) { return (!res && chunks >= 256) ? 4 : 2; }
 
 inline PipePlan pipe_plan(const RowArgs& a, bool res) {
     const PipeTuning tune = get_pipe_tuning();
     auto threads_for = [&](int j) { return ((a.chunks + 32 * j - 1) / (32 * j)) * 32; };
     PipePlan p;
-    p.J = pipe_default_j(a.chunks);
-    if (threads_for(p.J) > kPipeMaxThreads) p.J = 8;
+    p.J = pipe_default_j(a.chunks, res);
+    while (p.J < 8 && threads_for(p.J) > kPipeMaxThreads) p.J *= 2;
     const int tj = tune.chunks_per_thread;
     if ((tj == 1 || tj == 2 || tj == 4 || tj == 8) && threads_for(tj) <= kPipeMaxThreads) p.J = tj;
     p.threads = threads_for(p.J);

@@ -87,6 +87,12 @@ inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
     return (raw + 255) / 256 * 256;
 }
 
+// All-reduce + residual add + RMSNorm + quantisation: x is the rank-order
+// fp32 sum of `n_ranks` partial buffers (la.x unused), rounded to T.
+constexpr int kMaxArRanks = 8;
+cudaError_t launch_allreduce_rows(const LaunchArgs& la, const void* const* partials, int n_ranks, bool fp16,
+                                  cudaStream_t stream);
+
 // Read and clear the pipelined kernels' fault flags (current device).
 cudaError_t take_pipe_fault_bf16(unsigned int* out);
 cudaError_t take_pipe_fault_fp16(unsigned int* out);

@@ -55,6 +55,11 @@ MUTANTS = [
     ("silu_sigmoid_only", "gd / (1.0 + exp(-gd))", "1.0 / (1.0 + exp(-gd))"),
     ("silu_without_one", "gd / (1.0 + exp(-gd))", "gd / exp(-gd)"),
     ("silu_in_binary32", "return (float)(gd / (1.0 + exp(-gd)));", "return g / (1.0f + expf(-g));"),
+    # all-reduce + RMSNorm (pinned by test_oracle_allreduce.py)
+    ("ar_rounds_every_rank", "acc = acc + widen(dtype, partials[(int64_t)r * n * H + i]);",
+     "acc = widen(dtype, narrow(dtype, acc + widen(dtype, partials[(int64_t)r * n * H + i])));"),
+    ("ar_drops_last_rank", "for (int r = 1; r < nranks; ++r) acc", "for (int r = 1; r < nranks - 1; ++r) acc"),
+    ("ar_first_rank_twice", "float acc = widen(dtype, partials[i]);", "float acc = widen(dtype, partials[i]) * 2.0f;"),
     ("gate_up_swapped", "const uint16_t *g = a->x + t * 2 * d, *u = g + d;",
      "const uint16_t *u = a->x + t * 2 * d, *g = u + d;"),
 ]
@@ -81,7 +86,8 @@ def test_pins_catch_planted_mistake(mutant_dir, name, old, new):
                         os.path.join(ROOT, "tests", "test_oracle_op.py"),
                         os.path.join(ROOT, "tests", "test_oracle_act.py"),
                         os.path.join(ROOT, "tests", "test_oracle_scale_options.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_qk.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_qk.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_allreduce.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
     assert "failed" in r.stdout, r.stdout[-2000:]
