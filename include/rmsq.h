@@ -197,9 +197,10 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void *x, const void *residual, const v
  * whole batch (the NVFP4 workload's definition of the global scale; gs = 1
  * when that amax is 0), then exactly the RMSQ_NVFP4 quantisation with that gs
  * (vLLM PR #51925 summary, "Motivation": residual update + RMSNorm, block
- * scales, FP4 values, fp32 global scale).  Two passes: the first computes the
- * residual, the per-row inv_rms and the batch amax into `workspace`; the
- * second re-reads h (residual_out, or x without a residual) and quantises.
+ * scales, FP4 values, fp32 global scale).  Two kernels: the first computes
+ * the residual, and the per-row inv_rms and per-CTA maxima of |y| into
+ * `workspace`; the second takes the batch amax from those maxima, re-reads h
+ * (residual_out, or x without a residual) and quantises.
  *  out_global_scale  device, one fp32 (4-byte aligned): receives gs.
  *  workspace         device, 16-byte aligned, at least
  *                    rmsq_nvfp4_dynamic_workspace_bytes(n_tokens) bytes of
@@ -219,7 +220,9 @@ int rmsq_fused_add_rmsnorm_nvfp4_dynamic(const void *x, const void *residual, co
                                          int variant);
 
 /* Bytes of workspace rmsq_fused_add_rmsnorm_nvfp4_dynamic needs for n_tokens
- * rows: 256 + 4 * n_tokens, rounded up to a multiple of 256 (0 for n < 0). */
+ * rows: 256 + 8 * n_tokens (one fp32 inverse RMS per row and at most one
+ * fp32 partial maximum per row), rounded up to a multiple of 256 (0 for
+ * n < 0). */
 size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
 
 /* Largest batch rmsq_fused_add_rmsnorm_nvfp4_dynamic_noalloc accepts. */
@@ -234,8 +237,8 @@ size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
  * or latency-critical code that must not call cudaMalloc because it can
  * synchronise the device.  The caller still passes every input and output.
  *
- * The workspace lives in a fixed device array inside the library (256 + 4 *
- * RMSQ_NOALLOC_MAX_TOKENS bytes, about 257 KiB), present on every device that
+ * The workspace lives in a fixed device array inside the library (256 + 8 *
+ * RMSQ_NOALLOC_MAX_TOKENS bytes, about 513 KiB), present on every device that
  * loads the library until the process exits.  n_tokens above
  * RMSQ_NOALLOC_MAX_TOKENS returns RMSQ_ERR_UNSUPPORTED_SHAPE (use the entry
  * point with a workspace for larger batches).  Every call looks up the
@@ -243,8 +246,8 @@ size_t rmsq_nvfp4_dynamic_workspace_bytes(int64_t n_tokens);
  * (cudaGetSymbolAddress), so a reset of the device's primary context between
  * calls is followed; the first call on a device may load the library's device
  * code there: make that first call before any stream capture.  Every call on a
- * device shares the one array and leaves its contents behind; the call zeroes
- * what must start at zero (the amax word) itself.  Calls whose work overlaps on
+ * device shares the one array and leaves its contents behind; nothing in it
+ * has to start at zero (every call writes what it reads).  Calls whose work overlaps on
  * the GPU (other streams, or other host threads) race on the array: order them.
  * Arguments, results and every other rule are those of
  * rmsq_fused_add_rmsnorm_nvfp4_dynamic; without a CUDA device it returns
@@ -376,8 +379,12 @@ int rmsq_allreduce_add_rmsnorm_quant(const void *const *partials, int n_ranks, c
  * (every quant_mode; scales and codes laid out the same way with hidden = d).
  * e^x follows W. J. Cody and W. Waite's argument reduction with a degree-7
  * Taylor polynomial, each step a correctly rounded binary32 operation (within
- * 1.2 ulp of e^x over the normal range); the division and products are
- * correctly rounded, so results are reproducible bit for bit.
+ * 1.2 ulp of e^x over the normal range); the quotient is g times the
+ * hardware's approximate reciprocal of 1 + e^-g (within one ulp), so a is
+ * within 7.4 * 2^-24 relative of the exact silu(g) * u (results are
+ * deterministic: the same inputs always give the same bytes).  Where e^-g
+ * overflows (g < -88.72) silu is -0.  The quantisation of a is exact, as in
+ * the norm op.
  *  gate_up     device, [n_tokens, 2 d] bf16/fp16, row-major, 16-byte aligned.
  *  quant_mode  an rmsq_quant_mode, optionally OR-ed with RMSQ_QUANT_* options.
  *  scale_in    device fp32: FP8 static scale or NVFP4 global scale (else

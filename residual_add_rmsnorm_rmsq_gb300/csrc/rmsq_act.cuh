@@ -10,7 +10,9 @@
 // norm kernels (quantize_y) on a.  One CTA per row, thread t on the chunks
 // t*J .. t*J+J-1 of the row, as in the direct norm kernel.
 //
-// e^x is evaluated by W. J. Cody and W. Waite's method ("Software Manual for
+// silu(g) is g times the approximate reciprocal of 1 + e^-g (the result is
+// compared with the oracle's correctly rounded silu within a bound derived
+// from these steps).  e^x is evaluated by W. J. Cody and W. Waite's method ("Software Manual for
 // the Elementary Functions", 1980): x = n ln2 + r with n = rint(x log2 e) and
 // ln2 split in a high part of 15 significant bits (n ln2_hi is exact) and the
 // rest, r formed by two fused multiply-adds; e^r by the degree-7 Taylor
@@ -79,13 +81,24 @@ __device__ __forceinline__ float2 exp_cw2_mid(float2 x) {
     return mul2_rn(p, make_float2(pow2_bits(__float2int_rn(n.x)), pow2_bits(__float2int_rn(n.y))));
 }
 
-// a = silu(g) * u = (g / (1 + e^-g)) * u for two elements; MID: both |g| <= 87,
-// where exp_cw2_mid(-g) equals exp_cw2(-g).
+// 1 / x by the hardware approximation: within one ulp over the whole range
+// (subnormal results kept).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// a = silu(g) * u = g * (1 / (1 + e^-g)) * u for two elements; MID: both
+// |g| <= 87, where exp_cw2_mid(-g) equals exp_cw2(-g).  The quotient is g
+// times the approximate reciprocal of 1 + e^-g (one ulp), so silu is within
+// 6.4 * 2^-24 of its exact value: e^-g 1.2 ulp, the sum, the reciprocal and
+// the product.
 template <bool MID = false>
 __device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
     const float2 e = MID ? exp_cw2_mid(make_float2(-g.x, -g.y)) : exp_cw2(make_float2(-g.x, -g.y));
     const float2 den = add2_rn(make_float2(1.0f, 1.0f), e);
-    const float2 s = make_float2(__fdiv_rn(g.x, den.x), __fdiv_rn(g.y, den.y));
+    const float2 s = mul2_rn(g, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
     return mul2_rn(s, u);
 }
 

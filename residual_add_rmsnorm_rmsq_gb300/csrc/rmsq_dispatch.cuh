@@ -247,8 +247,10 @@ inline cudaError_t pipe_grid(const void* fn, const PipePlan& p, int n, int* grid
     return cudaSuccess;
 }
 
+// One launch of the row work; *grid_out (if given) receives the number of
+// CTAs launched.
 template <class E>
-cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
+cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream, int* grid_out = nullptr) {
     RowArgs a = make_row_args(la);
     const bool res = la.res != nullptr;
     cudaError_t err = cudaSuccess;
@@ -266,6 +268,7 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
         if (err != cudaSuccess) return err;
         int st = p.stages;
         void* params[] = {&a, &st};
+        if (grid_out) *grid_out = grid;
         return launch_kernel(fn, dim3(grid), dim3(p.threads), params, p.smem, stream);
     }
     const int J = a.chunks <= 1024 ? 1 : 2;
@@ -273,29 +276,24 @@ cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream) {
     const void* fn = pick_kernel<E>(la.mode, res, false, J);
     if (!fn) return cudaErrorInvalidValue;
     void* params[] = {&a};
+    if (grid_out) *grid_out = a.n;
     return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
 }
 
-// NVFP4 with a data-derived global scale: zero the workspace's amax word
-// (a one-thread kernel), pass 1 (row kernel, mode kNormAmax, in the requested
-// variant), pass 2 (block quantisation).  All three are launched with
-// programmatic dependent launch when it is on, so each launch overlaps the
-// end of the kernel before it; each waits for that kernel before touching
-// memory.
+// NVFP4 with a data-derived global scale: pass 1 (row kernel, mode
+// kNormAmax, in the requested variant), pass 2 (block quantisation), both
+// launched with programmatic dependent launch when it is on, so pass 2
+// overlaps the end of pass 1 and waits for it before touching memory.
 template <class E>
 cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* out_gs,
                                  cudaStream_t stream) {
-    unsigned int* amax_word = static_cast<unsigned int*>(workspace);
-    void* zparams[] = {&amax_word};
-    cudaError_t e = launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_zero_kernel), dim3(1), dim3(32),
-                                  zparams, 0, stream);
-    if (e != cudaSuccess) return e;
     LaunchArgs first = la;
     first.mode = kNormAmax;
     first.q = nullptr;
     first.scales = workspace;
     first.scale_in = nullptr;
-    e = launch_rows<E>(first, stream);
+    int parts = 0;
+    cudaError_t e = launch_rows<E>(first, stream, &parts);
     if (e != cudaSuccess) return e;
     const int64_t blocks_total = (int64_t)la.n * (la.hidden / 16);
     const int sms = sm_count(&e);
@@ -310,7 +308,7 @@ cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* o
     uint2* q = static_cast<uint2*>(la.q);
     uint8_t* bs = static_cast<uint8_t*>(la.scales);
     int n = la.n, hidden = la.hidden;
-    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden, &pair};
+    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden, &pair, &parts};
     return launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_quant_kernel<E>), dim3((unsigned)grid),
                          dim3(256), params, 0, stream);
 }

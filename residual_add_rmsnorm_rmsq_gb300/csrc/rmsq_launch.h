@@ -81,9 +81,10 @@ struct QkLaunch {
     int variant;   // kVariantAuto / kVariantDirect / kVariantPipelined
 };
 cudaError_t launch_qk_norm_rope(const QkLaunch& l, cudaStream_t stream);
-// Workspace bytes for n rows (amax word + padding + n fp32 inv_rms, rounded up to 256).
+// Workspace bytes for n rows (a 256-byte header, n fp32 inv_rms and at most n
+// per-CTA partial maxima, rounded up to 256).
 inline size_t nvfp4_dynamic_workspace_bytes(int64_t n) {
-    const size_t raw = 256 + 4 * static_cast<size_t>(n);
+    const size_t raw = 256 + 8 * static_cast<size_t>(n);
     return (raw + 255) / 256 * 256;
 }
 

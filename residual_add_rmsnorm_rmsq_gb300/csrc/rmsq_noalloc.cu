@@ -1,7 +1,7 @@
 // Allocation-free entry point for NVFP4 with a data-derived global scale.
 //
 // rmsq_fused_add_rmsnorm_nvfp4_dynamic needs a small device workspace (the
-// batch amax word and one fp32 per row).  Some callers cannot provide one:
+// per-row inverse RMS and per-CTA partial maxima of the first pass).  Some callers cannot provide one:
 // code that gets no device allocator from its host (a plugin inside an
 // engine that owns every byte of device memory through its own pool), or
 // latency-critical code that must never call cudaMalloc because it can
@@ -27,7 +27,7 @@
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = 256 + 4 * static_cast<size_t>(RMSQ_NOALLOC_MAX_TOKENS);
+constexpr size_t kNoallocScratchBytes = 256 + 8 * static_cast<size_t>(RMSQ_NOALLOC_MAX_TOKENS);
 static_assert(kNoallocScratchBytes % 256 == 0, "scratch size is a multiple of 256");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];

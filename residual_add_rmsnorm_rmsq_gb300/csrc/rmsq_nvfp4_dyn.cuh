@@ -2,12 +2,16 @@
 // over the whole batch, 1 for an all-zero batch), in two passes:
 //
 //  1. the row work in mode kNormAmax: residual add and write-back, RMSNorm,
-//     the row's inv_rms into the workspace, and the batch amax of |y| (one
-//     atomicMax per CTA on the workspace's amax word, zeroed before);
+//     the row's inv_rms into the workspace, and each CTA's amax of |y| into
+//     its slot of the workspace;
 //  2. nvfp4_dyn_blocks below: one thread per 16-element block re-reads h
 //     (residual_out, or x without a residual) and the weight, rebuilds
 //     y = (h * inv) * w exactly as pass 1 did, and writes the E4M3 block
-//     scale and the eight bytes of E2M1 codes with gs = 2688 / amax.
+//     scale and the eight bytes of E2M1 codes with gs = 2688 / amax, amax
+//     being the max of pass 1's per-CTA slots.
+//
+// Two launches and no atomics: the workspace needs no zeroing, so its
+// contents on entry do not matter.
 //
 // Pass 1 keeps h at normal L2 priority, so that pass 2, launched right after
 // it, mostly reads h from L2.
@@ -114,28 +118,29 @@ __device__ __forceinline__ void nvfp4_dyn_blocks(const uint4* h, const uint4* w,
 // gs = 2688 / amax, 1 when the batch amax is 0.
 __device__ __forceinline__ float nvfp4_dyn_gs(float amax) { return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f; }
 
-// Zeroes the workspace's amax word before pass 1.  A kernel rather than a
-// memset so that it joins the chain of programmatic dependent launches: it
-// may be scheduled while the preceding kernel finishes, waits for it (an
-// earlier call's pass 2 may still read the word) and lets pass 1 launch
-// early in turn.  A memset in its place cost ~3.8 us per call on GB300.
-static __global__ void __launch_bounds__(32) nvfp4_dyn_zero_kernel(unsigned int* amax_word) {
-    allow_dependents();
-    grid_dependency_wait();
-    if (threadIdx.x == 0) *amax_word = 0u;
-}
-
-// Pass 2 as its own kernel, launched after pass 1.
+// Pass 2 as its own kernel, launched after pass 1: the batch amax is the max
+// of pass 1's `parts` per-CTA partial maxima (a few KB, read from L2 by every
+// CTA; non-negative floats order like their bit patterns), then gs and the
+// blocks.
 template <class E>
 __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, const uint4* w,
                                                               const float* ws, uint2* q,
                                                               uint8_t* bscale, float* out_gs,
-                                                              int n, int hidden, int pair) {
+                                                              int n, int hidden, int pair, int parts) {
+    __shared__ float s_rtab[128];
+    __shared__ unsigned int s_max[8];
     allow_dependents();
     grid_dependency_wait();
-    const float gs = nvfp4_dyn_gs(__uint_as_float(reinterpret_cast<const unsigned int*>(ws)[0]));
+    const unsigned int* slots = reinterpret_cast<const unsigned int*>(ws + kWsInvOffset + n);
+    unsigned int m = 0u;
+    for (int i = threadIdx.x; i < parts; i += blockDim.x) m = max(m, slots[i]);
+    m = __reduce_max_sync(kFull, m);
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = 0u;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = max(m, s_max[i]);
+    const float gs = nvfp4_dyn_gs(__uint_as_float(m));
     if (blockIdx.x == 0 && threadIdx.x == 0) *out_gs = gs;
-    __shared__ float s_rtab[128];
     fill_nvfp4_rtab(s_rtab, gs);
     __syncthreads();
     nvfp4_dyn_blocks<E>(h, w, ws, q, bscale, n, hidden, gs, s_rtab,

@@ -29,17 +29,18 @@ enum Mode : int {
     kNvfp4 = 6,
     // First pass of NVFP4 with a data-derived global scale: residual add,
     // RMSNorm, the row's inv_rms stored in the workspace and the running
-    // amax of y folded into the workspace's amax word; no codes.
+    // CTA's amax of y into its slot of the workspace; no codes.
     kNormAmax = 7,
     // The norm alone (the first op of the unfused sequence): y rounded to
     // the activation type, stored at q as a [n, hidden] T tensor.
     kNormOnly = 8,
 };
 
-// Workspace of the data-derived NVFP4 global scale: word 0 holds the bits of
-// the batch amax of |y| (non-negative floats order like their bit patterns,
-// so atomicMax on the bits is a max on the values); the fp32 inv_rms of row t
-// sits at float index kWsInvOffset + t.
+// Workspace of the data-derived NVFP4 global scale: the fp32 inv_rms of row t
+// sits at float index kWsInvOffset + t, and the amax of |y| over the rows of
+// CTA b of the first pass at float index kWsInvOffset + n + b (at most one
+// CTA per row, so n slots suffice).  The second pass takes the batch amax as
+// the max of those partial maxima: nothing has to be zeroed before a call.
 constexpr int kWsInvOffset = 64;
 
 struct RowArgs {
@@ -362,9 +363,9 @@ __device__ __forceinline__ void quantize_row(const RowArgs& a, int row, const ui
     }
 }
 
-// End of a kNormAmax launch: CTA-wide max of the threads' running amax, then
-// one atomicMax per CTA on the workspace's amax word.  Every thread of the
-// CTA calls it (two __syncthreads); `s_max` is 32 floats of shared memory.
+// End of a kNormAmax launch: CTA-wide max of the threads' running amax into
+// the CTA's slot of the workspace.  Every thread of the CTA calls it (two
+// __syncthreads); `s_max` is 32 floats of shared memory.
 __device__ __forceinline__ void flush_amax(const RowArgs& a, float run_max, float* s_max, int tid,
                                            int nwarps) {
     const int lane = tid & 31, warp = tid >> 5;
@@ -375,13 +376,7 @@ __device__ __forceinline__ void flush_amax(const RowArgs& a, float run_max, floa
     if (tid == 0) {
         float t = 0.0f;
         for (int w = 0; w < nwarps; ++w) t = fmaxf(t, s_max[w]);
-        // The word only grows during the launch: skip the atomic when it
-        // already holds t or more (most CTAs, once a few have merged), which
-        // keeps the one address from serialising every CTA's update.
-        unsigned int* word = static_cast<unsigned int*>(a.scales);
-        unsigned int cur;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(word) : "memory");
-        if (t > 0.0f && __float_as_uint(t) > cur) atomicMax(word, __float_as_uint(t));
+        static_cast<float*>(a.scales)[kWsInvOffset + a.n + blockIdx.x] = t;
     }
 }
 

@@ -160,8 +160,9 @@ def test_valid_call_without_device_reports_no_device(L):
 def test_nvfp4_dynamic_argument_errors(L):
     vp = ctypes.c_void_p
     ws = rq.nvfp4_dynamic_workspace_bytes(4)
-    assert ws == 512 and rq.nvfp4_dynamic_workspace_bytes(64) == 512
-    assert rq.nvfp4_dynamic_workspace_bytes(65) == 768
+    # 256 + 8 n rounded up to 256: a header, an inverse RMS and a partial maximum per row
+    assert ws == 512 and rq.nvfp4_dynamic_workspace_bytes(32) == 512
+    assert rq.nvfp4_dynamic_workspace_bytes(33) == 768 and rq.nvfp4_dynamic_workspace_bytes(0) == 256
 
     def dyn(x=A, res=B, w=C, q=D, sc=E, gs=0x70000000, ro=F, wsp=0x78000000, wsb=ws, n=4, H=64, dt=0, v=0):
         return L.rmsq_fused_add_rmsnorm_nvfp4_dynamic(

@@ -102,7 +102,7 @@ def test_pipelined_first_pass_with_small_grids(shape):
 @pytest.mark.parametrize("variant", ["auto", "direct"])
 def test_graph_replay_resets_the_workspace(variant):
     """Captured once into a CUDA graph and replayed on new inputs: each replay
-    zeroes the amax word again."""
+    writes every workspace entry it reads (inverse RMS, per-CTA maxima)."""
     wls = [ri.make_workload(f"graph{i}", 900, 2048, res_sigma=1.0 + i, seed=300 + i) for i in range(3)]
     x = P.dev_act(wls[0].x, wls[0].dtype)
     r = P.dev_act(wls[0].residual, wls[0].dtype)
@@ -145,8 +145,8 @@ def test_graph_replay_resets_the_workspace(variant):
 def test_back_to_back_calls_share_a_workspace(variant, pdl):
     """Three calls queued on one stream with one workspace and no host
     synchronisation between them, with and without programmatic dependent
-    launch: each call's zeroing of the amax word must wait for the previous
-    call's second pass to have read it."""
+    launch: each call's first pass must not overwrite the per-CTA maxima
+    before the previous call's second pass has read them."""
     wls = [ri.make_workload(f"b2b{i}", 4096, 2048, res_sigma=0.5 + i, seed=500 + i) for i in range(3)]
     ws = torch.full((rq.nvfp4_dynamic_workspace_bytes(4096),), 0x7F, dtype=torch.uint8, device="cuda")
     ins = [(P.dev_act(wl.x, wl.dtype), P.dev_act(wl.residual, wl.dtype), P.dev_act(wl.weight, wl.dtype))
