@@ -356,6 +356,38 @@ class UnfusedBuffers:
         self.rq.quant(self.y[k], self.mode, self.scale_in, out_q=self.q[k], out_scales=self.sc[k], stream=stream)
 
 
+class AllReduceBuffers:
+    """Rotating buffer sets for all-reduce + residual add + RMSNorm + quant:
+    the ranks' partial tensors are emulated as separate buffers of this
+    device (the same loads a multi-GPU node issues to peer memory)."""
+
+    def __init__(self, torch, rq, wl, mode, ranks, min_total_bytes, max_sets=None):
+        tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+        n, H = wl.n_tokens, wl.hidden
+        self.rq, self.wl, self.mode, self.ranks = rq, wl, mode, ranks
+        # each rank's partial row read once, plus what the fused op moves besides x
+        self.bytes = algorithmic_bytes(mode, n, H, 2, True) + (ranks - 1) * n * H * 2
+        self.sets = max(2, math.ceil(min_total_bytes / self.bytes))
+        if max_sets is not None:
+            self.sets = min(self.sets, max_sets)
+        x0 = torch.from_numpy(wl.x.view(np.int16)).view(tdt).cuda()
+        r0 = torch.from_numpy(wl.residual.view(np.int16)).view(tdt).cuda()
+        self.w = torch.from_numpy(wl.weight.view(np.int16)).view(tdt).cuda()
+        self.scale_in = torch.tensor([0.05 if mode == "fp8_static" else 1000.0], dtype=torch.float32, device="cuda")
+        self.parts, self.r, self.ro, self.q, self.sc = [], [], [], [], []
+        for i in range(self.sets):
+            self.parts.append([x0 * (0.5 + 0.25 * k) for k in range(ranks)])
+            self.r.append(r0.clone())
+            self.ro.append(torch.empty_like(r0))
+            self.q.append(torch.empty(n, H // 2 if mode == "nvfp4" else H, dtype=torch.uint8, device="cuda"))
+            self.sc.append(rq.scales_like(mode, n, H, "cuda"))
+
+    def launch(self, k, stream):
+        self.rq.allreduce_add_rmsnorm_quant(self.parts[k], self.r[k], self.w, self.wl.eps, self.mode, self.scale_in,
+                                            out_q=self.q[k], out_scales=self.sc[k], residual_out=self.ro[k],
+                                            stream=stream)
+
+
 class QkBuffers:
     """Rotating buffer sets for QK-norm + RoPE (in place on qkv)."""
 
@@ -793,6 +825,21 @@ def sweep(torch, rq, stream, peak, args):
                                            "frac": round(gbs / peak, 4),
                                            "tokens_per_s": round(qk.n_tokens / (ms / 1e3), 1), "bytes": qb.bytes}
         del qb, qk
+        torch.cuda.empty_cache()
+    # all-reduce + RMSNorm at the token counts the fusion is meant for (the
+    # pages: profitable at small num_tokens), 2 and 8 ranks, on the Llama layer
+    for ranks in (2, 8):
+        for n_ar in (16, 256, 2048):
+            wl = ri.llama(n_ar, True)
+            for mode in ("fp8_static", "nvfp4"):
+                ab = AllReduceBuffers(torch, rq, wl, mode, ranks, 4 * L2_BYTES + 1, max_sets=64)
+                ms = time_launches(torch, rq, wl, mode, ab, args.sweep_steps, 5, stream)
+                gbs = ab.bytes / (ms / 1e3) / 1e9
+                out[f"allreduce_r{ranks}_{n_ar}x4096_{mode}"] = {
+                    "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "bytes": ab.bytes, "l2": "inputs > L2" if ab.sets * ab.bytes > 4 * L2_BYTES else "L2-resident"}
+                del ab
+            del wl
         torch.cuda.empty_cache()
     act = ri.llama_mlp(4096)
     for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):

@@ -282,50 +282,38 @@ __device__ __forceinline__ uint2 fp8_chunk(const float (&v)[8], float s, Fp8Reci
     return out;
 }
 
-// Two chunks a, b at once; the bracket products are formed in packed pairs
-// (a[k], b[k]) and turned into codes right away.
-__device__ __forceinline__ void fp8_chunk2(const float (&a)[8], const float (&b)[8], float s, Fp8Recips rc,
-                                           uint2& ca, uint2& cb) {
-    uint32_t dna[4], dnb[4], diff = 0u;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float2 e0 = make_float2(a[2 * p], b[2 * p]), e1 = make_float2(a[2 * p + 1], b[2 * p + 1]);
-        const float2 d0 = mul2_rn(e0, make_float2(rc.rdn, rc.rdn)), d1 = mul2_rn(e1, make_float2(rc.rdn, rc.rdn));
-        const float2 u0 = mul2_rn(e0, make_float2(rc.rup, rc.rup)), u1 = mul2_rn(e1, make_float2(rc.rup, rc.rup));
-        dna[p] = e4m3x2(d0.x, d1.x);
-        dnb[p] = e4m3x2(d0.y, d1.y);
-        diff |= (dna[p] ^ e4m3x2(u0.x, u1.x)) | ((dnb[p] ^ e4m3x2(u0.y, u1.y)) << 16);
-    }
-    ca = make_uint2(dna[0] | (dna[1] << 16), dna[2] | (dna[3] << 16));
-    cb = make_uint2(dnb[0] | (dnb[1] << 16), dnb[2] | (dnb[3] << 16));
-    if (diff != 0u) {   // rare: redo both chunks exactly
-        ca = fp8_chunk_exact(a, s);
-        cb = fp8_chunk_exact(b, s);
-    }
-}
-
 // Two chunks a, b under their own scales sa, sb (reciprocal brackets ra, rb):
-// the same test as fp8_chunk2, the products formed in packed pairs
-// (a[k] * ra, b[k] * rb).
+// the bracket products are formed in packed pairs (a[k] * ra, b[k] * rb) and
+// turned into codes right away; the codes of each bracket end are packed four
+// to a word (byte permutes) and the two ends compared word by word.
 __device__ __forceinline__ void fp8_chunk2s(const float (&a)[8], const float (&b)[8], float sa, float sb,
                                             Fp8Recips ra, Fp8Recips rb, uint2& ca, uint2& cb) {
-    uint32_t dna[4], dnb[4], diff = 0u;
+    uint32_t da[4], db[4], ua[4], ub[4];
     const float2 dn = make_float2(ra.rdn, rb.rdn), up = make_float2(ra.rup, rb.rup);
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         const float2 e0 = make_float2(a[2 * p], b[2 * p]), e1 = make_float2(a[2 * p + 1], b[2 * p + 1]);
         const float2 d0 = mul2_rn(e0, dn), d1 = mul2_rn(e1, dn);
         const float2 u0 = mul2_rn(e0, up), u1 = mul2_rn(e1, up);
-        dna[p] = e4m3x2(d0.x, d1.x);
-        dnb[p] = e4m3x2(d0.y, d1.y);
-        diff |= (dna[p] ^ e4m3x2(u0.x, u1.x)) | ((dnb[p] ^ e4m3x2(u0.y, u1.y)) << 16);
+        da[p] = e4m3x2(d0.x, d1.x);
+        db[p] = e4m3x2(d0.y, d1.y);
+        ua[p] = e4m3x2(u0.x, u1.x);
+        ub[p] = e4m3x2(u0.y, u1.y);
     }
-    ca = make_uint2(dna[0] | (dna[1] << 16), dna[2] | (dna[3] << 16));
-    cb = make_uint2(dnb[0] | (dnb[1] << 16), dnb[2] | (dnb[3] << 16));
+    ca = make_uint2(__byte_perm(da[0], da[1], 0x5410), __byte_perm(da[2], da[3], 0x5410));
+    cb = make_uint2(__byte_perm(db[0], db[1], 0x5410), __byte_perm(db[2], db[3], 0x5410));
+    const uint32_t diff = (ca.x ^ __byte_perm(ua[0], ua[1], 0x5410)) | (ca.y ^ __byte_perm(ua[2], ua[3], 0x5410)) |
+                          (cb.x ^ __byte_perm(ub[0], ub[1], 0x5410)) | (cb.y ^ __byte_perm(ub[2], ub[3], 0x5410));
     if (diff != 0u) {   // rare: redo both chunks exactly
         ca = fp8_chunk_exact(a, sa);
         cb = fp8_chunk_exact(b, sb);
     }
+}
+
+// Two chunks a, b under one scale.
+__device__ __forceinline__ void fp8_chunk2(const float (&a)[8], const float (&b)[8], float s, Fp8Recips rc,
+                                           uint2& ca, uint2& cb) {
+    fp8_chunk2s(a, b, s, s, rc, rc, ca, cb);
 }
 
 // Pairwise tree over the squares of eight consecutive elements, in packed

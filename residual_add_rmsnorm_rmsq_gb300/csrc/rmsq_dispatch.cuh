@@ -50,8 +50,22 @@ static __device__ unsigned int g_pipe_fault;
 #define RMSQ_PAIR_ACCESS 1
 #endif
 
+// Register budget of the pipelined kernel by chunks per thread (compile-time
+// tuning, results do not depend on it): with four chunks per thread the
+// natural allocation (~86) leaves five 128-thread CTAs per SM; 80 gives six.
+#ifndef RMSQ_PIPE_MAXNREG_J4
+#define RMSQ_PIPE_MAXNREG_J4 80
+#endif
+#ifndef RMSQ_PIPE_MAXNREG_J8
+#define RMSQ_PIPE_MAXNREG_J8 128
+#endif
+template <int J> constexpr int pipe_maxnreg() {
+    return J == 4 ? RMSQ_PIPE_MAXNREG_J4 : J == 8 ? RMSQ_PIPE_MAXNREG_J8 : 128;
+}
+
 template <class E, int MODE, bool RES, int J>
-__global__ void __launch_bounds__(kPipeMaxThreads, 1) pipe_entry(const RowArgs a, const int stages) {
+__global__ void __launch_bounds__(kPipeMaxThreads) __maxnreg__(pipe_maxnreg<J>())
+pipe_entry(const RowArgs a, const int stages) {
     pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
 }
 
@@ -121,17 +135,20 @@ struct OccEntry {
     int blocks;
 };
 
-// Shared-memory ring budget per CTA (two CTAs per SM).
+// Shared-memory ring budget per CTA (two CTAs per SM), and the opt-in
+// dynamic shared memory limit of a pipelined kernel (the ring plus, with four
+// or eight chunks per thread, the weights; the largest a CTA may use).
 constexpr int kPipeSmemBudget = 110 * 1024;
+constexpr int kPipeSmemLimit = 227 * 1024;
 
 // The opt-in dynamic shared memory limit of a pipelined instantiation (the
-// full ring budget, so that no launch ever lowers it below what another
+// largest a CTA may use, so that no launch ever lowers it below what another
 // launch of the same function needs) and its carve-out preference.  Function
 // attributes belong to the context of the current device, so they are set
 // before every launch (a host-side call, no device work): a second device, or
 // a device whose primary context was reset, never gets a launch without them.
 inline cudaError_t set_smem_attributes(const void* fn) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemBudget);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemLimit);
     // Prefer the largest shared-memory carve-out so that the rings of several
     // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
     if (e == cudaSuccess && RMSQ_MAX_SMEM_CARVEOUT)
@@ -228,7 +245,9 @@ inline PipePlan pipe_plan(const RowArgs& a, bool res) {
     p.stages = pipe_stages(stage_bytes);
     if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
         p.stages = tune.stages;
-    p.smem = p.stages * stage_bytes;
+    // The weights (four or eight chunks per thread) sit after the ring.
+    const int wbytes = co_weight_smem_bytes(p.J, p.threads * p.J);
+    p.smem = p.stages * stage_bytes + wbytes;
     return p;
 }
 

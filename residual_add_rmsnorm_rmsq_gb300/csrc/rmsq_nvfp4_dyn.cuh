@@ -132,8 +132,20 @@ __global__ void __launch_bounds__(256) nvfp4_dyn_quant_kernel(const uint4* h, co
     allow_dependents();
     grid_dependency_wait();
     const unsigned int* slots = reinterpret_cast<const unsigned int*>(ws + kWsInvOffset + n);
+    // Eight independent loads in flight per thread and round (2048 slots per
+    // round for 256 threads), so the slots cost one L2 round trip, not one per
+    // iteration.
     unsigned int m = 0u;
-    for (int i = threadIdx.x; i < parts; i += blockDim.x) m = max(m, slots[i]);
+    for (int base = 0; base < parts; base += 8 * (int)blockDim.x) {
+        unsigned int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * (int)blockDim.x + (int)threadIdx.x;
+            v[u] = i < parts ? __ldcg(slots + i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) m = max(m, v[u]);
+    }
     m = __reduce_max_sync(kFull, m);
     if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
     __syncthreads();

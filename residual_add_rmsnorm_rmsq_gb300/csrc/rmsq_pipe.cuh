@@ -58,45 +58,61 @@ __device__ __forceinline__ float co_warp_sum(const float (&h)[J][8]) {
     }
 }
 
-// Weights of the thread's chunks, loaded once per CTA: widened to fp32 for
-// one or two chunks per thread; kept packed (and widened per row) for more,
-// where the registers serve occupancy better.
+// Weights of the thread's chunks, loaded once per CTA and widened to fp32:
+// in registers for one or two chunks per thread; for more, in the CTA's
+// shared memory (where the registers serve occupancy better), each thread's
+// own chunks in a lane-interleaved layout (two float4 per chunk, the warp's
+// 32 lanes side by side: conflict-free 16-byte reads).  A thread reads back
+// only what it wrote, so no barrier is needed; the reads are volatile so that
+// the compiler keeps them in the row loop instead of hoisting them into
+// registers.
 template <class E, int J>
 struct CoWeights {
-    static constexpr bool kPacked = J >= 4;
-    float f[kPacked ? 1 : J][8];
-    uint32_t p[kPacked ? J : 1][4];
+    static constexpr bool kSmem = J >= 4;
+    float f[kSmem ? 1 : J][8];
+    float4* wsm;   // kSmem: this thread's first float4; chunk j at +(2 j) * 32 and +(2 j + 1) * 32
 
-    __device__ __forceinline__ void load(const uint4* w, int c0, int chunks) {
+    __device__ __forceinline__ void load(const uint4* w, int c0, int chunks, float4* smem_w, int warp, int lane) {
+        wsm = smem_w + (size_t)warp * J * 64 + lane;
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int c = c0 + 32 * j;
             const uint4 v = c < chunks ? ld_weight(w + c) : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+            float t[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if constexpr (kPacked) {
-                    p[j][k] = ws[k];
-                } else {
-                    f[j][2 * k] = E::lo(ws[k]);
-                    f[j][2 * k + 1] = E::hi(ws[k]);
-                }
+            for (int k = 0; k < 4; ++k) { t[2 * k] = E::lo(ws[k]); t[2 * k + 1] = E::hi(ws[k]); }
+            if constexpr (kSmem) {
+                wsm[(2 * j) * 32] = make_float4(t[0], t[1], t[2], t[3]);
+                wsm[(2 * j + 1) * 32] = make_float4(t[4], t[5], t[6], t[7]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) f[j][k] = t[k];
             }
         }
     }
-    // The packed words pass through an empty volatile asm on every use, so
-    // that the compiler cannot hoist their widening out of the row loop
-    // (which would bring back the registers the packing saves).
-    __device__ __forceinline__ float get(int j, int k) const {
-        if constexpr (kPacked) {
-            uint32_t v = p[j][k >> 1];
-            asm volatile("" : "+r"(v));
-            return (k & 1) ? E::hi(v) : E::lo(v);
+    // The eight weights of chunk j.
+    __device__ __forceinline__ void get(int j, float (&o)[8]) const {
+        if constexpr (kSmem) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float4* p = wsm + (2 * j + hf) * 32;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(o[4 * hf]), "=f"(o[4 * hf + 1]), "=f"(o[4 * hf + 2]), "=f"(o[4 * hf + 3])
+                             : "r"(smem_u32(p)));
+            }
         } else {
-            return f[j][k];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) o[k] = f[j][k];
         }
     }
 };
+
+// Shared-memory bytes of the weights of a pipelined launch (none for one or
+// two chunks per thread).
+__host__ __device__ constexpr int co_weight_smem_bytes(int J, int chunks_covered) {
+    return J >= 4 ? chunks_covered * 32 : 0;
+}
 
 // y = (h * inv) * w in place over h, in packed pairs (element k of chunks j
 // and j + 1; elements k and k + 1 of the one chunk when J == 1).
@@ -104,23 +120,27 @@ template <class E, int J>
 __device__ __forceinline__ void co_y(float (&h)[J][8], const CoWeights<E, J>& w, float inv) {
     const float2 iv = make_float2(inv, inv);
     if constexpr (J == 1) {
+        float wf[8];
+        w.get(0, wf);
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
-            const float2 t = mul2_rn(mul2_rn(make_float2(h[0][k], h[0][k + 1]), iv),
-                                     make_float2(w.get(0, k), w.get(0, k + 1)));
+            const float2 t = mul2_rn(mul2_rn(make_float2(h[0][k], h[0][k + 1]), iv), make_float2(wf[k], wf[k + 1]));
             h[0][k] = t.x;
             h[0][k + 1] = t.y;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < J; j += 2)
+        for (int j = 0; j < J; j += 2) {
+            float wa[8], wb[8];
+            w.get(j, wa);
+            w.get(j + 1, wb);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const float2 t = mul2_rn(mul2_rn(make_float2(h[j][k], h[j + 1][k]), iv),
-                                         make_float2(w.get(j, k), w.get(j + 1, k)));
+                const float2 t = mul2_rn(mul2_rn(make_float2(h[j][k], h[j + 1][k]), iv), make_float2(wa[k], wb[k]));
                 h[j][k] = t.x;
                 h[j + 1][k] = t.y;
             }
+        }
     }
 }
 
@@ -189,7 +209,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     }
 
     CoWeights<E, J> wts;
-    wts.load(a.w, c0, a.chunks);
+    wts.load(a.w, c0, a.chunks, reinterpret_cast<float4*>(ring + (size_t)stages * stage_bytes), warp, lane);
     const float sin = ModeTraits<MODE>::needs_scale_in ? __ldg(a.scale_in) : 0.0f;
     if constexpr (MODE == kNvfp4) fill_nvfp4_rtab(s_rtab, sin);   // ordered by the first row's barrier
     Fp8Recips rc_static = {0.0f, 0.0f};
