@@ -377,12 +377,12 @@ int rmsq_allreduce_add_rmsnorm_quant(const void *const *partials, int n_ranks, c
  * g_i = gate_up[t, i] and u_i = gate_up[t, d + i]; then exactly the
  * quantisation step of rmsq_fused_add_rmsnorm_quant with a in place of y
  * (every quant_mode; scales and codes laid out the same way with hidden = d).
- * e^x follows W. J. Cody and W. Waite's argument reduction with a degree-7
- * Taylor polynomial, each step a correctly rounded binary32 operation (within
- * 1.2 ulp of e^x over the normal range); the quotient is g times the
- * hardware's approximate reciprocal of 1 + e^-g (within one ulp), so a is
- * within 7.4 * 2^-24 relative of the exact silu(g) * u (results are
- * deterministic: the same inputs always give the same bytes).  Where e^-g
+ * e^x follows W. J. Cody and W. Waite's argument reduction, then the
+ * hardware's approximate 2^x on the reduced argument (within about 2.4 ulp
+ * of e^x over the normal range); the quotient is g times the hardware's
+ * approximate reciprocal of 1 + e^-g (within one ulp), so a is within
+ * 9.8 * 2^-24 relative of the exact silu(g) * u (results are deterministic:
+ * the same inputs always give the same bytes).  Where e^-g
  * overflows (g < -88.72) silu is -0.  The quantisation of a is exact, as in
  * the norm op.
  *  gate_up     device, [n_tokens, 2 d] bf16/fp16, row-major, 16-byte aligned.

@@ -12,15 +12,15 @@
 //
 // silu(g) is g times the approximate reciprocal of 1 + e^-g (the result is
 // compared with the oracle's correctly rounded silu within a bound derived
-// from these steps).  e^x is evaluated by W. J. Cody and W. Waite's method ("Software Manual for
-// the Elementary Functions", 1980): x = n ln2 + r with n = rint(x log2 e) and
-// ln2 split in a high part of 15 significant bits (n ln2_hi is exact) and the
-// rest, r formed by two fused multiply-adds; e^r by the degree-7 Taylor
-// polynomial in Horner form, one fused multiply-add per step; then the
-// scaling by 2^n in two power-of-two factors (the second is 1 unless 2^n is
-// not a normal binary32).  Every step is one correctly rounded binary32
-// operation in a fixed order, done in packed pairs where two elements take
-// the same step.
+// from these steps).  e^x is evaluated with W. J. Cody and W. Waite's
+// argument reduction ("Software Manual for the Elementary Functions", 1980):
+// x = n ln2 + r with n = rint(x log2 e) and ln2 split in a high part of 15
+// significant bits (n ln2_hi is exact) and the rest, r formed by two fused
+// multiply-adds; e^r = 2^(r log2 e) by the hardware approximation of 2^x on
+// that small argument; then the scaling by 2^n in two power-of-two factors
+// (the second is 1 unless 2^n is not a normal binary32).  Within about 2.4
+// ulp of e^x; every step is deterministic, done in packed pairs where two
+// elements take the same step.
 #pragma once
 
 #include "rmsq_dispatch.cuh"
@@ -28,6 +28,13 @@
 namespace rmsq {
 
 __device__ __forceinline__ float pow2_bits(int k) { return __int_as_float((k + 127) << 23); }
+
+// 2^a by the hardware approximation (ex2.approx, about two ulps).
+__device__ __forceinline__ float ex2_approx(float a) {
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
 
 // e^x for two elements.
 __device__ __forceinline__ float2 exp_cw2(float2 x) {
@@ -40,15 +47,8 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
     const float2 n = make_float2(rintf(t.x), rintf(t.y));
     const float2 nn = make_float2(-n.x, -n.y);
     const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), xc));
-    // 1/k!, k = 7 .. 0, rounded to binary32
-    float2 p = make_float2(1.98412701e-4f, 1.98412701e-4f);
-    p = fma2_rn(p, r, make_float2(1.38888892e-3f, 1.38888892e-3f));
-    p = fma2_rn(p, r, make_float2(8.33333377e-3f, 8.33333377e-3f));
-    p = fma2_rn(p, r, make_float2(4.16666679e-2f, 4.16666679e-2f));
-    p = fma2_rn(p, r, make_float2(1.66666672e-1f, 1.66666672e-1f));
-    p = fma2_rn(p, r, make_float2(0.5f, 0.5f));
-    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
-    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const float2 rl = mul2_rn(r, make_float2(log2e, log2e));
+    const float2 p = make_float2(ex2_approx(rl.x), ex2_approx(rl.y));
     // 2^k = 2^ka * 2^kb with both factors normal: ka = min(k, 127), or k + 64
     // below -126; kb = k - ka (0 unless 2^k alone is out of the normal range).
     const int k0 = __float2int_rn(n.x), k1 = __float2int_rn(n.y);
@@ -70,14 +70,8 @@ __device__ __forceinline__ float2 exp_cw2_mid(float2 x) {
     const float2 n = make_float2(rintf(t.x), rintf(t.y));
     const float2 nn = make_float2(-n.x, -n.y);
     const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), x));
-    float2 p = make_float2(1.98412701e-4f, 1.98412701e-4f);
-    p = fma2_rn(p, r, make_float2(1.38888892e-3f, 1.38888892e-3f));
-    p = fma2_rn(p, r, make_float2(8.33333377e-3f, 8.33333377e-3f));
-    p = fma2_rn(p, r, make_float2(4.16666679e-2f, 4.16666679e-2f));
-    p = fma2_rn(p, r, make_float2(1.66666672e-1f, 1.66666672e-1f));
-    p = fma2_rn(p, r, make_float2(0.5f, 0.5f));
-    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
-    p = fma2_rn(p, r, make_float2(1.0f, 1.0f));
+    const float2 rl = mul2_rn(r, make_float2(log2e, log2e));
+    const float2 p = make_float2(ex2_approx(rl.x), ex2_approx(rl.y));
     return mul2_rn(p, make_float2(pow2_bits(__float2int_rn(n.x)), pow2_bits(__float2int_rn(n.y))));
 }
 
@@ -90,9 +84,9 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 // a = silu(g) * u = g * (1 / (1 + e^-g)) * u for two elements; MID: both
-// |g| <= 87, where exp_cw2_mid(-g) equals exp_cw2(-g).  The quotient is g
-// times the approximate reciprocal of 1 + e^-g (one ulp), so silu is within
-// 6.4 * 2^-24 of its exact value: e^-g 1.2 ulp, the sum, the reciprocal and
+// |g| <= 87 (e^-g by exp_cw2_mid, else by exp_cw2).  The quotient is g times
+// the approximate reciprocal of 1 + e^-g (one ulp), so silu is within
+// 8.8 * 2^-24 of its exact value: e^-g 2.4 ulp, the sum, the reciprocal and
 // the product.
 template <bool MID = false>
 __device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
@@ -168,7 +162,7 @@ __global__ void __launch_bounds__(kActMaxThreads) act_rows_kernel(const RowArgs 
     if constexpr (SILU) {
         // The usual case (every gate of the thread within +-87, tested on the
         // bit patterns: a NaN or infinity fails it) takes the shorter e^x
-        // steps, with identical results.
+        // steps (the hardware 2^x on the reduced argument).
         uint32_t in_range = 0xffffffffu;
 #pragma unroll
         for (int j = 0; j < J; ++j) {

@@ -135,11 +135,38 @@ struct OccEntry {
     int blocks;
 };
 
-// Shared-memory ring budget per CTA (two CTAs per SM), and the opt-in
-// dynamic shared memory limit of a pipelined kernel (the ring plus, with four
-// or eight chunks per thread, the weights; the largest a CTA may use).
+// Shared-memory ring budget per CTA (two CTAs per SM).
 constexpr int kPipeSmemBudget = 110 * 1024;
-constexpr int kPipeSmemLimit = 227 * 1024;
+
+// The largest dynamic shared memory a CTA of `fn` may use on the current
+// device: the per-block opt-in maximum less the function's static shared
+// memory (cached per device and function; neither changes with a context
+// reset).
+inline int dyn_smem_limit(const void* fn, cudaError_t* err) {
+    struct Entry {
+        int dev;
+        const void* fn;
+        int limit;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int used = 0;
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].dev == dev && cache[i].fn == fn) return cache[i].limit;
+    int optin = 0;
+    *err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (*err != cudaSuccess) return 0;
+    cudaFuncAttributes fa;
+    *err = cudaFuncGetAttributes(&fa, fn);
+    if (*err != cudaSuccess) return 0;
+    const int limit = optin - static_cast<int>(fa.sharedSizeBytes);
+    if (used < 256) cache[used++] = {dev, fn, limit};
+    return limit;
+}
 
 // The opt-in dynamic shared memory limit of a pipelined instantiation (the
 // largest a CTA may use, so that no launch ever lowers it below what another
@@ -148,7 +175,10 @@ constexpr int kPipeSmemLimit = 227 * 1024;
 // before every launch (a host-side call, no device work): a second device, or
 // a device whose primary context was reset, never gets a launch without them.
 inline cudaError_t set_smem_attributes(const void* fn) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPipeSmemLimit);
+    cudaError_t e = cudaSuccess;
+    const int limit = dyn_smem_limit(fn, &e);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     // Prefer the largest shared-memory carve-out so that the rings of several
     // CTAs fit on one SM (the kernels barely use L1: loads bypass it).
     if (e == cudaSuccess && RMSQ_MAX_SMEM_CARVEOUT)

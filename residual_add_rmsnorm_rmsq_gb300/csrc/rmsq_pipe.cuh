@@ -66,10 +66,18 @@ __device__ __forceinline__ float co_warp_sum(const float (&h)[J][8]) {
 // only what it wrote, so no barrier is needed; the reads are volatile so that
 // the compiler keeps them in the row loop instead of hoisting them into
 // registers.
+// Compile-time tuning (results do not depend on it): 0 keeps the weights of
+// four or eight chunks per thread packed in registers instead.
+#ifndef RMSQ_PIPE_WSMEM
+#define RMSQ_PIPE_WSMEM 1
+#endif
+
 template <class E, int J>
 struct CoWeights {
-    static constexpr bool kSmem = J >= 4;
-    float f[kSmem ? 1 : J][8];
+    static constexpr bool kSmem = J >= 4 && RMSQ_PIPE_WSMEM;
+    static constexpr bool kPacked = J >= 4 && !RMSQ_PIPE_WSMEM;
+    float f[(kSmem || kPacked) ? 1 : J][8];
+    uint32_t pk[kPacked ? J : 1][4];
     float4* wsm;   // kSmem: this thread's first float4; chunk j at +(2 j) * 32 and +(2 j + 1) * 32
 
     __device__ __forceinline__ void load(const uint4* w, int c0, int chunks, float4* smem_w, int warp, int lane) {
@@ -85,6 +93,9 @@ struct CoWeights {
             if constexpr (kSmem) {
                 wsm[(2 * j) * 32] = make_float4(t[0], t[1], t[2], t[3]);
                 wsm[(2 * j + 1) * 32] = make_float4(t[4], t[5], t[6], t[7]);
+            } else if constexpr (kPacked) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) pk[j][k] = ws[k];
             } else {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) f[j][k] = t[k];
@@ -101,6 +112,16 @@ struct CoWeights {
                              : "=f"(o[4 * hf]), "=f"(o[4 * hf + 1]), "=f"(o[4 * hf + 2]), "=f"(o[4 * hf + 3])
                              : "r"(smem_u32(p)));
             }
+        } else if constexpr (kPacked) {
+            // through an empty volatile asm, so that the widening stays in the
+            // row loop instead of being hoisted into registers
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint32_t v = pk[j][k];
+                asm volatile("" : "+r"(v));
+                o[2 * k] = E::lo(v);
+                o[2 * k + 1] = E::hi(v);
+            }
         } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) o[k] = f[j][k];
@@ -111,7 +132,7 @@ struct CoWeights {
 // Shared-memory bytes of the weights of a pipelined launch (none for one or
 // two chunks per thread).
 __host__ __device__ constexpr int co_weight_smem_bytes(int J, int chunks_covered) {
-    return J >= 4 ? chunks_covered * 32 : 0;
+    return (J >= 4 && RMSQ_PIPE_WSMEM) ? chunks_covered * 32 : 0;
 }
 
 // y = (h * inv) * w in place over h, in packed pairs (element k of chunks j

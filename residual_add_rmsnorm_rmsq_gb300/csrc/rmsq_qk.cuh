@@ -306,14 +306,14 @@ __global__ void __maxnreg__(RMSQ_QK_PIPE_MAXNREG)
     };
     load_w(warp);
 
-    int k = 0;
+    int k = 0, s = 0;
+    uint32_t parity = 0;   // stage s and its phase, advanced per token (no division)
     bool faulted = false;
     for (;; ++k) {
         const int t = blockIdx.x + k * G;
         if (t >= a.n) break;
-        const int s = k % stages;
         // one answer per warp: the head math below shuffles across all lanes
-        const bool ok = __all_sync(kFull, mbar_wait_bounded(&full[s], static_cast<uint32_t>(k / stages) & 1u));
+        const bool ok = __all_sync(kFull, mbar_wait_bounded(&full[s], parity));
         const int64_t p = s_pos[s];
         if (ok && p >= 0 && p < a.max_pos) {
             const unsigned char* st = ring + (size_t)s * stage_bytes;
@@ -349,6 +349,10 @@ __global__ void __maxnreg__(RMSQ_QK_PIPE_MAXNREG)
             issue(k + stages, s, p_next);
             const int tn = blockIdx.x + (k + stages + 1) * G;
             if (tn < a.n) p_next = __ldg(a.pos + tn);
+        }
+        if (++s == stages) {
+            s = 0;
+            parity ^= 1u;
         }
     }
     if (faulted && tid == 0) {
