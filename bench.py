@@ -668,6 +668,12 @@ def run_ours(args, rank, world, dist):
     rq.load()
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     stream = torch.cuda.Stream()
+    if args.sweep_only:
+        if rank == 0:
+            peak, _ = measured_peak()
+            print(json.dumps({"sweep_only": args.sweep_only, "modes": sweep(torch, rq, stream, peak, args)}),
+                  flush=True)
+        return
 
     mk, mode = workload_spec(args.workload)
     wl = mk()
@@ -787,23 +793,30 @@ def decode_sweep(torch, rq, stream, args):
 def sweep(torch, rq, stream, peak, args):
     """Every quant mode on its n_tokens >= 4096 workload (GB/s, fraction of
     peak), the unfused two-op sequence beside the fused op on two of them,
-    QK-norm + RoPE on a Qwen3-shaped attention input (4096 tokens, 32 + 4 + 4
-    heads of 128), and SiLU+Mul + quantisation on a Llama-8B-shaped MLP
-    activation (4096 tokens, d = 14336)."""
+    QK-norm + RoPE on a Qwen3-shaped attention input (4096 / 16384 tokens,
+    32 + 4 + 4 heads of 128), all-reduce + RMSNorm on the Llama layer (2 and 8
+    emulated ranks), and SiLU+Mul + quantisation on a Llama-8B-shaped MLP
+    activation (4096 tokens, d = 14336).  With --sweep-only REGEX, only the
+    entries whose name matches."""
+    import re
     import rmsq_inputs as ri
     out = {}
-    groups = [
-        (lambda: ri.llama(4096, True), ["llama_fp8_per_token", "llama_fp8_static"]),
-        (lambda: ri.llama(4096, False), ["llama_fp8_per_token_nores"]),
-        (lambda: ri.dsv3(8192), ["dsv3_fp8_group128_row", "dsv3_fp8_group128_col",
-                                 "dsv3_fp8_group64_row", "dsv3_fp8_group64_col"]),
-        (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096", "qwen_nvfp4_dynamic_4096"]),
-        (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384", "qwen_nvfp4_dynamic_16384"]),
-    ]
+    want = re.compile(args.sweep_only) if args.sweep_only else None
+
+    def wanted(name):
+        return want is None or want.search(name) is not None
+
+    def entry(name, ms, nbytes, tokens, **extra):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "tokens_per_s": round(tokens / (ms / 1e3), 1), "bytes": nbytes, **extra}
+
     # The unfused two-op sequence on the same workloads, for the fusion's
     # saving at kernel level: time per step of both ops against the fused op.
     for make, name, mode in ((lambda: ri.llama(4096, True), "llama_fp8_per_token", "fp8_per_token"),
                              (lambda: ri.dsv3(8192), "dsv3_fp8_group128_row", "fp8_group128_row")):
+        if not wanted(f"{name}_unfused"):
+            continue
         wl = make()
         fb = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
         fused_ms = time_launches(torch, rq, wl, mode, fb, args.sweep_steps, 5, stream)
@@ -817,50 +830,78 @@ def sweep(torch, rq, stream, peak, args):
         del ub, wl
         torch.cuda.empty_cache()
     for n_qk in (4096, 16384):
+        name = f"qwen_qk_norm_rope_{n_qk}"
+        if not wanted(name):
+            continue
         qk = ri.qwen_qk(n_qk)
         qb = QkBuffers(torch, rq, qk, 4 * L2_BYTES + 1)
-        ms = time_launches(torch, rq, qk, None, qb, args.sweep_steps, 5, stream)
-        gbs = qb.bytes / (ms / 1e3) / 1e9
-        out[f"qwen_qk_norm_rope_{n_qk}"] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1),
-                                           "frac": round(gbs / peak, 4),
-                                           "tokens_per_s": round(qk.n_tokens / (ms / 1e3), 1), "bytes": qb.bytes}
+        entry(name, time_launches(torch, rq, qk, None, qb, args.sweep_steps, 5, stream), qb.bytes, qk.n_tokens)
         del qb, qk
         torch.cuda.empty_cache()
     # all-reduce + RMSNorm at the token counts the fusion is meant for (the
     # pages: profitable at small num_tokens), 2 and 8 ranks, on the Llama layer
     for ranks in (2, 8):
         for n_ar in (16, 256, 2048):
-            wl = ri.llama(n_ar, True)
             for mode in ("fp8_static", "nvfp4"):
+                name = f"allreduce_r{ranks}_{n_ar}x4096_{mode}"
+                if not wanted(name):
+                    continue
+                wl = ri.llama(n_ar, True)
                 ab = AllReduceBuffers(torch, rq, wl, mode, ranks, 4 * L2_BYTES + 1, max_sets=64)
                 ms = time_launches(torch, rq, wl, mode, ab, args.sweep_steps, 5, stream)
-                gbs = ab.bytes / (ms / 1e3) / 1e9
-                out[f"allreduce_r{ranks}_{n_ar}x4096_{mode}"] = {
-                    "us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                    "bytes": ab.bytes, "l2": "inputs > L2" if ab.sets * ab.bytes > 4 * L2_BYTES else "L2-resident"}
-                del ab
-            del wl
+                entry(name, ms, ab.bytes, n_ar,
+                      l2="inputs > L2" if ab.sets * ab.bytes > 4 * L2_BYTES else "L2-resident")
+                del ab, wl
         torch.cuda.empty_cache()
-    act = ri.llama_mlp(4096)
+    act = None
     for mode in ("fp8_static", "fp8_group128_row", "nvfp4"):
         name = f"llama_mlp_silu_mul_{mode}"
+        if not wanted(name):
+            continue
+        act = act or ri.llama_mlp(4096)
         bufs = ActBuffers(torch, rq, act, mode, 4 * L2_BYTES + 1)
-        ms = time_launches(torch, rq, act, mode, bufs, args.sweep_steps, 5, stream)
-        gbs = bufs.bytes / (ms / 1e3) / 1e9
-        out[name] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                     "tokens_per_s": round(act.n_tokens / (ms / 1e3), 1), "bytes": bufs.bytes}
+        entry(name, time_launches(torch, rq, act, mode, bufs, args.sweep_steps, 5, stream), bufs.bytes,
+              act.n_tokens)
         del bufs
         torch.cuda.empty_cache()
     del act
+    # Launch time against batch size on the Llama layer (per-token, residual):
+    # the slope is the steady-state cost per row, the intercept the fixed cost
+    # of a launch (ramp-up of the first copies, the last rows, completion).
+    for n_scan in (512, 1024, 2048, 4096, 8192, 16384):
+        name = f"scan_llama_fp8_per_token_{n_scan}"
+        if not wanted(name):
+            continue
+        wl = ri.llama(n_scan, True)
+        bufs = Buffers(torch, rq, wl, "fp8_per_token", 4 * L2_BYTES + 1)
+        entry(name, time_launches(torch, rq, wl, "fp8_per_token", bufs, args.sweep_steps, 5, stream), bufs.bytes,
+              n_scan)
+        del bufs, wl
+        torch.cuda.empty_cache()
+    scan = [(int(k.rsplit("_", 1)[1]), v["us"]) for k, v in out.items() if k.startswith("scan_")]
+    if len(scan) >= 2:
+        xs, ys = np.array([a for a, _ in scan], float), np.array([b for _, b in scan], float)
+        slope, icpt = np.polyfit(xs, ys, 1)
+        out["scan_llama_fp8_per_token_fit"] = {"ns_per_row": round(slope * 1e3, 3), "intercept_us": round(icpt, 3),
+                                               "steady_GB/s": round(28676 / slope / 1e3, 1)}
+    groups = [
+        (lambda: ri.llama(4096, True), ["llama_fp8_per_token", "llama_fp8_static"]),
+        (lambda: ri.llama(4096, False), ["llama_fp8_per_token_nores"]),
+        (lambda: ri.dsv3(8192), ["dsv3_fp8_group128_row", "dsv3_fp8_group128_col",
+                                 "dsv3_fp8_group64_row", "dsv3_fp8_group64_col"]),
+        (lambda: ri.qwen_nvfp4(4096), ["qwen_nvfp4_4096", "qwen_nvfp4_dynamic_4096"]),
+        (lambda: ri.qwen_nvfp4(16384), ["qwen_nvfp4_16384", "qwen_nvfp4_dynamic_16384"]),
+    ]
     for make, names in groups:
+        names = [n for n in names if wanted(n)]
+        if not names:
+            continue
         wl = make()
         for name in names:
             mode = workload_spec(name)[1]
             bufs = Buffers(torch, rq, wl, mode, 4 * L2_BYTES + 1)
-            ms = time_launches(torch, rq, wl, mode, bufs, args.sweep_steps, 5, stream)
-            gbs = bufs.bytes / (ms / 1e3) / 1e9
-            out[name] = {"us": round(ms * 1e3, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                         "tokens_per_s": round(wl.n_tokens / (ms / 1e3), 1), "bytes": bufs.bytes}
+            entry(name, time_launches(torch, rq, wl, mode, bufs, args.sweep_steps, 5, stream), bufs.bytes,
+                  wl.n_tokens)
             del bufs
             torch.cuda.empty_cache()
     return out
@@ -877,6 +918,8 @@ def main():
                     help="seconds of untimed replays around the timed region, for the clock samples")
     ap.add_argument("--sweep-steps", type=int, default=300)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-only", default=None,
+                    help="regex: run only these sweep entries and print them (no headline line); for profiling")
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--variant", choices=["auto", "direct", "pipelined"], default="auto")

@@ -179,12 +179,16 @@ __device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
 // packed multiply-adds left elsewhere multiply exact squares or scale by
 // powers of two, where fused and separate roundings agree.
 __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+#if RMSQ_F32X2
     float2 d;
     asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
         "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
         "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
+#else
+    return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+#endif
 }
 
 // ---------------------------------------------------------------------------
