@@ -65,9 +65,11 @@ def test_all_zero_batch_uses_unit_global_scale():
         assert got["global_scale"][0] == 1.0 and not got["q"].any() and not got["scales"].any()
 
 
-def test_in_place_and_reused_workspace():
-    """The workspace is scratch: stale contents from another call must not leak."""
-    ws = torch.full((rq.nvfp4_dynamic_workspace_bytes(4096),), 0x7F, dtype=torch.uint8, device="cuda")
+@pytest.mark.parametrize("fill", [0x00, 0x7F, 0xFF])
+def test_in_place_and_reused_workspace(fill):
+    """The workspace is scratch: neither its contents on entry (a constant
+    byte) nor what another call left there may leak into a call."""
+    ws = torch.full((rq.nvfp4_dynamic_workspace_bytes(4096),), fill, dtype=torch.uint8, device="cuda")
     for seed in (1, 2):
         wl = ri.make_workload(f"inplace_{seed}", 300, 2048, res_sigma=1.0 + seed, seed=40 + seed)
         check_dyn(wl, f"inplace_{seed}", in_place=True, workspace=ws)
