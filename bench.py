@@ -174,24 +174,26 @@ def profiled_traffic(kernel_name: str, digest: str):
     return e.get("dram_bytes_per_launch")
 
 
+def launch_shape(wl, mode: str, residual: bool, torch) -> dict:
+    """The launch the library makes for this workload on this device
+    (rmsq_query_launch): kernel variant, chunks per thread, ring stages, CTAs,
+    threads per CTA."""
+    import residual_add_rmsnorm_rmsq_gb300 as rq
+    qmode = "nvfp4" if mode == "nvfp4_dynamic" else mode
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float16
+    return rq.query_launch(qmode, wl.n_tokens, wl.hidden, residual, tdt, VARIANT)
+
+
 def kernel_name(wl, mode: str, residual: bool, torch) -> str:
     """Name (as ncu prints it, without the namespace) of the row kernel the
-    library launches for this workload: the pipelined kernel from 4 rows per SM
-    on (direct kernel below); its chunks per thread: 2 with a residual, 4
-    without from hidden 2048 up, doubled while a row would need more than 512
-    threads)."""
+    library launches for this workload (for the data-derived NVFP4 scale, its
+    first kernel), from the library's own launch choice."""
     import residual_add_rmsnorm_rmsq_gb300 as rq
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    pipelined = VARIANT == "pipelined" or (VARIANT == "auto" and wl.n_tokens >= 4 * sms)
+    shape = launch_shape(wl, mode, residual, torch)
     e = "Bf16T" if wl.dtype == "bf16" else "Fp16T"
-    m = rq.MODES["nvfp4" if mode == "nvfp4_dynamic" else mode]
-    chunks = wl.hidden // 8
-    if pipelined:
-        j = 4 if (not residual and chunks >= 256) else 2
-        while j < 8 and -(-chunks // (32 * j)) * 32 > 512:
-            j *= 2
-        return f"pipe_entry<{e}, {m}, {int(residual)}, {j}>"
-    return f"rows_kernel<{e}, {m}, {int(residual)}, {1 if chunks <= 1024 else 2}>"
+    m = 7 if mode == "nvfp4_dynamic" else rq.MODES[mode]
+    kind = "pipe_entry" if shape["pipelined"] else "rows_kernel"
+    return f"{kind}<{e}, {m}, {int(residual)}, {shape['chunks_per_thread']}>"
 
 
 def workload_spec(name: str):
@@ -729,7 +731,8 @@ def run_ours(args, rank, world, dist):
         "dtype": "bf16", "data": "synthetic (seeded splitmix64/Box-Muller, shapes of the pages' workloads)",
         "tokens_per_s": round(tokens_s, 1),
         "config": workload_config(args.workload, wl, mode),
-        "launch": {"variant": VARIANT, "kernel": kname, "buffer_sets": bufs.sets,
+        "launch": {"variant": VARIANT, "kernel": kname, "shape": launch_shape(wl, mode, bufs.res, torch),
+                   "buffer_sets": bufs.sets,
                    "bytes_per_step": per_launch,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

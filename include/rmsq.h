@@ -448,6 +448,21 @@ int rmsq_query_sizes(int quant_mode, int64_t n_tokens, int64_t hidden, size_t *q
                      size_t *scale_bytes);
 
 /*
+ * rmsq_query_launch — the launch rmsq_fused_add_rmsnorm_quant_ex would make on
+ * the current device for a mode, shape, residual (0/1), dtype and variant,
+ * without launching anything: out[0] = 1 for the pipelined kernel, 0 for the
+ * direct one; out[1] = 16-byte chunks per thread; out[2] = ring stages (0
+ * for the direct kernel); out[3] = CTAs; out[4] = threads per CTA (all 0 for
+ * n_tokens = 0).  The pages have no counterpart: it reports this
+ * implementation's choice (for profiling and tuning).  out: host, 5 int32.
+ * Errors as for rmsq_fused_add_rmsnorm_quant_ex's mode, shape, dtype and
+ * variant; RMSQ_ERR_NO_DEVICE / RMSQ_ERR_UNSUPPORTED_DEVICE without a
+ * suitable device.
+ */
+int rmsq_query_launch(int quant_mode, int64_t n_tokens, int64_t hidden, int has_residual, int dtype,
+                      int variant, int32_t *out);
+
+/*
  * rmsq_debug_convert — the library's own fp32 -> 8-bit / 4-bit conversions on
  * a device array, so that tests can pin them against a reference encoder.
  * kind 0: out[i] = e4m3(in[i]) (E4M3FN, nearest even, saturating);

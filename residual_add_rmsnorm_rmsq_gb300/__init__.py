@@ -62,7 +62,7 @@ EXPORTS = ("rmsq_fused_add_rmsnorm_quant", "rmsq_fused_add_rmsnorm_quant_ex",
            "rmsq_fused_add_rmsnorm", "rmsq_quant", "rmsq_qk_norm_rope", "rmsq_qk_norm_rope_ex",
            "rmsq_allreduce_add_rmsnorm_quant",
            "rmsq_set_pipeline_config", "rmsq_set_programmatic_launch", "rmsq_take_fault_flags",
-           "rmsq_query_sizes", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
+           "rmsq_query_sizes", "rmsq_query_launch", "rmsq_debug_convert", "rmsq_debug_activation", "rmsq_debug_bounded_wait",
            "rmsq_status_string", "rmsq_last_cuda_error", "rmsq_version")
 
 
@@ -122,6 +122,8 @@ def load(path: str | None = None):
         L.rmsq_query_sizes.argtypes = [ci, i64, i64, ctypes.POINTER(ctypes.c_size_t),
                                        ctypes.POINTER(ctypes.c_size_t)]
         L.rmsq_query_sizes.restype = ci
+        L.rmsq_query_launch.argtypes = [ci, i64, i64, ci, ci, ci, ctypes.POINTER(ctypes.c_int32)]
+        L.rmsq_query_launch.restype = ci
         L.rmsq_debug_convert.argtypes = [ci, vp, vp, i64, vp]
         L.rmsq_debug_convert.restype = ci
         L.rmsq_debug_activation.argtypes = [ci, vp, vp, vp, i64, vp]
@@ -409,6 +411,20 @@ def fused_add_rmsnorm_nvfp4_dynamic(x: torch.Tensor, residual: torch.Tensor | No
     if st:
         raise RmsqError(st, "rmsq_fused_add_rmsnorm_nvfp4_dynamic")
     return out_q, out_scales, out_global_scale, residual_out
+
+
+def query_launch(mode: str, n_tokens: int, hidden: int, residual: bool = True, dtype=torch.bfloat16,
+                 variant: str = "auto") -> dict:
+    """rmsq_query_launch: the launch the fused op would make on the current
+    device for this mode and shape (kernel variant, chunks per thread, ring
+    stages, CTAs, threads per CTA); nothing is launched."""
+    out = (ctypes.c_int32 * 5)()
+    st = load().rmsq_query_launch(mode_code(mode), n_tokens, hidden, 1 if residual else 0, DTYPES[dtype],
+                                  _variant(variant), out)
+    if st:
+        raise RmsqError(st, "rmsq_query_launch")
+    return {"pipelined": bool(out[0]), "chunks_per_thread": out[1], "stages": out[2], "ctas": out[3],
+            "threads": out[4]}
 
 
 def set_pipeline_config(chunks_per_thread: int = 0, stages: int = 0, ctas_per_sm: int = 0,

@@ -244,6 +244,40 @@ int rmsq_fused_add_rmsnorm_quant_ex(const void* x, const void* residual, const v
     return RMSQ_OK;
 }
 
+int rmsq_query_launch(int quant_mode, int64_t n_tokens, int64_t hidden, int has_residual, int dtype, int variant,
+                      int32_t* out) {
+    if (dtype != RMSQ_BF16 && dtype != RMSQ_FP16) return RMSQ_ERR_INVALID_ARG;
+    if (variant != RMSQ_VARIANT_AUTO && variant != RMSQ_VARIANT_DIRECT && variant != RMSQ_VARIANT_PIPELINED)
+        return RMSQ_ERR_INVALID_ARG;
+    if ((has_residual != 0 && has_residual != 1) || !out) return RMSQ_ERR_INVALID_ARG;
+    int st = check_shape(quant_mode, n_tokens, hidden);
+    if (st != RMSQ_OK) return st;
+    if (n_tokens == 0) {
+        for (int i = 0; i < 5; ++i) out[i] = 0;
+        return RMSQ_OK;
+    }
+    st = check_device();
+    if (st != RMSQ_OK) return st;
+    // Only the shape matters for the plan; the pointers stand for aligned
+    // buffers (the direct kernel's paired accesses take them when they are).
+    alignas(32) static unsigned char dummy[32];
+    rmsq::LaunchArgs la = {};
+    la.x = dummy;
+    la.res = has_residual ? dummy : nullptr;
+    la.w = dummy;
+    la.res_out = has_residual ? dummy : nullptr;
+    la.mode = quant_mode & RMSQ_QUANT_MODE_MASK;
+    la.n = static_cast<int>(n_tokens);
+    la.hidden = static_cast<int>(hidden);
+    la.variant = variant == RMSQ_VARIANT_DIRECT ? rmsq::kVariantDirect
+                 : variant == RMSQ_VARIANT_PIPELINED ? rmsq::kVariantPipelined : rmsq::kVariantAuto;
+    int v[5] = {0, 0, 0, 0, 0};
+    const cudaError_t e = dtype == RMSQ_BF16 ? rmsq::query_rows_bf16(la, v) : rmsq::query_rows_fp16(la, v);
+    if (e != cudaSuccess) return fail_cuda(e);
+    for (int i = 0; i < 5; ++i) out[i] = v[i];
+    return RMSQ_OK;
+}
+
 int rmsq_allreduce_add_rmsnorm_quant(const void* const* partials, int n_ranks, const void* residual,
                                      const void* weight, float eps, int quant_mode, const float* scale_in,
                                      void* out_q, void* out_scales, void* residual_out, int64_t n_tokens,

@@ -262,23 +262,42 @@ struct PipePlan {
 // elements.
 inline int pipe_default_j(int chunks, bool res) { return (!res && chunks >= 256) ? 4 : 2; }
 
+// Chunks per thread when the CTAs have many rows each (below): four with a
+// residual above hidden 2048, eight without from hidden 4096 (else as the
+// default).
+inline int pipe_many_rows_j(int chunks, bool res) {
+    if (res) return chunks > 256 ? 4 : 2;
+    return chunks >= 512 ? 8 : pipe_default_j(chunks, res);
+}
+
+// The plan for J chunks per thread (doubled while a row would need more than
+// 512 threads) and `stages` ring stages (fewer if the ring would not fit the
+// budget).
+inline PipePlan make_pipe_plan(const RowArgs& a, bool res, int J, int stages) {
+    auto threads_for = [&](int j) { return ((a.chunks + 32 * j - 1) / (32 * j)) * 32; };
+    PipePlan p;
+    p.J = J;
+    while (p.J < 8 && threads_for(p.J) > kPipeMaxThreads) p.J *= 2;
+    p.threads = threads_for(p.J);
+    const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
+    p.stages = stages;
+    while (p.stages > 1 && p.stages * stage_bytes > kPipeSmemBudget) --p.stages;
+    // The weights (four or eight chunks per thread) sit after the ring.
+    p.smem = p.stages * stage_bytes + co_weight_smem_bytes(p.J, p.threads * p.J);
+    return p;
+}
+
 inline PipePlan pipe_plan(const RowArgs& a, bool res) {
     const PipeTuning tune = get_pipe_tuning();
     auto threads_for = [&](int j) { return ((a.chunks + 32 * j - 1) / (32 * j)) * 32; };
-    PipePlan p;
-    p.J = pipe_default_j(a.chunks, res);
-    while (p.J < 8 && threads_for(p.J) > kPipeMaxThreads) p.J *= 2;
+    int J = pipe_default_j(a.chunks, res);
     const int tj = tune.chunks_per_thread;
-    if ((tj == 1 || tj == 2 || tj == 4 || tj == 8) && threads_for(tj) <= kPipeMaxThreads) p.J = tj;
-    p.threads = threads_for(p.J);
-    const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);   // x (+ residual) of one row
-    p.stages = pipe_stages(stage_bytes);
+    if ((tj == 1 || tj == 2 || tj == 4 || tj == 8) && threads_for(tj) <= kPipeMaxThreads) J = tj;
+    const int stage_bytes = a.chunks * 16 * (res ? 2 : 1);
+    int stages = pipe_stages(stage_bytes);
     if (tune.stages >= 1 && tune.stages <= kMaxStages && tune.stages * stage_bytes <= kPipeSmemBudget)
-        p.stages = tune.stages;
-    // The weights (four or eight chunks per thread) sit after the ring.
-    const int wbytes = co_weight_smem_bytes(p.J, p.threads * p.J);
-    p.smem = p.stages * stage_bytes + wbytes;
-    return p;
+        stages = tune.stages;
+    return make_pipe_plan(a, res, J, stages);
 }
 
 // Persistent grid of `fn` for a plan: as many CTAs as fit on the SMs at once
@@ -296,37 +315,96 @@ inline cudaError_t pipe_grid(const void* fn, const PipePlan& p, int n, int* grid
     return cudaSuccess;
 }
 
+// Rows per CTA from which the many-rows plan is taken.
+constexpr int kManyRowsPerCta = 8;
+
+// The launch of the row work for `la`: kernel, grid, block, plan.
+struct RowLaunch {
+    bool pipe;
+    const void* fn;
+    int grid, threads, smem, stages, J;
+};
+
+// Chooses the variant (direct kernel below kPipeMinRowsPerSm rows per SM,
+// unless one is forced) and, for the pipelined kernel, the plan (measured on
+// GB300): when each CTA of the persistent grid gets at least
+// kManyRowsPerCta rows, a one-stage ring with pipe_many_rows_j chunks per
+// thread, whose smaller CTAs and rings let more CTAs share an SM (hidden
+// 7168 with a residual, 8192 rows: 71.4 -> 68.9 us; hidden 8192: 53 -> 40
+// us; Qwen-shaped NVFP4, 16384 rows: 37.3 -> 36.0 us); with fewer rows per
+// CTA the two-stage ring's head start at the kernel's beginning weighs more
+// and pipe_plan's default stays (Llama- and Qwen-shaped layers of 4096
+// rows).  A tuning setting of the chunks per thread or the stages keeps
+// pipe_plan as tuned.
+template <class E>
+cudaError_t plan_rows(const LaunchArgs& la, const RowArgs& a, RowLaunch* out) {
+    const bool res = la.res != nullptr;
+    cudaError_t err = cudaSuccess;
+    const int sms = sm_count(&err);
+    if (err != cudaSuccess) return err;
+    out->pipe = la.variant == kVariantPipelined ||
+                (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
+    if (!out->pipe) {
+        out->J = a.chunks <= 1024 ? 1 : 2;
+        out->threads = ((a.chunks + out->J - 1) / out->J + 31) / 32 * 32;
+        out->fn = pick_kernel<E>(la.mode, res, false, out->J);
+        out->grid = a.n;
+        out->smem = 0;
+        out->stages = 0;
+        return out->fn ? cudaSuccess : cudaErrorInvalidValue;
+    }
+    const PipeTuning tune = get_pipe_tuning();
+    PipePlan p = pipe_plan(a, res);
+    const void* fn = pick_kernel<E>(la.mode, res, true, p.J);
+    if (!fn) return cudaErrorInvalidValue;
+    int grid = 0;
+    err = pipe_grid(fn, p, a.n, &grid);
+    if (err != cudaSuccess) return err;
+    if (tune.chunks_per_thread == 0 && tune.stages == 0) {
+        const PipePlan q = make_pipe_plan(a, res, pipe_many_rows_j(a.chunks, res), 1);
+        const void* fq = pick_kernel<E>(la.mode, res, true, q.J);
+        int gq = 0;
+        if (!fq) return cudaErrorInvalidValue;
+        err = pipe_grid(fq, q, a.n, &gq);
+        if (err != cudaSuccess) return err;
+        if ((int64_t)a.n >= (int64_t)kManyRowsPerCta * gq) {
+            p = q;
+            fn = fq;
+            grid = gq;
+        }
+    }
+    out->fn = fn;
+    out->grid = grid;
+    out->threads = p.threads;
+    out->smem = p.smem;
+    out->stages = p.stages;
+    out->J = p.J;
+    return cudaSuccess;
+}
+
 // One launch of the row work; *grid_out (if given) receives the number of
 // CTAs launched.
 template <class E>
 cudaError_t launch_rows(const LaunchArgs& la, cudaStream_t stream, int* grid_out = nullptr) {
     RowArgs a = make_row_args(la);
-    const bool res = la.res != nullptr;
-    cudaError_t err = cudaSuccess;
-    const int sms = sm_count(&err);
+    RowLaunch l;
+    const cudaError_t err = plan_rows<E>(la, a, &l);
     if (err != cudaSuccess) return err;
-    bool pipe = la.variant == kVariantPipelined ||
-                (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
-
-    if (pipe) {
-        const PipePlan p = pipe_plan(a, res);
-        const void* fn = pick_kernel<E>(la.mode, res, true, p.J);
-        if (!fn) return cudaErrorInvalidValue;
-        int grid = 0;
-        err = pipe_grid(fn, p, a.n, &grid);
-        if (err != cudaSuccess) return err;
-        int st = p.stages;
+    if (grid_out) *grid_out = l.grid;
+    if (l.pipe) {
+        int st = l.stages;
         void* params[] = {&a, &st};
-        if (grid_out) *grid_out = grid;
-        return launch_kernel(fn, dim3(grid), dim3(p.threads), params, p.smem, stream);
+        return launch_kernel(l.fn, dim3(l.grid), dim3(l.threads), params, l.smem, stream);
     }
-    const int J = a.chunks <= 1024 ? 1 : 2;
-    const int threads = ((a.chunks + J - 1) / J + 31) / 32 * 32;
-    const void* fn = pick_kernel<E>(la.mode, res, false, J);
-    if (!fn) return cudaErrorInvalidValue;
     void* params[] = {&a};
-    if (grid_out) *grid_out = a.n;
-    return launch_kernel(fn, dim3(a.n), dim3(threads), params, 0, stream);
+    return launch_kernel(l.fn, dim3(l.grid), dim3(l.threads), params, 0, stream);
+}
+
+// The launch launch_rows would make for `la` (no launch).
+template <class E>
+cudaError_t query_rows(const LaunchArgs& la, RowLaunch* out) {
+    const RowArgs a = make_row_args(la);
+    return plan_rows<E>(la, a, out);
 }
 
 // NVFP4 with a data-derived global scale: pass 1 (row kernel, mode

@@ -51,6 +51,10 @@ void set_programmatic_launch(bool on);
 // One launch of the row kernel for bf16 / fp16 activations.
 cudaError_t launch_rows_bf16(const LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_rows_fp16(const LaunchArgs& a, cudaStream_t stream);
+// The launch launch_rows_* would make (none is made): out = {pipelined (0/1),
+// chunks per thread, ring stages, CTAs, threads per CTA}.
+cudaError_t query_rows_bf16(const LaunchArgs& a, int* out);
+cudaError_t query_rows_fp16(const LaunchArgs& a, int* out);
 // NVFP4 with a data-derived global scale (two passes); `workspace` holds the
 // batch amax word and the per-row inv_rms.
 cudaError_t launch_nvfp4_dynamic_bf16(const LaunchArgs& a, void* workspace, float* out_gs, cudaStream_t stream);

@@ -277,6 +277,21 @@ def test_qk_norm_rope_argument_errors(L):
             assert qk(v=v) == rq.ERR_NO_DEVICE
 
 
+def test_query_launch_argument_errors(L):
+    out = (ctypes.c_int32 * 5)()
+    assert L.rmsq_query_launch(1, 16, 4096, 1, 2, 0, out) == rq.ERR_INVALID_ARG       # dtype
+    assert L.rmsq_query_launch(1, 16, 4096, 1, 0, 3, out) == rq.ERR_INVALID_ARG       # variant
+    assert L.rmsq_query_launch(1, 16, 4096, 2, 0, 0, out) == rq.ERR_INVALID_ARG       # residual flag
+    assert L.rmsq_query_launch(1, 16, 4096, 1, 0, 0, None) == rq.ERR_INVALID_ARG
+    assert L.rmsq_query_launch(9, 16, 4096, 1, 0, 0, out) == rq.ERR_INVALID_ARG       # mode
+    assert L.rmsq_query_launch(2, 16, 4000, 1, 0, 0, out) == rq.ERR_UNSUPPORTED_SHAPE  # not a multiple of 128
+    for i in range(5):
+        out[i] = 7
+    assert L.rmsq_query_launch(1, 0, 4096, 1, 0, 0, out) == rq.OK and list(out) == [0] * 5
+    if not torch.cuda.is_available():
+        assert L.rmsq_query_launch(1, 16, 4096, 1, 0, 0, out) == rq.ERR_NO_DEVICE
+
+
 def test_process_wide_switches(L):
     """The tuning switches only store settings: valid values are accepted,
     others rejected, and the defaults are put back."""
