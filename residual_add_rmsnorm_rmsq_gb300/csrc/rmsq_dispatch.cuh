@@ -5,11 +5,13 @@
 //             hidden 8192, else 2), loads straight into registers.
 //  pipelined: persistent CTAs (as many as fit on the SMs), `stages` rows of
 //             x / residual in flight per CTA through the shared-memory ring.
-//             J = 2 up to hidden 8192, else 4 (<= 512 threads); two stages
-//             per CTA by default, so that up to 3-4 CTAs share an SM: the
-//             per-row dependency chain (two block reductions, IEEE divide and
-//             square root) rather than bytes in flight limits a CTA, so more
-//             CTAs per SM beat a deeper ring (measured on GB300).
+//             The per-row dependency chain (block reductions, IEEE divide
+//             and square root) rather than bytes in flight limits a CTA, so
+//             more CTAs per SM beat a deeper ring (measured on GB300): two
+//             stages and J = 2 with a residual (4 without) when the CTAs get
+//             few rows each, one stage and J = 4 (8 without a residual) from
+//             8 rows per CTA on (plan_rows); J doubled while a row would need
+//             more than 512 threads.
 #pragma once
 
 #include <atomic>
