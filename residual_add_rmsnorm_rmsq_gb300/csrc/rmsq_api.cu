@@ -623,12 +623,13 @@ int rmsq_take_fault_flags(uint32_t* flags) {
     if (!flags) return RMSQ_ERR_INVALID_ARG;
     const int st = check_device();
     if (st != RMSQ_OK) return st;
-    unsigned int a = 0, b = 0, c = 0;
+    unsigned int a = 0, b = 0, c = 0, d = 0;
     cudaError_t e = rmsq::take_pipe_fault_bf16(&a);
     if (e == cudaSuccess) e = rmsq::take_pipe_fault_fp16(&b);
     if (e == cudaSuccess) e = rmsq::take_pipe_fault_qk(&c);
+    if (e == cudaSuccess) e = rmsq::take_pipe_fault_ar(&d);
     if (e != cudaSuccess) return fail_cuda(e);
-    *flags = a | b | c;
+    *flags = a | b | c | d;
     return RMSQ_OK;
 }
 

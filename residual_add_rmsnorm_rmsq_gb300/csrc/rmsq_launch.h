@@ -102,6 +102,7 @@ cudaError_t launch_allreduce_rows(const LaunchArgs& la, const void* const* parti
 cudaError_t take_pipe_fault_bf16(unsigned int* out);
 cudaError_t take_pipe_fault_fp16(unsigned int* out);
 cudaError_t take_pipe_fault_qk(unsigned int* out);
+cudaError_t take_pipe_fault_ar(unsigned int* out);
 cudaError_t launch_convert(int kind, const float* in, uint8_t* out, int64_t n, cudaStream_t stream);
 
 }  // namespace rmsq

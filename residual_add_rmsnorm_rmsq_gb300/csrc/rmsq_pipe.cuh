@@ -25,9 +25,42 @@
 // (again bounded) and returns.
 #pragma once
 
+#include "rmsq_launch.h"
 #include "rmsq_rowmath.cuh"
 
 namespace rmsq {
+
+// The ranks' partial-sum buffers of the all-reduce variant, passed by value
+// in the kernel parameters.
+struct ArRanks {
+    const uint4* part[kMaxArRanks];
+    int n;
+};
+
+// x = T(sum over ranks of fp32(partial)) for one chunk whose n partials sit
+// `stride` chunks apart in shared memory: rank order, one rounding at the
+// end (the all-reduce's reduction; the direct all-reduce kernel adds the same
+// values in the same order).
+template <class E>
+__device__ __forceinline__ uint4 ar_chunk_sum(const uint4* p, int stride, int n) {
+    const uint4 v0 = p[0];
+    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { acc[2 * k] = E::lo(w0[k]); acc[2 * k + 1] = E::hi(w0[k]); }
+    for (int r = 1; r < n; ++r) {
+        const uint4 v = p[(size_t)r * stride];
+        const uint32_t wr[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 t = add2_rn(make_float2(acc[2 * k], acc[2 * k + 1]), make_float2(E::lo(wr[k]), E::hi(wr[k])));
+            acc[2 * k] = t.x;
+            acc[2 * k + 1] = t.y;
+        }
+    }
+    return make_uint4(E::pack(acc[0], acc[1]), E::pack(acc[2], acc[3]), E::pack(acc[4], acc[5]),
+                      E::pack(acc[6], acc[7]));
+}
 
 constexpr int kMaxStages = 8;
 constexpr int kPipeMaxThreads = 512;
@@ -183,8 +216,11 @@ __device__ __forceinline__ void co_store_fp8(const RowArgs& a, int row, const fl
         if (c0 + 32 * j < a.chunks) st_stream(qrow + c0 + 32 * j, codes[j]);
 }
 
-template <class E, int MODE, bool RES, int J>
-__device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, unsigned int* fault) {
+// AR: x is the all-reduce of the ranks' partial rows (rk), each copied into
+// the stage beside the residual row.
+template <class E, int MODE, bool RES, int J, bool AR = false>
+__device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, unsigned int* fault,
+                                          const ArRanks* rk = nullptr) {
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ __align__(16) float s_sum[2][32];
@@ -196,7 +232,9 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     const int c0 = warp * J * 32 + lane;   // the thread's first chunk; the others follow at strides of 32
     const int G = gridDim.x;
     const uint32_t row_bytes = static_cast<uint32_t>(a.chunks) * 16u;
-    const uint32_t stage_bytes = RES ? 2u * row_bytes : row_bytes;   // one row of x (+ residual)
+    const int nsrc = AR ? rk->n : 1;   // rows that make up x
+    // one row of x (or of each rank's partial) (+ residual)
+    const uint32_t stage_bytes = static_cast<uint32_t>(nsrc + (RES ? 1 : 0)) * row_bytes;
 
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
@@ -218,8 +256,15 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
     auto issue = [&](int row, int s) {
         unsigned char* dst = ring + (size_t)s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        bulk_g2s(dst, a.x + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
-        if constexpr (RES) bulk_g2s(dst + row_bytes, a.res + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
+        if constexpr (AR) {
+            for (int r = 0; r < nsrc; ++r)
+                bulk_g2s(dst + (size_t)r * row_bytes, rk->part[r] + (int64_t)row * a.chunks, row_bytes, &full[s],
+                         policy);
+        } else {
+            bulk_g2s(dst, a.x + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
+        }
+        if constexpr (RES)
+            bulk_g2s(dst + (size_t)nsrc * row_bytes, a.res + (int64_t)row * a.chunks, row_bytes, &full[s], policy);
     };
     if (tid == 0) {
         policy = (KEEP && !RES) ? l2_policy_evict_normal() : l2_policy_evict_first();
@@ -254,10 +299,12 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                 const int c = c0 + 32 * j;
                 uint32_t hw[4] = {0u, 0u, 0u, 0u};
                 if (ok && c < a.chunks) {
-                    const uint4 xv = sx[c];
+                    uint4 xv;
+                    if constexpr (AR) xv = ar_chunk_sum<E>(sx + c, a.chunks, nsrc);
+                    else xv = sx[c];
                     hw[0] = xv.x; hw[1] = xv.y; hw[2] = xv.z; hw[3] = xv.w;
                     if constexpr (RES) {
-                        const uint4 rv = sx[a.chunks + c];
+                        const uint4 rv = sx[(size_t)nsrc * a.chunks + c];
                         const uint32_t rs[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
                         for (int k = 0; k < 4; ++k) hw[k] = E::add2(hw[k], rs[k]);

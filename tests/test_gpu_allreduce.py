@@ -80,6 +80,49 @@ def test_dtypes_without_residual_and_ragged_hidden(dtype, R):
         _check(R, 5, H, "fp8_static", dtype=dtype, seed=H + 1)
 
 
+def _pipelined_rows():
+    """A batch that takes the pipelined kernel (from 4 rows per SM), with a ragged tail."""
+    return 4 * torch.cuda.get_device_properties(0).multi_processor_count + 37
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+def test_pipelined_kernel_modes_and_rank_counts(mode, R):
+    """From 4 rows per SM and up to 4 ranks the pipelined kernel: every
+    rank's partial row and the residual row copied into a shared-memory ring
+    stage, summed there in rank order (8 ranks: the direct kernel)."""
+    _check(R, _pipelined_rows(), 2048, mode, seed=R * 7 + 1)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("R", [3, 5])
+def test_pipelined_kernel_dtypes_without_residual_and_ragged_hidden(dtype, R):
+    n = _pipelined_rows()
+    for H in (16, 1000, 4104):
+        _check(R, n, H, "fp8_per_token", dtype=dtype, residual=False, seed=H)
+        _check(R, n, H, "fp8_static", dtype=dtype, seed=H + 1)
+    _check(R, n, 4096, "fp8_group64_row", dtype=dtype, residual=False, seed=2)
+
+
+@pytest.mark.parametrize("shape", [(0, 0, 0), (4, 1, 0), (2, 1, 1), (0, 2, 2)],
+                         ids=["default", "four-chunks-one-stage", "one-stage-one-cta-per-sm", "two-ctas-per-sm"])
+def test_pipelined_kernel_many_rows_per_cta(shape):
+    """Several rows per CTA (a wrapping ring), in place, under forced plans."""
+    J, stages, cps = shape
+    rq.set_pipeline_config(J, stages, cps, 0)
+    try:
+        _check(2, 3001, 2048, "fp8_static", in_place=True, seed=5)
+        _check(4, 1500, 4096, "nvfp4", seed=6)
+    finally:
+        rq.set_pipeline_config(0, 0, 0, 0)
+
+
+def test_rows_too_wide_for_the_ring_take_the_direct_kernel():
+    """Four ranks' rows of hidden 16384 plus the residual exceed the ring
+    budget: the direct kernel serves the batch, with the same results."""
+    _check(4, _pipelined_rows(), 16384, "fp8_group128_row", seed=9)
+
+
 def test_in_place_residual_update():
     _check(2, 64, 4096, "nvfp4", in_place=True, seed=5)
     _check(4, 64, 4096, "fp8_group64_col", in_place=True, seed=6)
