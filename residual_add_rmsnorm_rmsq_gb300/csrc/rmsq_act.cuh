@@ -36,6 +36,23 @@ __device__ __forceinline__ float ex2_approx(float a) {
     return r;
 }
 
+// The same approximation without the handling of subnormal inputs and
+// results (a single hardware instruction): identical to ex2_approx for every
+// |a| <= 0.5 (checked exhaustively on GB300), where 2^a is normal and a
+// subnormal a gives 1 either way.
+__device__ __forceinline__ float ex2_approx_ftz(float a) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+
+// rint(t) and 2^rint(t) for |t| < 2^22 without a float-to-integer conversion:
+// t + 1.5 * 2^23 lands in [2^23, 2^24), where the spacing of binary32 is 1, so
+// the addition rounds t to the nearest integer (ties to even, as rint), whose
+// value minus 1.5 * 2^23 is n and whose bit pattern is 0x4b400000 + n.
+constexpr float kRintMagic = 12582912.0f;   // 1.5 * 2^23
+__device__ __forceinline__ int rint_bits_to_int(float tm) { return __float_as_int(tm) - 0x4b400000; }
+
 // e^x for two elements.
 __device__ __forceinline__ float2 exp_cw2(float2 x) {
     const float hi_lim = 89.0f, lo_lim = -104.0f;    // e^89 > FLT_MAX; e^-104 < half the least subnormal
@@ -44,14 +61,15 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
     const float ln2_hi = 0.693145751953125f;         // 0x3f317200
     const float ln2_lo = 1.428606765330187045e-06f;  // RN(ln2 - ln2_hi)
     const float2 t = mul2_rn(xc, make_float2(log2e, log2e));
-    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 tm = add2_rn(t, make_float2(kRintMagic, kRintMagic));   // |t| < 151
+    const float2 n = add2_rn(tm, make_float2(-kRintMagic, -kRintMagic));  // rint(t)
     const float2 nn = make_float2(-n.x, -n.y);
     const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), xc));
     const float2 rl = mul2_rn(r, make_float2(log2e, log2e));
     const float2 p = make_float2(ex2_approx(rl.x), ex2_approx(rl.y));
     // 2^k = 2^ka * 2^kb with both factors normal: ka = min(k, 127), or k + 64
     // below -126; kb = k - ka (0 unless 2^k alone is out of the normal range).
-    const int k0 = __float2int_rn(n.x), k1 = __float2int_rn(n.y);
+    const int k0 = rint_bits_to_int(tm.x), k1 = rint_bits_to_int(tm.y);
     const int a0 = k0 < -126 ? k0 + 64 : min(k0, 127), a1 = k1 < -126 ? k1 + 64 : min(k1, 127);
     float2 e = mul2_rn(mul2_rn(p, make_float2(pow2_bits(a0), pow2_bits(a1))),
                        make_float2(pow2_bits(k0 - a0), pow2_bits(k1 - a1)));
@@ -63,16 +81,19 @@ __device__ __forceinline__ float2 exp_cw2(float2 x) {
 
 // e^x for two elements with |x| <= 87: the same steps as exp_cw2, where
 // nothing is clamped, 2^n is a normal binary32 (|n| <= 126) and no special
-// value arises, so the result is identical with a single scaling factor.
+// value arises, so the result is identical with a single scaling factor; the
+// reduced argument is within 0.5 + 2^-16 in magnitude, so the plain hardware
+// 2^x gives the same value as ex2_approx.
 __device__ __forceinline__ float2 exp_cw2_mid(float2 x) {
     const float log2e = 1.44269502162933349609375f, ln2_hi = 0.693145751953125f, ln2_lo = 1.428606765330187045e-06f;
     const float2 t = mul2_rn(x, make_float2(log2e, log2e));
-    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 tm = add2_rn(t, make_float2(kRintMagic, kRintMagic));
+    const float2 n = add2_rn(tm, make_float2(-kRintMagic, -kRintMagic));
     const float2 nn = make_float2(-n.x, -n.y);
     const float2 r = fma2_rn(nn, make_float2(ln2_lo, ln2_lo), fma2_rn(nn, make_float2(ln2_hi, ln2_hi), x));
     const float2 rl = mul2_rn(r, make_float2(log2e, log2e));
-    const float2 p = make_float2(ex2_approx(rl.x), ex2_approx(rl.y));
-    return mul2_rn(p, make_float2(pow2_bits(__float2int_rn(n.x)), pow2_bits(__float2int_rn(n.y))));
+    const float2 p = make_float2(ex2_approx_ftz(rl.x), ex2_approx_ftz(rl.y));
+    return mul2_rn(p, make_float2(pow2_bits(rint_bits_to_int(tm.x)), pow2_bits(rint_bits_to_int(tm.y))));
 }
 
 // 1 / x by the hardware approximation: within one ulp over the whole range
@@ -80,6 +101,15 @@ __device__ __forceinline__ float2 exp_cw2_mid(float2 x) {
 __device__ __forceinline__ float rcp_approx(float x) {
     float r;
     asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// The same without the handling of subnormal inputs and results (a single
+// hardware instruction): identical to rcp_approx for every x in [1, 2^126)
+// (checked exhaustively on GB300), which holds 1 + e^-g for |g| <= 87.
+__device__ __forceinline__ float rcp_approx_ftz(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 
@@ -92,7 +122,8 @@ template <bool MID = false>
 __device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
     const float2 e = MID ? exp_cw2_mid(make_float2(-g.x, -g.y)) : exp_cw2(make_float2(-g.x, -g.y));
     const float2 den = add2_rn(make_float2(1.0f, 1.0f), e);
-    const float2 s = mul2_rn(g, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+    const float2 s = MID ? mul2_rn(g, make_float2(rcp_approx_ftz(den.x), rcp_approx_ftz(den.y)))
+                         : mul2_rn(g, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
     return mul2_rn(s, u);
 }
 
