@@ -257,6 +257,18 @@ __device__ __forceinline__ Fp8Recips fp8_recips(float s) {
             __fmul_rn(r, 1.000003814697265625f)};      // 1 + 2^-18
 }
 
+// The same for a dynamic scale (amax / 448, at least 1e-12, at most
+// FLT_MAX / 448 < 2^120), with the single-instruction reciprocal that flushes
+// subnormal inputs and results: for every s in [2^-126, 2^126) it equals the
+// one above (checked exhaustively on GB300), and both s and 1 / s are normal
+// there.  A static scale is the caller's and may lie outside that range.
+__device__ __forceinline__ Fp8Recips fp8_recips_dyn(float s) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+    return {__fmul_rn(r, 0.999996185302734375f),       // 1 - 2^-18
+            __fmul_rn(r, 1.000003814697265625f)};      // 1 + 2^-18
+}
+
 // E4M3 codes of v[k] / s, element k in byte k, for the eight elements of a
 // chunk.  The bracketing test is applied to the whole chunk at once (one
 // branch per eight elements); the rare chunk with a code that differs between

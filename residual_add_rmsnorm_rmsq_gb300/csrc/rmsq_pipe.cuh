@@ -357,7 +357,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
             float sc = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
             if (a.e8m0) sc = pow2_ceil(sc);
             if (tid == 0) store_scale(a, row, sc);
-            const Fp8Recips r1 = fp8_recips(sc);
+            const Fp8Recips r1 = fp8_recips_dyn(sc);
             float sv[J];
             Fp8Recips rc[J];
 #pragma unroll
@@ -418,7 +418,7 @@ __device__ __forceinline__ void pipe_body(const RowArgs& a, const int stages, un
                 float sc = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
                 if (a.e8m0) sc = pow2_ceil(sc);
                 sv[j] = sc;
-                rc[j] = fp8_recips(sc);
+                rc[j] = fp8_recips_dyn(sc);
                 const int c = c0 + 32 * j;
                 if (c < a.chunks && (lane % GL) == 0) {
                     const int g = c / GL;
