@@ -198,11 +198,13 @@ __device__ __forceinline__ void compute_y(const uint32_t (&hw)[J][4], const floa
     }
 }
 
-// E4M3 codes of y / s for the thread's chunks of `row`, stored.
-template <int J>
+// E4M3 codes of y / s for the thread's chunks of `row`, stored.  DYN: s is a
+// dynamic scale (within [1e-12, 2^120)), whose reciprocal takes the
+// single-instruction form (fp8_recips_dyn).
+template <int J, bool DYN = false>
 __device__ __forceinline__ void store_fp8_codes(const RowArgs& a, int row, const float (&y)[J][8], float s,
                                                 int c0) {
-    const Fp8Recips rc = fp8_recips(s);
+    const Fp8Recips rc = DYN ? fp8_recips_dyn(s) : fp8_recips(s);
     uint2* qrow = reinterpret_cast<uint2*>(a.q + (int64_t)row * a.hidden);
     uint2 codes[J];
     if constexpr (J == 1) {
@@ -245,7 +247,7 @@ __device__ __forceinline__ void per_token_finish(const RowArgs& a, int row, cons
     float s = fmaxf(__fdiv_rn(m, 448.0f), 1e-12f);
     if (a.e8m0) s = pow2_ceil(s);
     if (tid == 0) store_scale(a, row, s);
-    store_fp8_codes<J>(a, row, y, s, tid * J);
+    store_fp8_codes<J, true>(a, row, y, s, tid * J);
 }
 
 // The quantisation of `MODE` of the fp32 values y of the thread's chunks
@@ -331,7 +333,7 @@ __device__ __forceinline__ void quantize_y(const RowArgs& a, int row, const floa
                 else store_scale(a, (int64_t)row * (a.hidden / G) + g, s);
             }
         }
-        store_fp8_codes<J>(a, row, y, s, c0);
+        store_fp8_codes<J, MODE != kFp8Static>(a, row, y, s, c0);
     }
 }
 
