@@ -189,12 +189,12 @@ inline cudaError_t set_smem_attributes(const void* fn) {
     return e;
 }
 
-inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t* err) {
+// Resident CTAs per SM of `fn` at `threads` threads and `smem` dynamic
+// shared-memory bytes (cached per device and launch shape).
+inline int occupancy_blocks(const void* fn, int threads, int smem, cudaError_t* err) {
     static std::mutex mu;
     static OccEntry cache[64];
     static int used = 0;
-    *err = set_smem_attributes(fn);
-    if (*err != cudaSuccess) return 0;
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return 0;
@@ -207,6 +207,14 @@ inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t
     if (*err != cudaSuccess) return 0;
     if (used < 64) cache[used++] = {dev, fn, smem, threads, blocks};
     return blocks;
+}
+
+// The same for a pipelined kernel, whose shared-memory attributes are set
+// first.
+inline int pipe_blocks_per_sm(const void* fn, int threads, int smem, cudaError_t* err) {
+    *err = set_smem_attributes(fn);
+    if (*err != cudaSuccess) return 0;
+    return occupancy_blocks(fn, threads, smem, err);
 }
 
 inline int sm_count(cudaError_t* err) {
@@ -424,22 +432,26 @@ cudaError_t launch_nvfp4_dynamic(const LaunchArgs& la, void* workspace, float* o
     int parts = 0;
     cudaError_t e = launch_rows<E>(first, stream, &parts);
     if (e != cudaSuccess) return e;
-    const int64_t blocks_total = (int64_t)la.n * (la.hidden / 16);
     const int sms = sm_count(&e);
     if (e != cudaSuccess) return e;
-    int64_t grid = (blocks_total + 256 * kDynUnroll - 1) / (256 * kDynUnroll);
-    if (grid > (int64_t)sms * 8) grid = (int64_t)sms * 8;
+    const void* fn = reinterpret_cast<const void*>(&nvfp4_dyn_quant_kernel<E>);
+    int per_sm = kDynCtasPerSm;
+    if (per_sm <= 0) per_sm = occupancy_blocks(fn, 256, 0, &e);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int rows_per_sweep = 0, threads = 0;
+    nvfp4_dyn_shape(la.n, la.hidden, (int64_t)sms * per_sm * 256, &rows_per_sweep, &threads);
+    const int64_t grid = ((int64_t)threads + 255) / 256;
     auto at32 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 32 == 0; };
     const uint4* h = static_cast<const uint4*>(la.res ? la.res_out : la.x);
     const uint4* w = static_cast<const uint4*>(la.w);
-    int pair = (RMSQ_PAIR_ACCESS && at32(h) && at32(w)) ? 1 : 0;
+    int pair = (RMSQ_PAIR_ACCESS && at32(h)) ? 1 : 0;
     const float* ws = static_cast<const float*>(workspace);
     uint2* q = static_cast<uint2*>(la.q);
     uint8_t* bs = static_cast<uint8_t*>(la.scales);
     int n = la.n, hidden = la.hidden;
-    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden, &pair, &parts};
-    return launch_kernel(reinterpret_cast<const void*>(&nvfp4_dyn_quant_kernel<E>), dim3((unsigned)grid),
-                         dim3(256), params, 0, stream);
+    void* params[] = {&h, &w, &ws, &q, &bs, &out_gs, &n, &hidden, &pair, &parts, &rows_per_sweep, &threads};
+    return launch_kernel(fn, dim3((unsigned)grid), dim3(256), params, 0, stream);
 }
 
 // Reads and clears this unit's pipeline fault flag (current device).
