@@ -13,8 +13,9 @@
 // Two launches and no atomics: the workspace needs no zeroing, so its
 // contents on entry do not matter.
 //
-// Pass 1 keeps h at normal L2 priority, so that pass 2, launched right after
-// it, mostly reads h from L2.
+// Pass 1 stores h at normal L2 priority (not streaming), so that pass 2,
+// launched right after it, finds a small batch's h in L2; tens of MB of h
+// (16384 rows of 2048) come back from DRAM all the same.
 //
 // The NVFP4 step follows the vLLM PR #51925 summary ("Motivation": block
 // scales and FP4 values from the normalised activations and an fp32 global
