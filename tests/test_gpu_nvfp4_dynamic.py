@@ -57,6 +57,15 @@ def test_ragged_hidden(H):
         check_dyn(ri.make_workload(f"dyn_{n}x{H}", n, H, res_sigma=1.5, seed=n + H), f"dyn_{n}x{H}")
 
 
+@pytest.mark.parametrize("n,H", [(3001, 2064), (50001, 48), (2500, 7168)])
+def test_second_pass_column_walk(n, H):
+    """The second pass gives each thread one column of 16-element blocks and
+    walks it down the rows at a stride of R rows: an odd number of blocks
+    per row (129, 3, 448) and several rows per thread, with the last pair
+    of rows ragged."""
+    check_dyn(ri.make_workload(f"walk_{n}x{H}", n, H, res_sigma=1.0, seed=n + H), f"walk_{n}x{H}")
+
+
 def test_all_zero_batch_uses_unit_global_scale():
     wl = ri.Workload("zeros", 9, 256, "bf16", 1e-6, np.zeros((9, 256), np.uint16), None,
                      ri.to_bits(np.ones(256), "bf16"))
