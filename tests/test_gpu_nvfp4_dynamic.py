@@ -66,6 +66,12 @@ def test_second_pass_column_walk(n, H):
     check_dyn(ri.make_workload(f"walk_{n}x{H}", n, H, res_sigma=1.0, seed=n + H), f"walk_{n}x{H}")
 
 
+def test_second_pass_column_walk_fp16_without_residual():
+    """The same walk over x itself (no residual) in fp16."""
+    wl = ri.make_workload("walk_fp16_nores", 5000, 2048, dtype="fp16", residual=False, seed=77)
+    check_dyn(wl, "walk_fp16_nores")
+
+
 def test_all_zero_batch_uses_unit_global_scale():
     wl = ri.Workload("zeros", 9, 256, "bf16", 1e-6, np.zeros((9, 256), np.uint16), None,
                      ri.to_bits(np.ones(256), "bf16"))
