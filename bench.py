@@ -549,17 +549,37 @@ def _oracle_scale_in(wl, mode, scale_in):
     return scale_in if scale_in is not None else (wl.static_scale if mode == "fp8_static" else 0.0)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(wl, mode, scale_in=None, budget_s: float = 20.0) -> dict:
     """The oracle as it stands, row-parallel over the process's cores, on a
-    bounded prefix of the workload's rows; median of 3 runs."""
+    bounded prefix of the workload's rows; median of 3 runs.  Beside it, the
+    same oracle on one thread over a prefix of 1/cores as many rows."""
     import oracle
     cores = len(os.sched_getaffinity(0))
     scale = _oracle_scale_in(wl, mode, scale_in)
     rows = min(wl.n_tokens, 256)
 
-    def run(rows):
+    def run(rows, threads=cores):
         oracle.run(wl.x[:rows], None if wl.residual is None else wl.residual[:rows], wl.weight,
-                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=cores)
+                   eps=wl.eps, mode=mode, scale_in=scale, dtype=wl.dtype, nthreads=threads)
 
     while True:
         t = time.perf_counter()
@@ -575,9 +595,20 @@ def cpu_baseline(wl, mode, scale_in=None, budget_s: float = 20.0) -> dict:
         times.append(time.perf_counter() - t)
     med = statistics.median(times)
     nbytes = algorithmic_bytes(mode, rows, wl.hidden, 2, wl.residual is not None)
+    rows1 = max(1, rows // cores)
+    times1 = []
+    for _ in range(3):
+        t = time.perf_counter()
+        run(rows1, 1)
+        times1.append(time.perf_counter() - t)
+    med1 = statistics.median(times1)
+    nbytes1 = algorithmic_bytes(mode, rows1, wl.hidden, 2, wl.residual is not None)
     return {"value": round(nbytes / med / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "tokens_per_s": round(rows / med, 1),
-            "sample": f"first {rows} of {wl.n_tokens} rows, median of 3 runs, {cores} threads"}
+            "sample": f"first {rows} of {wl.n_tokens} rows, median of 3 runs, {cores} threads",
+            "cpu": cpu_model(),
+            "single_thread": {"value": round(nbytes1 / med1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"first {rows1} rows, median of 3 runs, 1 thread"}}
 
 
 def parity_vs_oracle(wl, mode, scale_in, got: dict) -> dict:
@@ -654,7 +685,8 @@ def run_reference(args, rank, world):
         "data": "synthetic", "tokens_per_s": round(rows / dt, 1),
         "config": workload_config(args.workload, wl, mode),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"first {rows} of {wl.n_tokens} rows per step (host cores, no GPU)"},
+                         "sample": f"first {rows} of {wl.n_tokens} rows per step (host cores, no GPU)",
+                         "cpu": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
