@@ -2,7 +2,8 @@
 // per thread J, variant).  Included once per activation type.
 //
 //  direct:    one CTA per row, ceil(hidden / 8 / J) threads (J = 1 up to
-//             hidden 8192, else 2), loads straight into registers.
+//             hidden 8192, else 2; also 2 when the rows would not all be
+//             resident at once with J = 1), loads straight into registers.
 //  pipelined: persistent CTAs (as many as fit on the SMs), `stages` rows of
 //             x / residual in flight per CTA through the shared-memory ring.
 //             The per-row dependency chain (block reductions, IEEE divide
@@ -193,7 +194,8 @@ inline cudaError_t set_smem_attributes(const void* fn) {
 // shared-memory bytes (cached per device and launch shape).
 inline int occupancy_blocks(const void* fn, int threads, int smem, cudaError_t* err) {
     static std::mutex mu;
-    static OccEntry cache[64];
+    constexpr int kCache = 256;   // more than the launch shapes in use; beyond it, queried per call
+    static OccEntry cache[kCache];
     static int used = 0;
     int dev = 0;
     *err = cudaGetDevice(&dev);
@@ -205,7 +207,7 @@ inline int occupancy_blocks(const void* fn, int threads, int smem, cudaError_t* 
     int blocks = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, smem);
     if (*err != cudaSuccess) return 0;
-    if (used < 64) cache[used++] = {dev, fn, smem, threads, blocks};
+    if (used < kCache) cache[used++] = {dev, fn, smem, threads, blocks};
     return blocks;
 }
 
@@ -355,13 +357,32 @@ cudaError_t plan_rows(const LaunchArgs& la, const RowArgs& a, RowLaunch* out) {
     out->pipe = la.variant == kVariantPipelined ||
                 (la.variant == kVariantAuto && a.n >= kPipeMinRowsPerSm * sms);
     if (!out->pipe) {
+        auto threads_for = [&](int j) { return ((a.chunks + j - 1) / j + 31) / 32 * 32; };
         out->J = a.chunks <= 1024 ? 1 : 2;
-        out->threads = ((a.chunks + out->J - 1) / out->J + 31) / 32 * 32;
         out->fn = pick_kernel<E>(la.mode, res, false, out->J);
+        if (!out->fn) return cudaErrorInvalidValue;
+        if (out->J == 1 && a.chunks >= 2) {
+            // One CTA per row: when the rows do not all fit on the SMs at once
+            // with one chunk per thread, two chunks per thread (half the
+            // threads, so more CTAs per SM) finish in fewer waves.
+            const int per_sm1 = occupancy_blocks(out->fn, threads_for(1), 0, &err);
+            if (err != cudaSuccess) return err;
+            if ((int64_t)a.n > (int64_t)per_sm1 * sms) {
+                const void* f2 = pick_kernel<E>(la.mode, res, false, 2);
+                if (!f2) return cudaErrorInvalidValue;
+                const int per_sm2 = occupancy_blocks(f2, threads_for(2), 0, &err);
+                if (err != cudaSuccess) return err;
+                if (per_sm2 > per_sm1) {
+                    out->J = 2;
+                    out->fn = f2;
+                }
+            }
+        }
+        out->threads = threads_for(out->J);
         out->grid = a.n;
         out->smem = 0;
         out->stages = 0;
-        return out->fn ? cudaSuccess : cudaErrorInvalidValue;
+        return cudaSuccess;
     }
     const PipeTuning tune = get_pipe_tuning();
     PipePlan p = pipe_plan(a, res);
