@@ -361,21 +361,23 @@ cudaError_t plan_rows(const LaunchArgs& la, const RowArgs& a, RowLaunch* out) {
         out->J = a.chunks <= 1024 ? 1 : 2;
         out->fn = pick_kernel<E>(la.mode, res, false, out->J);
         if (!out->fn) return cudaErrorInvalidValue;
-        if (out->J == 1 && a.chunks >= 2) {
-            // One CTA per row: when the rows do not all fit on the SMs at once
-            // with one chunk per thread, two chunks per thread (half the
-            // threads, so more CTAs per SM) finish in fewer waves.
+        if (out->J == 1 && a.chunks >= 2 && a.n > sms) {
+            // One CTA per row (measured on GB300, 256 rows of hidden 8192):
+            // when the rows do not all fit on the SMs at once with one chunk
+            // per thread, two chunks per thread (half the threads, so more
+            // CTAs per SM) finish in fewer waves; without a residual they
+            // are also faster once SMs hold two rows (static and group
+            // scales 7-10 %; with a residual the same or 2 % slower).
             const int per_sm1 = occupancy_blocks(out->fn, threads_for(1), 0, &err);
             if (err != cudaSuccess) return err;
-            if ((int64_t)a.n > (int64_t)per_sm1 * sms) {
-                const void* f2 = pick_kernel<E>(la.mode, res, false, 2);
-                if (!f2) return cudaErrorInvalidValue;
-                const int per_sm2 = occupancy_blocks(f2, threads_for(2), 0, &err);
-                if (err != cudaSuccess) return err;
-                if (per_sm2 > per_sm1) {
-                    out->J = 2;
-                    out->fn = f2;
-                }
+            const void* f2 = pick_kernel<E>(la.mode, res, false, 2);
+            if (!f2) return cudaErrorInvalidValue;
+            const int per_sm2 = occupancy_blocks(f2, threads_for(2), 0, &err);
+            if (err != cudaSuccess) return err;
+            const bool waves = (int64_t)a.n > (int64_t)per_sm1 * sms && per_sm2 > per_sm1;
+            if (waves || (!res && per_sm2 >= per_sm1)) {
+                out->J = 2;
+                out->fn = f2;
             }
         }
         out->threads = threads_for(out->J);
