@@ -56,18 +56,28 @@ static __device__ unsigned int g_pipe_fault;
 // Register budget of the pipelined kernel by chunks per thread (compile-time
 // tuning, results do not depend on it): with four chunks per thread the
 // natural allocation (~86) leaves five 128-thread CTAs per SM; 80 gives six.
+// NVFP4 with two chunks per thread: 64 (from ~68) lets eight 128-thread CTAs
+// share an SM instead of seven (Qwen3-shaped layer, hidden 2048, 16384
+// rows: 36.1 -> 35.1 us); the FP8 modes at two chunks per thread were 3-5 %
+// slower under that cap (hidden 4096), so they keep the natural allocation.
 #ifndef RMSQ_PIPE_MAXNREG_J4
 #define RMSQ_PIPE_MAXNREG_J4 80
 #endif
 #ifndef RMSQ_PIPE_MAXNREG_J8
 #define RMSQ_PIPE_MAXNREG_J8 128
 #endif
+#ifndef RMSQ_PIPE_MAXNREG_NVFP4_J2
+#define RMSQ_PIPE_MAXNREG_NVFP4_J2 64
+#endif
 template <int J> constexpr int pipe_maxnreg() {
     return J == 4 ? RMSQ_PIPE_MAXNREG_J4 : J == 8 ? RMSQ_PIPE_MAXNREG_J8 : 128;
 }
+template <int MODE, int J> constexpr int pipe_mode_maxnreg() {
+    return (MODE == kNvfp4 && J == 2) ? RMSQ_PIPE_MAXNREG_NVFP4_J2 : pipe_maxnreg<J>();
+}
 
 template <class E, int MODE, bool RES, int J>
-__global__ void __launch_bounds__(kPipeMaxThreads) __maxnreg__(pipe_maxnreg<J>())
+__global__ void __launch_bounds__(kPipeMaxThreads) __maxnreg__((pipe_mode_maxnreg<MODE, J>()))
 pipe_entry(const RowArgs a, const int stages) {
     pipe_body<E, MODE, RES, J>(a, stages, &g_pipe_fault);
 }
