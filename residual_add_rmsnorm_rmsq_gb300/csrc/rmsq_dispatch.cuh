@@ -56,10 +56,11 @@ static __device__ unsigned int g_pipe_fault;
 // Register budget of the pipelined kernel by chunks per thread (compile-time
 // tuning, results do not depend on it): with four chunks per thread the
 // natural allocation (~86) leaves five 128-thread CTAs per SM; 80 gives six.
-// NVFP4 with two chunks per thread: 64 (from ~68) lets eight 128-thread CTAs
-// share an SM instead of seven (Qwen3-shaped layer, hidden 2048, 16384
-// rows: 36.1 -> 35.1 us); the FP8 modes at two chunks per thread were 3-5 %
-// slower under that cap (hidden 4096), so they keep the natural allocation.
+// NVFP4 with two chunks per thread: a cap of 64 (the allocation drops from
+// 68 to 56) lets nine 128-thread CTAs share an SM instead of seven
+// (Qwen3-shaped layer, hidden 2048, 16384 rows: 36.1 -> 35.3 us); the FP8
+// modes at two chunks per thread were 3-5 % slower under that cap (hidden
+// 4096), so they keep the natural allocation.
 #ifndef RMSQ_PIPE_MAXNREG_J4
 #define RMSQ_PIPE_MAXNREG_J4 80
 #endif
